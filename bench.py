@@ -1,0 +1,435 @@
+"""Benchmark of the block-quantized GEMV on GB300.
+
+One step is one pass of the whole product over one activation: quantize_act
+(the activation quantized per 256-element block under m*2^e) and q_gemv (the
+Q4_K-like 4096x4096 matrix times it: exact block sums, once-rounded block
+values, in-order row fold) -- the workload the headline metric is quoted on.
+Weights are seeded synthetic data with the format's distributions; each step
+reads a different copy of the matrix, and the copies total more than 4x the
+L2, so every step streams its weights from HBM.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+                  [--workload q4k_4096x4096|q8_0_512x1024|q6k_14336x4096|f16_49152x576]
+
+Prints one JSON line.  --impl reference times the CPU oracle (test
+infrastructure; a deliberately plain scalar C program) on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from block_quantized_weight_quantize_gb300 import synth  # noqa: E402
+
+L2_BYTES = 129 * 1024 * 1024
+WORKLOADS = {
+    # name: (fmt, rows, K, ncols, seed, outlier fraction, description)
+    "q4k_4096x4096": (synth.FMT_Q4K, 4096, 4096, 1, 1, 0.001,
+                      "Q4_K-like GEMV 4096x4096, batch 1, activation N(0,1) with 0.1% outliers x50"),
+    "q8_0_512x1024": (synth.FMT_Q8_0, 512, 1024, 1, 0, 0.0, "Q8_0 GEMV 512x1024, batch 1"),
+    "q6k_14336x4096": (synth.FMT_Q6K, 14336, 4096, 1, 2, 0.0, "Q6_K-like FFN gate 14336x4096, batch 1"),
+    "f16_49152x576": (synth.FMT_F16, 49152, 576, 1, 3, 0.0, "F16 tied-embedding logits 49152x576, batch 1"),
+    "q4k_4096x4096_b16": (synth.FMT_Q4K, 4096, 4096, 16, 1, 0.001, "Q4_K-like GEMV 4096x4096, 16 columns"),
+}
+
+
+def kernel_sources_sha() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "block_quantized_weight_quantize_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in self.lines:
+            f = [t.strip() for t in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": ["no samples"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def algorithmic_bytes(fmt, rows, K, ncols):
+    """Weights + activation (codes, 4-B block scales, 2-B unit sums) + outputs."""
+    wb = synth.weight_bytes(fmt, rows, K)
+    if fmt == synth.FMT_F16:
+        return wb, wb + ncols * 2 * K + 4 * rows * ncols
+    blk = synth.BLOCK[fmt]
+    return wb, wb + ncols * (K + 4 * (K // blk) + 2 * (K // 16)) + 4 * rows * ncols
+
+
+# ---------------------------------------------------------------- our arm
+
+def run_ours(args, rank, world):
+    import torch
+    import block_quantized_weight_quantize_gb300 as qb
+
+    fmt, rows, K, ncols, seed, outl, desc = WORKLOADS[args.workload]
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    rng = np.random.default_rng(seed + 1000 * rank)
+    lg = synth.draw(fmt, rng, rows, K)
+    Wh = synth.pack(fmt, lg)
+    x = synth.draw_act(rng, ncols, K, outlier_frac=outl)
+    wbytes, abytes = algorithmic_bytes(fmt, rows, K, ncols)
+    ncopy = max(2, -(-4 * L2_BYTES // wbytes))        # copies totalling >= 4x L2
+    W = torch.empty((ncopy, Wh.size), dtype=torch.uint8, device=dev)
+    W[0].copy_(torch.from_numpy(Wh))
+    for i in range(1, ncopy):
+        W[i].copy_(W[0])
+    xd = torch.from_numpy(x).to(dev)
+    out = torch.empty((ncols, rows), dtype=torch.float32, device=dev)
+    if fmt == synth.FMT_F16:
+        act = torch.empty((ncols, K), dtype=torch.int16, device=dev)
+    else:
+        act = qb.alloc_act(ncols, K, synth.BLOCK[fmt], dev)
+    stream = torch.cuda.Stream(dev)
+
+    def step(i, s):
+        qb.matvec(fmt, W[i % ncopy], rows, K, xd, out=out, act=act, stream=s)
+
+    def gemv_only(i, s):
+        if fmt == synth.FMT_F16:
+            qb.q_gemv_f16(W[i % ncopy], rows, K, act, ncols, out, s)
+        else:
+            qb.q_gemv(fmt, W[i % ncopy], rows, K, act, ncols, out, s)
+
+    # eager warm-up (also loads the kernels), then graphs of G steps each
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            step(i, stream)
+    stream.synchronize()
+    G = min(args.steps, 1000)
+
+    def capture(fn, n):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            g.capture_begin()
+            for i in range(n):
+                fn(i, stream)
+            g.capture_end()
+        return g
+
+    g_main = capture(step, G)
+    rem = args.steps % G
+    g_rem = capture(step, rem) if rem else None
+    g_w = capture(step, max(1, min(args.warmup, G)))
+
+    def replay_steps(n_full, g_tail):
+        for _ in range(n_full):
+            g_main.replay()
+        if g_tail is not None:
+            g_tail.replay()
+
+    # warm-up: W steps
+    with torch.cuda.stream(stream):
+        for _ in range(max(1, args.warmup // max(1, min(args.warmup, G)))):
+            g_w.replay()
+    stream.synchronize()
+
+    dist = world > 1
+    if dist:
+        import torch.distributed as tdist
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev.index) as clk:
+        if dist:
+            tdist.barrier()
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            replay_steps(args.steps // G, g_rem)
+            e1.record(stream)
+        torch.cuda.synchronize()
+        if dist:
+            tdist.barrier()
+    ms = e0.elapsed_time(e1)
+    if dist:
+        t = torch.tensor([ms], device=dev)
+        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+        ms = float(t.item())
+    clocks = clk.summary()
+
+    # ---- roofline: the product kernel alone, live, over rotating copies
+    n_roof = 2000
+    g_roof = capture(gemv_only, n_roof)
+    with torch.cuda.stream(stream):
+        g_roof.replay()
+        e0.record(stream)
+        for _ in range(3):
+            g_roof.replay()
+        e1.record(stream)
+    stream.synchronize()
+    per_launch_s = e0.elapsed_time(e1) / 1e3 / (3 * n_roof)
+    peak, peak_kind = measured_peaks()
+    achieved = abytes / per_launch_s / 1e9
+    traffic = None
+    tp = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tp):
+        tj = json.load(open(tp))
+        ent = tj.get(args.workload)
+        if ent and ent.get("src_sha") == kernel_sources_sha():
+            traffic = ent.get("dram_bytes_per_launch")
+
+    # ---- e2e: the public binding with host buffers, copies inside the timed region
+    xh = torch.from_numpy(x).pin_memory()
+    oh = torch.empty((ncols, rows), dtype=torch.float32).pin_memory()
+    n_e2e = min(args.steps, 3000)
+    for i in range(5):
+        with torch.cuda.stream(stream):
+            xd.copy_(xh, non_blocking=True)
+            step(i, stream)
+            oh.copy_(out, non_blocking=True)
+    stream.synchronize()
+    if dist:
+        tdist.barrier()
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for i in range(n_e2e):
+            xd.copy_(xh, non_blocking=True)
+            step(i, stream)
+            oh.copy_(out, non_blocking=True)
+    stream.synchronize()
+    e2e_s = time.perf_counter() - t0
+    if dist:
+        t = torch.tensor([e2e_s], device=dev)
+        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+        e2e_s = float(t.item())
+
+    assert qb.q_device_status() == qb.QB_OK
+    step_s = ms / 1e3 / args.steps
+    value = world * wbytes / step_s / 1e9
+    res = {
+        "metric": "weight GB/s at batch 1 (Q4_K-like GEMV 4096x4096, rows/s and fraction of 8 TB/s alongside)"
+        if args.workload == "q4k_4096x4096" else f"weight GB/s ({desc})",
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms / args.steps, 6),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "int8 codes x int8 codes, exact int32/int64, f32 rounding" if fmt != synth.FMT_F16 else "f16 x f16, f32",
+        "data": "synthetic (seeded PCG64; the format's code/scale distributions); no trained weights",
+        "config": {
+            "workload": desc,
+            "rows": rows, "K": K, "ncols": ncols,
+            "format": synth.FORMAT_NAMES[fmt],
+            "weight_bytes_per_step": wbytes,
+            "l2": f"each step reads a different one of {ncopy} weight copies ({ncopy * wbytes / 2**20:.0f} MiB "
+                  f"> 4x L2); no flush",
+            "timing": f"CUDA graphs of {G} steps (quantize_act + q_gemv, programmatic dependent launch) "
+                      f"replayed; CUDA events on the launching stream",
+            "parallelism": "replicas" if world > 1 else "single GPU",
+        },
+        "rows_per_s": round(world * rows / step_s, 1),
+        "frac_of_8tbs": round(value / 8000.0, 4),
+        "frac_of_measured_copy": round(value / peak, 4),
+        "gpu_launches": 2 * args.steps,
+        "clocks": clocks,
+        "roofline": {
+            "bound": "hbm",
+            "kernel": f"gemv_kernel<{synth.FORMAT_NAMES[fmt]}, {ncols}>" if fmt != synth.FMT_F16 else "gemv_f16_kernel",
+            "achieved": round(achieved, 1),
+            "peak": peak,
+            "peak_kind": f"{peak_kind} (HBM copy, burst)",
+            "unit": "GB/s",
+            "frac": round(achieved / peak, 4),
+            "traffic": traffic,
+            "algorithmic_bytes_per_launch": abytes,
+            "avg_launch_us": round(per_launch_s * 1e6, 4),
+            "launches_timed": 3 * n_roof,
+        },
+        "e2e": {
+            "value": round(world * wbytes * n_e2e / e2e_s / 1e9, 2),
+            "unit": "GB/s",
+            "h2d_bytes_per_step": int(x.nbytes),
+            "d2h_bytes_per_step": int(4 * rows * ncols),
+            "steps": n_e2e,
+            "how": "per step: pinned x -> device, quantize_act + q_gemv through the Python binding, out -> "
+                   "pinned host; host wall clock over all steps",
+        },
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline(fmt, rows, K, ncols, Wh, x, wbytes, budget_s=args.cpu_seconds)
+    return res
+
+
+# ---------------------------------------------------------------- the oracle on the host
+
+def _oracle_threads():
+    return max(1, os.cpu_count() or 1)
+
+
+def oracle_pass(fmt, rows, K, Wh, x, nthreads, row_limit=None):
+    """quantize + product over (a sample of) rows, rows split across threads
+    (ctypes releases the GIL; the oracle is reentrant)."""
+    import concurrent.futures as cf
+    import oracle
+    r_end = rows if row_limit is None else min(rows, row_limit)
+    if fmt == synth.FMT_F16:
+        x16 = oracle.quantize_f16(x)
+        W16 = Wh.view(np.uint16).reshape(rows, K)[:r_end]
+        chunks = np.array_split(np.arange(r_end), nthreads)
+        with cf.ThreadPoolExecutor(nthreads) as ex:
+            list(ex.map(lambda c: oracle.gemv_f16(np.ascontiguousarray(W16[c]), len(c), K, x16)
+                        if len(c) else None, chunks))
+        return r_end
+    codes, m, e, _ = oracle.quantize_blocks(x, synth.BLOCK[fmt])
+    out = np.zeros((x.shape[0], rows), np.float32)
+    bounds = np.linspace(0, r_end, nthreads + 1).astype(int)
+    with cf.ThreadPoolExecutor(nthreads) as ex:
+        list(ex.map(lambda i: oracle.gemv(fmt, Wh, rows, K, codes, m, e, int(bounds[i]), int(bounds[i + 1]), out),
+                    range(nthreads)))
+    return r_end
+
+
+def cpu_baseline(fmt, rows, K, ncols, Wh, x, wbytes, budget_s=10.0):
+    n = _oracle_threads()
+    oracle_pass(fmt, rows, K, Wh, x, n)          # warm (also builds the oracle if needed)
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle_pass(fmt, rows, K, Wh, x, n)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    return {"value": round(wbytes * reps / el / 1e9, 4), "unit": "GB/s", "cores": n, "kind": "oracle",
+            "sample": f"{reps} full passes (quantize + all {rows} rows) in {el:.1f} s, rows split over {n} "
+                      f"threads of the scalar C oracle"}
+
+
+def run_reference(args):
+    fmt, rows, K, ncols, seed, outl, desc = WORKLOADS[args.workload]
+    rng = np.random.default_rng(seed)
+    lg = synth.draw(fmt, rng, rows, K)
+    Wh = synth.pack(fmt, lg)
+    x = synth.draw_act(rng, ncols, K, outlier_frac=outl)
+    n = _oracle_threads()
+    # size each step's row sample so the whole run stays within ~2 minutes
+    t0 = time.perf_counter()
+    oracle_pass(fmt, rows, K, Wh, x, n)
+    full = time.perf_counter() - t0
+    budget = 100.0 / max(1, args.steps + args.warmup)
+    rows_s = int(max(1, min(rows, rows * budget / max(full, 1e-6))))
+    for _ in range(args.warmup):
+        oracle_pass(fmt, rows, K, Wh, x, n, rows_s)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_pass(fmt, rows, K, Wh, x, n, rows_s)
+    el = time.perf_counter() - t0
+    rec = synth.record_bytes(fmt, K)
+    value = rec * rows_s * args.steps / el / 1e9
+    sample = f"each step: quantize + {rows_s} of {rows} rows, split over {n} threads of the scalar C oracle"
+    return {
+        "impl": "reference",
+        "metric": "weight GB/s at batch 1 (Q4_K-like GEMV 4096x4096, rows/s and fraction of 8 TB/s alongside)"
+        if args.workload == "q4k_4096x4096" else f"weight GB/s ({desc})",
+        "value": round(value, 4), "unit": "GB/s", "n_gpus": 0, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(el * 1e3 / args.steps, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "int64/int128 exact, f32 rounding (scalar C)",
+        "data": "synthetic (seeded PCG64)", "config": {"workload": desc, "rows": rows, "K": K, "ncols": ncols},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": n, "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100000)
+    ap.add_argument("--warmup", type=int, default=1000)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="q4k_4096x4096", choices=sorted(WORKLOADS))
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as tdist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        tdist.init_process_group("nccl")
+    res = run_ours(args, rank, world)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as tdist
+        tdist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

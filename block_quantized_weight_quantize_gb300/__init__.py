@@ -1,6 +1,174 @@
 """Block-quantized weight x quantized activation GEMV for GB300 (sm_103a).
 
-The compute path is the C-ABI library ``libqgemv.so`` (CUDA kernels); this
-package is its thin Python binding.  Importing the package does not load the
-library; the first call does, and fails loudly if it is missing.
+The compute path is the C-ABI library ``libqgemv.so`` (hand-written CUDA
+kernels; declared in ``include/qgemv.h``).  This module is its thin Python
+binding: it marshals torch tensors (device memory, streams) into the C calls
+and raises on a non-zero status.  Every step of the product runs in the
+library's kernels.  Importing the package does not load the library; the
+first call does, and raises if it is missing -- there is no fallback.
+
+Layouts are those of ``include/qgemv.h``: weights as bytes (uint8 tensors of
+``q_weight_bytes`` bytes, or uint16 [rows, K] for F16); activation codes int8
+[ncols, K], scales int32 [ncols, K/block] (each the 4-byte struct {m u8, pad
+u8, e i16}), unit sums int16 [ncols, K/16]; outputs f32 [ncols, rows].
 """
+from __future__ import annotations
+
+import ctypes
+import os
+
+F16, Q8_0, Q4K, Q6K = 1, 8, 12, 14
+BLOCK = {Q8_0: 32, Q4K: 256, Q6K: 256}
+FORMATS = {"f16": F16, "q8_0": Q8_0, "q4k": Q4K, "q6k": Q6K}
+
+QB_OK, QB_E_ARG, QB_E_FORMAT, QB_E_BLOCK, QB_E_CUDA, QB_E_UNREADABLE, QB_E_DEVICE = 0, -1, -2, -3, -4, -5, -6
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libqgemv.so")
+
+# every entry point include/qgemv.h declares
+EXPORTS = ("quantize_act", "q_gemv", "quantize_act_f16", "q_gemv_f16", "q_check_weights", "q_weight_bytes",
+           "q_block_values", "q_device_status", "q_strerror")
+
+
+class QbError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {strerror(status)} ({status})")
+
+
+class _Act(ctypes.Structure):
+    _fields_ = [("block", ctypes.c_int), ("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p),
+                ("sums16", ctypes.c_void_p)]
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded C-ABI library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with __graft_entry__.build() "
+                               "(there is no non-CUDA fallback)")
+        L = ctypes.CDLL(LIB_PATH)
+        P, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+        L.quantize_act.argtypes, L.quantize_act.restype = [i32, P, i64, i32, P, P, P, P], i32
+        L.q_gemv.argtypes, L.q_gemv.restype = [i32, P, i64, i64, ctypes.POINTER(_Act), i32, P, P], i32
+        L.quantize_act_f16.argtypes, L.quantize_act_f16.restype = [P, i64, i32, P, P], i32
+        L.q_gemv_f16.argtypes, L.q_gemv_f16.restype = [P, i64, i64, P, i32, P, P], i32
+        L.q_check_weights.argtypes, L.q_check_weights.restype = [i32, P, i64, i64, P], i32
+        L.q_weight_bytes.argtypes, L.q_weight_bytes.restype = [i32, i64, i64], i64
+        L.q_block_values.argtypes = [i32, P, i64, i64, ctypes.POINTER(_Act), i32, P, P, P, P]
+        L.q_block_values.restype = i32
+        L.q_device_status.argtypes, L.q_device_status.restype = [P], i32
+        L.q_strerror.argtypes, L.q_strerror.restype = [i32], ctypes.c_char_p
+        _lib = L
+    return _lib
+
+
+def strerror(status: int) -> str:
+    return lib().q_strerror(status).decode()
+
+
+def _check(rc: int, where: str):
+    if rc != QB_OK:
+        raise QbError(rc, where)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _stream(stream):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+# ------------------------------------------------------------------ activations
+
+def alloc_act(ncols: int, K: int, block: int, device="cuda"):
+    """Device buffers (codes, scales, sums16) for a quantized activation."""
+    import torch
+    codes = torch.empty((ncols, K), dtype=torch.int8, device=device)
+    scales = torch.empty((ncols, K // block), dtype=torch.int32, device=device)
+    sums16 = torch.empty((ncols, K // 16), dtype=torch.int16, device=device)
+    return codes, scales, sums16
+
+
+def quantize_act(block: int, x, codes, scales, sums16, stream=None) -> None:
+    """quantize_blocks under PerBlock: x f32 [ncols, K] -> codes, scales, sums16."""
+    ncols, K = x.shape
+    _check(lib().quantize_act(block, _ptr(x), K, ncols, _ptr(codes), _ptr(scales), _ptr(sums16), _stream(stream)),
+           "quantize_act")
+
+
+def _act(block, codes, scales, sums16):
+    return _Act(block, codes.data_ptr(), scales.data_ptr(), sums16.data_ptr() if sums16 is not None else 0)
+
+
+def q_gemv(fmt: int, W, rows: int, K: int, act, ncols: int, out, stream=None) -> None:
+    """dot under PerBlock for every row and column: out f32 [ncols, rows].
+    act = (codes, scales, sums16) as written by quantize_act."""
+    codes, scales, sums16 = act
+    a = _act(BLOCK[fmt], codes, scales, sums16)
+    _check(lib().q_gemv(fmt, _ptr(W), rows, K, ctypes.byref(a), ncols, _ptr(out), _stream(stream)), "q_gemv")
+
+
+def q_block_values(fmt: int, W, rows: int, K: int, act, ncols: int, C=None, O=None, v=None, stream=None) -> None:
+    codes, scales, sums16 = act
+    a = _act(BLOCK[fmt], codes, scales, sums16)
+    _check(lib().q_block_values(fmt, _ptr(W), rows, K, ctypes.byref(a), ncols, _ptr(C), _ptr(O), _ptr(v),
+                                _stream(stream)), "q_block_values")
+
+
+def quantize_act_f16(x, x16, stream=None) -> None:
+    ncols, K = x.shape
+    _check(lib().quantize_act_f16(_ptr(x), K, ncols, _ptr(x16), _stream(stream)), "quantize_act_f16")
+
+
+def q_gemv_f16(W, rows: int, K: int, x16, ncols: int, out, stream=None) -> None:
+    _check(lib().q_gemv_f16(_ptr(W), rows, K, _ptr(x16), ncols, _ptr(out), _stream(stream)), "q_gemv_f16")
+
+
+def q_check_weights(fmt: int, W, rows: int, K: int, stream=None) -> int:
+    """QB_OK, or QB_E_UNREADABLE if a block scale is inf/NaN (synchronizes)."""
+    rc = lib().q_check_weights(fmt, _ptr(W), rows, K, _stream(stream))
+    if rc not in (QB_OK, QB_E_UNREADABLE):
+        raise QbError(rc, "q_check_weights")
+    return rc
+
+
+def q_weight_bytes(fmt: int, rows: int, K: int) -> int:
+    n = lib().q_weight_bytes(fmt, rows, K)
+    if n < 0:
+        raise QbError(int(n), "q_weight_bytes")
+    return int(n)
+
+
+def q_device_status(stream=None) -> int:
+    return lib().q_device_status(_stream(stream))
+
+
+# ------------------------------------------------------------------ one call
+
+def matvec(fmt: int, W, rows: int, K: int, x, out=None, act=None, stream=None):
+    """quantize_act then q_gemv (or quantize_act_f16 then q_gemv_f16): x f32
+    [ncols, K] on the device -> out f32 [ncols, rows].  `act` may pass
+    preallocated activation buffers (from alloc_act, or a uint16 [ncols, K]
+    tensor for F16)."""
+    import torch
+    ncols = x.shape[0]
+    if out is None:
+        out = torch.empty((ncols, rows), dtype=torch.float32, device=x.device)
+    if fmt == F16:
+        x16 = act if act is not None else torch.empty((ncols, K), dtype=torch.int16, device=x.device)
+        quantize_act_f16(x, x16, stream)
+        q_gemv_f16(W, rows, K, x16, ncols, out, stream)
+        return out
+    act = act if act is not None else alloc_act(ncols, K, BLOCK[fmt], x.device)
+    quantize_act(BLOCK[fmt], x, *act, stream=stream)
+    q_gemv(fmt, W, rows, K, act, ncols, out, stream)
+    return out

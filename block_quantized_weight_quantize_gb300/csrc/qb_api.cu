@@ -1,0 +1,242 @@
+// qb_api.cu -- the extern "C" entry points declared in include/qgemv.h:
+// argument checks on the host, then one launch per call on the caller's
+// stream.  Also the weight-scale scan (numerics page, reads / Unreadable) and
+// the device fault word.
+#include <cstdint>
+#include <algorithm>
+#include <cstring>
+
+#include "qb_common.cuh"
+#include "qb_launch.h"
+
+namespace qb {
+
+__device__ int g_fault = 0;
+__device__ int g_unreadable = 0;
+
+int *fault_word() {
+    static int *cache[64] = {nullptr};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    if (!cache[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_fault) != cudaSuccess) return nullptr;
+        cache[dev] = static_cast<int *>(p);
+    }
+    return cache[dev];
+}
+
+int num_sms() {
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    if (cache[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
+// One thread per weight block: an f16 scale with exponent field 31 (inf/NaN).
+__global__ void check_weights_kernel(const uint8_t *__restrict__ W, int64_t rows, int64_t nb, int64_t rec,
+                                     int fmt, int64_t K) {
+    pdl_launch_dependents();
+    pdl_wait();
+    const int64_t n = rows * nb;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t r = i / nb, b = i - r * nb;
+        const uint8_t *rp = W + r * rec;
+        uint32_t bad = 0;
+        if (fmt == kQ8_0) {
+            const uint32_t h = rp[K + 2 * b] | (rp[K + 2 * b + 1] << 8);
+            bad = ((h >> 10) & 31) == 31;
+        } else if (fmt == kQ4K) {
+            const uint32_t w = *reinterpret_cast<const uint32_t *>(rp + 144 * b);
+            bad = (((w >> 10) & 31) == 31) | (((w >> 26) & 31) == 31);
+        } else {
+            const uint32_t h = rp[208 * nb + 2 * b] | (rp[208 * nb + 2 * b + 1] << 8);
+            bad = ((h >> 10) & 31) == 31;
+        }
+        if (bad) atomicOr(&g_unreadable, 1);
+    }
+}
+
+int launch_check_weights(int fmt, const void *W, int64_t rows, int64_t K, int *flag, cudaStream_t stream) {
+    const int64_t nb = K / fmt_block(fmt), rec = record_bytes(fmt, K);
+    const int64_t n = rows * nb;
+    const unsigned grid = (unsigned)std::min<int64_t>((n + 255) / 256, (int64_t)num_sms() * 8);
+    int zero = 0;
+    if (cudaMemcpyToSymbolAsync(g_unreadable, &zero, sizeof(int), 0, cudaMemcpyHostToDevice, stream) != cudaSuccess)
+        return QB_E_CUDA;
+    int rc = launch_pdl(check_weights_kernel, dim3(grid), dim3(256), 0, stream, static_cast<const uint8_t *>(W),
+                        rows, nb, rec, fmt, K);
+    if (rc) return rc;
+    if (cudaMemcpyFromSymbolAsync(flag, g_unreadable, sizeof(int), 0, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+        return QB_E_CUDA;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return QB_E_CUDA;
+    return QB_OK;
+}
+
+static int fmt_index(qb_fmt f) {
+    switch (f) {
+    case QB_Q8_0: return kQ8_0;
+    case QB_Q4K: return kQ4K;
+    case QB_Q6K: return kQ6K;
+    default: return -1;
+    }
+}
+
+static bool misaligned(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; }
+
+constexpr int64_t kMaxK = int64_t(1) << 18;  // a row's record must fit a CTA tile in shared memory
+
+}  // namespace qb
+
+using namespace qb;
+
+extern "C" {
+
+int quantize_act(int block, const float *x, int64_t K, int ncols, int8_t *codes, qb_scale *scales, int16_t *sums16,
+                 void *stream) {
+    if (block != 32 && block != 256) return QB_E_BLOCK;
+    if (!x || !codes || !scales || !sums16) return QB_E_ARG;
+    if (K < 0 || K % block != 0 || K > (int64_t(1) << 24) || ncols < 1 || ncols > 16) return QB_E_ARG;
+    if (misaligned(x) || misaligned(codes) || (reinterpret_cast<uintptr_t>(scales) & 3u) ||
+        (reinterpret_cast<uintptr_t>(sums16) & 3u))
+        return QB_E_ARG;
+    if (K == 0) return QB_OK;
+    return launch_quantize_act(block, x, K, ncols, codes, scales, sums16, static_cast<cudaStream_t>(stream));
+}
+
+static int check_gemv_args(qb_fmt fmt, const void *W, int64_t rows, int64_t K, const qb_act *act, int ncols,
+                           const void *out) {
+    const int f = fmt_index(fmt);
+    if (f < 0) return QB_E_FORMAT;
+    if (!W || !act || !out || !act->codes || !act->scales) return QB_E_ARG;
+    if (f != kQ8_0 && !act->sums16) return QB_E_ARG;
+    if (act->block != fmt_block(f)) return QB_E_BLOCK;
+    if (rows < 0 || K < 0 || K % fmt_block(f) != 0 || K > kMaxK || ncols < 1 || ncols > 16) return QB_E_ARG;
+    if (rows > (int64_t(1) << 31)) return QB_E_ARG;
+    if (misaligned(W) || misaligned(act->codes) || (act->sums16 && misaligned(act->sums16)) ||
+        (reinterpret_cast<uintptr_t>(act->scales) & 3u) || (reinterpret_cast<uintptr_t>(out) & 3u))
+        return QB_E_ARG;
+    return QB_OK;
+}
+
+static int gemv_common(qb_fmt fmt, const void *W, int64_t rows, int64_t K, const qb_act *act, int ncols, float *out,
+                       int32_t *C, int32_t *O, float *v, int mode, void *stream) {
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    GemvArgs a;
+    a.W = W;
+    a.rows = rows;
+    a.K = K;
+    a.codes = act->codes;
+    a.scales = act->scales;
+    a.sums16 = act->sums16;
+    a.ncols = ncols;
+    a.out = out;
+    a.dbgC = C;
+    a.dbgO = O;
+    a.dbgV = v;
+    a.mode = mode;
+    switch (fmt_index(fmt)) {
+    case kQ8_0: return launch_gemv_q8_0(a, s);
+    case kQ4K: return launch_gemv_q4k(a, s);
+    default: return launch_gemv_q6k(a, s);
+    }
+}
+
+int q_gemv(qb_fmt fmt, const void *W, int64_t rows, int64_t K, const qb_act *act, int ncols, float *out,
+           void *stream) {
+    const int rc = check_gemv_args(fmt, W, rows, K, act, ncols, out);
+    if (rc) return rc;
+    if (rows == 0) return QB_OK;
+    if (K == 0) {  // rows of no blocks: the fold of no terms is +0
+        return cudaMemsetAsync(out, 0, (size_t)ncols * rows * sizeof(float), static_cast<cudaStream_t>(stream)) ==
+                       cudaSuccess
+                   ? QB_OK
+                   : QB_E_CUDA;
+    }
+    return gemv_common(fmt, W, rows, K, act, ncols, out, nullptr, nullptr, nullptr, 0, stream);
+}
+
+int q_block_values(qb_fmt fmt, const void *W, int64_t rows, int64_t K, const qb_act *act, int ncols, int32_t *C,
+                   int32_t *O, float *v, void *stream) {
+    const void *any = C ? (const void *)C : O ? (const void *)O : (const void *)v;
+    if (!any) return QB_E_ARG;
+    const int rc = check_gemv_args(fmt, W, rows, K, act, ncols, any);
+    if (rc) return rc;
+    if (rows == 0 || K == 0) return QB_OK;
+    return gemv_common(fmt, W, rows, K, act, ncols, nullptr, C, O, v, 1, stream);
+}
+
+int quantize_act_f16(const float *x, int64_t K, int ncols, uint16_t *x16, void *stream) {
+    if (!x || !x16) return QB_E_ARG;
+    if (K < 0 || ncols < 1 || ncols > 16 || K > (int64_t(1) << 24)) return QB_E_ARG;
+    if ((reinterpret_cast<uintptr_t>(x) & 3u) || (reinterpret_cast<uintptr_t>(x16) & 1u)) return QB_E_ARG;
+    if (K == 0) return QB_OK;
+    return launch_quantize_f16(x, K * ncols, x16, static_cast<cudaStream_t>(stream));
+}
+
+int q_gemv_f16(const uint16_t *W, int64_t rows, int64_t K, const uint16_t *x16, int ncols, float *out, void *stream) {
+    if (!W || !x16 || !out) return QB_E_ARG;
+    if (rows < 0 || K < 0 || K % 8 != 0 || ncols < 1 || ncols > 16 || rows > (int64_t(1) << 31)) return QB_E_ARG;
+    if ((int64_t)ncols * K * 4 > 227 * 1024) return QB_E_ARG;
+    if (misaligned(W) || (reinterpret_cast<uintptr_t>(x16) & 1u) || (reinterpret_cast<uintptr_t>(out) & 3u))
+        return QB_E_ARG;
+    if (rows == 0) return QB_OK;
+    if (K == 0)
+        return cudaMemsetAsync(out, 0, (size_t)ncols * rows * sizeof(float), static_cast<cudaStream_t>(stream)) ==
+                       cudaSuccess
+                   ? QB_OK
+                   : QB_E_CUDA;
+    return launch_gemv_f16(W, rows, K, x16, ncols, out, static_cast<cudaStream_t>(stream));
+}
+
+int q_check_weights(qb_fmt fmt, const void *W, int64_t rows, int64_t K, void *stream) {
+    const int f = fmt_index(fmt);
+    if (fmt == QB_F16) return QB_OK;  // no block scales
+    if (f < 0) return QB_E_FORMAT;
+    if (!W || rows < 0 || K < 0 || K % fmt_block(f) != 0 || K > kMaxK || misaligned(W)) return QB_E_ARG;
+    if (rows == 0 || K == 0) return QB_OK;
+    int flag = 0;
+    const int rc = launch_check_weights(f, W, rows, K, &flag, static_cast<cudaStream_t>(stream));
+    if (rc) return rc;
+    return flag ? QB_E_UNREADABLE : QB_OK;
+}
+
+int64_t q_weight_bytes(qb_fmt fmt, int64_t rows, int64_t K) {
+    if (rows < 0 || K < 0) return QB_E_ARG;
+    if (fmt == QB_F16) return K % 8 ? QB_E_ARG : rows * K * 2;
+    const int f = fmt_index(fmt);
+    if (f < 0) return QB_E_FORMAT;
+    if (K % fmt_block(f) != 0) return QB_E_ARG;
+    return rows * record_bytes(f, K);
+}
+
+int q_device_status(void *stream) {
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int h = 0, zero = 0;
+    if (cudaMemcpyFromSymbolAsync(&h, g_fault, sizeof(int), 0, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return QB_E_CUDA;
+    if (cudaMemcpyToSymbolAsync(g_fault, &zero, sizeof(int), 0, cudaMemcpyHostToDevice, s) != cudaSuccess)
+        return QB_E_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return QB_E_CUDA;
+    return h ? QB_E_DEVICE : QB_OK;
+}
+
+const char *q_strerror(int status) {
+    switch (status) {
+    case QB_OK: return "ok";
+    case QB_E_ARG: return "invalid argument (null or misaligned pointer, size out of range)";
+    case QB_E_FORMAT: return "weight format not read by this library";
+    case QB_E_BLOCK: return "activation block differs from the weight format's block";
+    case QB_E_CUDA: return "CUDA call or launch failed";
+    case QB_E_UNREADABLE: return "weights hold an infinite or NaN block scale";
+    case QB_E_DEVICE: return "a kernel gave up a bounded wait";
+    default: return "unknown status";
+    }
+}
+
+}  // extern "C"

@@ -1,0 +1,7 @@
+// qb_gemv_q6k.cu -- instantiation of the product kernel for one weight format
+// (one translation unit per format so the three compile in parallel).
+#include "qb_gemv.cuh"
+
+namespace qb {
+int launch_gemv_q6k(const GemvArgs &a, cudaStream_t stream) { return launch_gemv_fmt<kQ6K>(a, stream); }
+}  // namespace qb

@@ -1,0 +1,7 @@
+// qb_gemv_q8_0.cu -- instantiation of the product kernel for one weight format
+// (one translation unit per format so the three compile in parallel).
+#include "qb_gemv.cuh"
+
+namespace qb {
+int launch_gemv_q8_0(const GemvArgs &a, cudaStream_t stream) { return launch_gemv_fmt<kQ8_0>(a, stream); }
+}  // namespace qb

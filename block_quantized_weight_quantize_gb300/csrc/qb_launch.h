@@ -1,0 +1,62 @@
+// qb_launch.h -- host-side launch helper and the internal launcher prototypes.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "qgemv.h"
+
+namespace qb {
+
+// Launch with programmatic dependent launch allowed (the kernel may begin
+// while the previous kernel on the stream drains; each kernel here calls
+// griddepcontrol.wait before touching data a predecessor may produce).
+template <typename... KArgs, typename... Args>
+inline int launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                      Args... args) {
+    if (grid.x == 0) return QB_OK;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t err = cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+    return err == cudaSuccess ? QB_OK : QB_E_CUDA;
+}
+
+int launch_quantize_act(int block, const float *x, int64_t K, int ncols, int8_t *codes, qb_scale *scales,
+                        int16_t *sums16, cudaStream_t stream);
+int launch_quantize_f16(const float *x, int64_t n, uint16_t *x16, cudaStream_t stream);
+
+// The per-format product launchers (qb_gemv_*.cu).  mode 0: rows folded into
+// out; mode 1: per-block C, O, v written instead (testing).
+struct GemvArgs {
+    const void *W;
+    int64_t rows;
+    int64_t K;
+    const int8_t *codes;
+    const qb_scale *scales;
+    const int16_t *sums16;
+    int ncols;
+    float *out;
+    int32_t *dbgC;
+    int32_t *dbgO;
+    float *dbgV;
+    int mode;
+};
+int launch_gemv_q8_0(const GemvArgs &a, cudaStream_t stream);
+int launch_gemv_q4k(const GemvArgs &a, cudaStream_t stream);
+int launch_gemv_q6k(const GemvArgs &a, cudaStream_t stream);
+int launch_gemv_f16(const uint16_t *W, int64_t rows, int64_t K, const uint16_t *x16, int ncols, float *out,
+                    cudaStream_t stream);
+int launch_check_weights(int fmt, const void *W, int64_t rows, int64_t K, int *flag, cudaStream_t stream);
+
+int num_sms();
+// Device address of the library's fault word on the current device (NULL on failure).
+int *fault_word();
+
+}  // namespace qb

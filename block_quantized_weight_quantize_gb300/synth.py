@@ -77,23 +77,23 @@ def log_uniform_f16_bits(rng: np.random.Generator, lo: float, hi: float, shape) 
 
 
 def draw_q8_0(rng, rows, K, d_range=(1e-3, 1e-2)):
-    q = rng.integers(-127, 128, size=(rows, K), dtype=np.int64).astype(np.int8)
+    q = rng.integers(-127, 128, size=(rows, K), dtype=np.int8)
     d = log_uniform_f16_bits(rng, *d_range, (rows, K // 32))
     return {"q": q, "d": d}
 
 
 def draw_q4k(rng, rows, K, d_range=(1e-4, 1e-2)):
-    q = rng.integers(0, 16, size=(rows, K), dtype=np.int64).astype(np.uint8)
-    sc = rng.integers(0, 64, size=(rows, K // 32), dtype=np.int64).astype(np.uint8)
-    mn = rng.integers(0, 64, size=(rows, K // 32), dtype=np.int64).astype(np.uint8)
+    q = rng.integers(0, 16, size=(rows, K), dtype=np.uint8)
+    sc = rng.integers(0, 64, size=(rows, K // 32), dtype=np.uint8)
+    mn = rng.integers(0, 64, size=(rows, K // 32), dtype=np.uint8)
     d = log_uniform_f16_bits(rng, *d_range, (rows, K // 256))
     dmin = log_uniform_f16_bits(rng, *d_range, (rows, K // 256))
     return {"q": q, "sc": sc, "mn": mn, "d": d, "dmin": dmin}
 
 
 def draw_q6k(rng, rows, K, d_range=(1e-5, 1e-3)):
-    q = rng.integers(0, 64, size=(rows, K), dtype=np.int64).astype(np.uint8)
-    sc = rng.integers(-128, 128, size=(rows, K // 16), dtype=np.int64).astype(np.int8)
+    q = rng.integers(0, 64, size=(rows, K), dtype=np.uint8)
+    sc = rng.integers(-128, 128, size=(rows, K // 16), dtype=np.int8)
     d = log_uniform_f16_bits(rng, *d_range, (rows, K // 256))
     return {"q": q, "sc": sc, "d": d}
 

@@ -1,0 +1,162 @@
+/*
+ * qgemv.h -- C ABI of the block-quantized weight x quantized activation
+ * product on GB300 (sm_103a).  Plain pointers and sizes; no C++ types.
+ *
+ * What is computed (the decode engine's numerics page, "ActScaling::PerBlock",
+ * functions quantize_blocks / dot / exact_sum / scaled_to_f32; the block-scale
+ * lane page, functions block_sums / lane):
+ *   - an activation row is quantized per weight block to int8 codes under a
+ *     scale m*2^e with m in 128..255 (the least such scale with
+ *     127*m*2^e >= the block's largest magnitude; codes the nearest integers
+ *     of x/scale, ties to even);
+ *   - for every weight block of a row, the two integer sums sum(coef*a) and
+ *     sum(offs*a) are formed exactly, multiplied by the block's scales and the
+ *     activation scale, summed exactly in a wide integer and rounded once to
+ *     f32 (to nearest even on the f32 grid, a subnormal result then flushed to
+ *     a zero of its sign);
+ *   - the rounded block values of a row are added in block order from +0 in
+ *     f32 (round to nearest even, subnormal results flushed).
+ * F16 weights (numerics page, f32_to_f16 / fdot / tree): the activation is
+ * rounded to f16; element i's exact product goes to lane i mod 8 in index
+ * order from +0; the 8 lanes fold as ((l0+l1)+(l2+l3))+((l4+l5)+(l6+l7)).
+ *
+ * Memory: every data pointer is DEVICE memory owned by the caller; the
+ * library allocates nothing and keeps no per-call state.  Weight pointers
+ * must be 16-byte aligned.  Calls are asynchronous on `stream` (a
+ * cudaStream_t passed as void*, NULL = the legacy default stream), except
+ * q_check_weights, which synchronizes that stream.  Kernels are launched with
+ * programmatic dependent launch: a product kernel may start streaming its
+ * weights while the previous kernel on the stream finishes, and waits for it
+ * before it reads activations or writes outputs.
+ *
+ * Errors: 0 on success, else a negative QB_E_* code (argument checks happen
+ * on the host before any launch; nothing is launched on error).
+ *
+ * Layouts (little endian; the pages fix the logical form of a coded row --
+ * every weight is a*coef + b*offs of its segment (numerics page, structs
+ * CodedRow, Segment, Scale) -- but no bytes, so these are this library's own).
+ * A matrix is `rows` row records laid end to end, q_weight_bytes() in all.
+ *   QB_Q8_0 (block 32):  int8 codes[K] | f16 d[K/32] | zero pad to 16 B.
+ *                        weight = d*q.
+ *   QB_Q4K  (block 256): K/256 blocks of 144 B:
+ *                        f16 d | f16 dmin | sc: eight 6-bit fields in a 48-bit
+ *                        little-endian integer (field s at bits 6s..6s+5) |
+ *                        mn: the same | qs: 16 B per 32-element sub-block s,
+ *                        byte j = q[32s+j] | q[32s+16+j] << 4.
+ *                        weight = d*sc[s]*q - dmin*mn[s], q in 0..15.
+ *   QB_Q6K  (block 256): K/256 blocks of 208 B | f16 d[K/256] | pad to 16 B.
+ *                        A block: ql (128 B; per 32-element chunk c, byte j =
+ *                        low nibbles of q[32c+j] | q[32c+16+j] << 4) |
+ *                        qh (64 B; per chunk c, bytes 0..3: byte b holds the
+ *                        top 2 bits of q[32c+4k+b] at bits 2k..2k+1, k=0..3;
+ *                        bytes 4..7 the same for q[32c+16+4k+b]) |
+ *                        sc (16 x int8, one per 16-element unit).
+ *                        weight = d*sc[u]*(q-32), q in 0..63.
+ *   QB_F16:              f16 W[rows][K], K % 8 == 0.
+ * Activations (ncols columns): codes int8 [ncols][K]; scales qb_scale
+ * [ncols][K/block]; sums16 int16 [ncols][K/16] (the sum of each 16-element
+ * unit's codes -- the activation side's unit sums of the lane page).
+ * Outputs f32 out[c*rows + r].
+ */
+#ifndef QGEMV_H
+#define QGEMV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define QB_API __attribute__((visibility("default")))
+#else
+#define QB_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { QB_F16 = 1, QB_Q8_0 = 8, QB_Q4K = 12, QB_Q6K = 14 } qb_fmt;
+
+enum {
+    QB_OK = 0,
+    QB_E_ARG = -1,        /* null pointer, misaligned weights, K or rows out of range, ncols not in 1..16 */
+    QB_E_FORMAT = -2,     /* a format this library does not read (numerics page, reads) */
+    QB_E_BLOCK = -3,      /* act->block differs from the format's block */
+    QB_E_CUDA = -4,       /* a CUDA call or launch failed */
+    QB_E_UNREADABLE = -5, /* q_check_weights found an inf/NaN block scale (numerics page, Unreadable) */
+    QB_E_DEVICE = -6      /* a kernel gave up a bounded wait (q_device_status) */
+};
+
+/* An activation block's scale m*2^e, m in 128..255 (numerics page, ActScale
+ * under PerBlock).  m == 0 marks a block holding an infinity: it has no scale,
+ * and every row's dot with it is the engine's NaN 0x7FC00000. */
+typedef struct {
+    uint8_t m;
+    uint8_t _pad;
+    int16_t e;
+} qb_scale;
+
+/* A quantized activation (numerics page, struct ActRow): `block` elements
+ * share one scale; all pointers device memory, laid out as above. */
+typedef struct {
+    int block;
+    const int8_t *codes;
+    const qb_scale *scales;
+    const int16_t *sums16;
+} qb_act;
+
+/* quantize_blocks (numerics page): x f32 [ncols][K] quantized per block of
+ * `block` (32 or 256) elements.  absmax reads a denormal as zero and passes
+ * NaN over; a denormal or NaN element gets code 0; an all-zero block gets
+ * m=128, e=0; a block with an infinity gets m=0.  K % block == 0, K <= 2^24,
+ * ncols in 1..16.  Writes codes, scales and sums16. */
+QB_API int quantize_act(int block, const float *x, int64_t K, int ncols, int8_t *codes, qb_scale *scales,
+                 int16_t *sums16, void *stream);
+
+/* dot under PerBlock (numerics page) for every row of W and every column of
+ * act: out[c*rows + r].  fmt in {QB_Q8_0, QB_Q4K, QB_Q6K}; act->block must be
+ * the format's block (32, 256, 256); K % block == 0; ncols in 1..16.  A row
+ * with an inf/NaN block scale (numerics page, Unreadable) is written as the
+ * engine's NaN 0x7FC00000; use q_check_weights to refuse such matrices up
+ * front. */
+QB_API int q_gemv(qb_fmt fmt, const void *W, int64_t rows, int64_t K, const qb_act *act, int ncols, float *out,
+           void *stream);
+
+/* f32_to_f16 (numerics page) over x f32 [ncols][K]: round to nearest even,
+ * subnormals kept, past the top infinite; NaN becomes 0x7E00. */
+QB_API int quantize_act_f16(const float *x, int64_t K, int ncols, uint16_t *x16, void *stream);
+
+/* fdot with LANES = 8 and the pairwise tree (numerics page) for F16 weights
+ * W [rows][K] against x16 [ncols][K]: out[c*rows + r].  K % 8 == 0; ncols in
+ * 1..16; a NaN result is written as 0x7FC00000. */
+QB_API int q_gemv_f16(const uint16_t *W, int64_t rows, int64_t K, const uint16_t *x16, int ncols, float *out,
+               void *stream);
+
+/* reads (numerics page) / Unreadable: scans every block scale of W for inf or
+ * NaN.  Synchronizes `stream`.  Returns QB_OK, QB_E_UNREADABLE, or an error. */
+QB_API int q_check_weights(qb_fmt fmt, const void *W, int64_t rows, int64_t K, void *stream);
+
+/* Bytes of a rows x K matrix in `fmt` (row records included), or a negative
+ * QB_E_* code for an unread format or a K the format cannot hold. */
+QB_API int64_t q_weight_bytes(qb_fmt fmt, int64_t rows, int64_t K);
+
+/* Per-block results for testing the lane (lane page, block_sums / lane): for
+ * every column c, row r and weight block b, the block's exact sums C and O
+ * (int32, [ncols][rows][K/block]; O is 0 for formats without offsets) and its
+ * value rounded once (f32, same layout).  Same kernels' arithmetic as q_gemv,
+ * without the row fold.  Any of C, O, v may be NULL. */
+QB_API int q_block_values(qb_fmt fmt, const void *W, int64_t rows, int64_t K, const qb_act *act, int ncols,
+                   int32_t *C, int32_t *O, float *v, void *stream);
+
+/* Reads and clears the library's device fault word (set when a kernel gives
+ * up a bounded wait on its own copies).  Synchronizes `stream`.  Returns
+ * QB_OK or QB_E_DEVICE. */
+QB_API int q_device_status(void *stream);
+
+/* A static string for a status code. */
+QB_API const char *q_strerror(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QGEMV_H */

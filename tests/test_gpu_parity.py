@@ -1,0 +1,353 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Integer results (activation codes, scales, unit sums, block sums C and O) and
+every block's once-rounded f32 value must match bit for bit.  Rows must match
+within |delta| <= 1e-5 * sum_b |v_b| (the product's stated tolerance, which
+allows a tree fold of the block values); the kernels fold in block order as
+the oracle does, so the tests demand -- and check -- bit equality.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import block_quantized_weight_quantize_gb300 as qb
+from block_quantized_weight_quantize_gb300 import synth
+from helpers import bits, dev, host, make_case, oracle_act, unpack_scales
+
+pytestmark = pytest.mark.gpu
+
+FMTS = [synth.FMT_Q8_0, synth.FMT_Q4K, synth.FMT_Q6K]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    import torch
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    qb.lib()
+    yield
+    torch.cuda.synchronize()
+    assert qb.q_device_status() == qb.QB_OK
+
+
+def gpu_quantize(x: np.ndarray, block: int):
+    import torch
+    ncols, K = x.shape
+    codes, scales, sums = qb.alloc_act(ncols, K, block)
+    qb.quantize_act(block, dev(x), codes, scales, sums)
+    torch.cuda.synchronize()
+    return codes, scales, sums
+
+
+def gpu_rows(fmt, W, rows, K, act, ncols):
+    import torch
+    out = torch.full((ncols, rows), float("nan"), dtype=torch.float32, device="cuda")
+    qb.q_gemv(fmt, dev(W) if isinstance(W, np.ndarray) else W, rows, K, act, ncols, out)
+    torch.cuda.synchronize()
+    return host(out)
+
+
+def tolerance_ok(got, want, v_abs_sum):
+    return np.all(np.abs(got.astype(np.float64) - want.astype(np.float64)) <= 1e-5 * v_abs_sum)
+
+
+# ---------------------------------------------------------------- quantize_act
+
+def _edge_activation(ncols, K, block, seed):
+    rng = np.random.default_rng(seed)
+    x = synth.draw_act(rng, ncols, K, outlier_frac=0.001)
+    nb = K // block
+    planted = [
+        lambda b: 0.0,                                           # all-zero block
+        lambda b: np.float32(1e-38) * x[0, b],                   # bottom of the f32 range
+        lambda b: np.float32(1e37) * x[0, b],                    # top of the f32 range
+        lambda b: np.round(x[0, b] * 4) / 4,                     # many exact ties
+    ]
+    for i, f in enumerate(planted):
+        if i < nb:
+            sl = slice(i * block, (i + 1) * block)
+            x[0, sl] = f(sl)
+    if nb > 4:
+        x[0, 4 * block + 3] = np.nan                             # NaN element
+        x[0, 4 * block + 5] = np.uint32(0x00012345).view(np.float32)   # denormal element
+    if nb > 5:
+        x[0, 5 * block + 1] = np.inf                              # a block with an infinity
+    if nb > 6:
+        x[0, 6 * block:7 * block] = np.uint32(0x00000042).view(np.float32)  # only denormals
+    return x
+
+
+@pytest.mark.parametrize("block,K", [(32, 1024), (256, 4096), (32, 96), (256, 256)])
+@pytest.mark.parametrize("ncols", [1, 3, 16])
+def test_quantize_act_bit_exact(block, K, ncols):
+    x = _edge_activation(ncols, K, block, seed=block + ncols + K)
+    codes, m, e, s16, packed = oracle_act(x, block)
+    gc, gs, gsum = gpu_quantize(x, block)
+    assert np.array_equal(host(gc), codes)
+    gm, ge = unpack_scales(host(gs))
+    assert np.array_equal(gm, m) and np.array_equal(ge, e)
+    assert np.array_equal(host(gsum), s16)
+
+
+# ---------------------------------------------------------------- block values (the lane)
+
+SHAPES = {synth.FMT_Q8_0: [(37, 1024), (129, 2048), (5, 32)],
+          synth.FMT_Q4K: [(37, 1024), (130, 4096), (3, 256)],
+          synth.FMT_Q6K: [(37, 1024), (130, 4096), (3, 256)]}
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_block_values_bit_exact(fmt):
+    import torch
+    for si, (rows, K) in enumerate(SHAPES[fmt]):
+        for ncols in (1, 4):
+            lg, W, x = make_case(fmt, rows, K, ncols, seed=100 * fmt + si, outliers=0.001)
+            blk = synth.BLOCK[fmt]
+            codes, m, e, s16, packed = oracle_act(x, blk)
+            C, O, v = oracle.block_values(fmt, W, rows, K, codes, m, e)
+            nb = K // blk
+            gC = torch.empty((ncols, rows, nb), dtype=torch.int32, device="cuda")
+            gO = torch.empty_like(gC)
+            gv = torch.empty((ncols, rows, nb), dtype=torch.float32, device="cuda")
+            qb.q_block_values(fmt, dev(W), rows, K, (dev(codes), dev(packed), dev(s16)), ncols, gC, gO, gv)
+            torch.cuda.synchronize()
+            assert np.array_equal(host(gC), C), (rows, K, ncols)
+            assert np.array_equal(host(gO), O), (rows, K, ncols)
+            assert np.array_equal(bits(host(gv)), bits(v)), (rows, K, ncols)
+
+
+def test_block_values_wide_exponent_spread():
+    """Q4_K blocks whose d and dmin exponents lie far apart (up to the whole f16
+    range, subnormals included) take the 128-bit combine; still bit-exact."""
+    import torch
+    rng = np.random.default_rng(77)
+    rows, K = 64, 1024
+    lg = synth.draw_q4k(rng, rows, K)
+    extremes = np.array([0x0001, 0x0003, 0x03FF, 0x0400, 0x7BFF, 0x7800, 0x3C00, 0x1234], np.uint16)
+    lg["d"] = rng.choice(extremes, size=lg["d"].shape).astype(np.uint16)
+    lg["dmin"] = rng.choice(extremes, size=lg["dmin"].shape).astype(np.uint16)
+    lg["d"][0, 0], lg["dmin"][0, 0] = 0x0001, 0x7BFF          # spread 2^-24 vs 65504
+    lg["d"][1, 0], lg["dmin"][1, 0] = 0x7BFF, 0x0001
+    W = synth.pack_q4k(**lg)
+    x = synth.draw_act(rng, 2, K) * np.float32(1e-30)         # push values toward the f32 bottom too
+    x[1] *= np.float32(1e35)
+    codes, m, e, s16, packed = oracle_act(x, 256)
+    C, O, v = oracle.block_values(synth.FMT_Q4K, W, rows, K, codes, m, e)
+    gv = torch.empty((2, rows, K // 256), dtype=torch.float32, device="cuda")
+    qb.q_block_values(synth.FMT_Q4K, dev(W), rows, K, (dev(codes), dev(packed), dev(s16)), 2, None, None, gv)
+    torch.cuda.synchronize()
+    assert np.array_equal(bits(host(gv)), bits(v))
+
+
+# ---------------------------------------------------------------- rows
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("ncols", [1, 2, 3, 4, 5, 8, 13, 16])
+def test_gemv_rows_bit_exact(fmt, ncols):
+    K = 2048 if fmt == synth.FMT_Q8_0 else 4096
+    rows = 261   # several tiles and a ragged tail
+    lg, W, x = make_case(fmt, rows, K, ncols, seed=7 * fmt + ncols, outliers=0.001)
+    blk = synth.BLOCK[fmt]
+    codes, m, e, s16, packed = oracle_act(x, blk)
+    want = oracle.gemv(fmt, W, rows, K, codes, m, e)
+    act = gpu_quantize(x, blk)   # the product consumes the GPU's own quantization
+    got = gpu_rows(fmt, W, rows, K, act, ncols)
+    assert np.array_equal(bits(got), bits(want))
+    _, _, v = oracle.block_values(fmt, W, rows, K, codes, m, e)
+    assert tolerance_ok(got, want, np.abs(v.astype(np.float64)).sum(-1))
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_batch_invariance(fmt):
+    K = 1024
+    rows = 97
+    lg, W, x = make_case(fmt, rows, K, 16, seed=31 + fmt)
+    act = gpu_quantize(x, synth.BLOCK[fmt])
+    allc = gpu_rows(fmt, W, rows, K, act, 16)
+    for c in (0, 5, 15):
+        one = tuple(t[c:c + 1].contiguous() for t in act)
+        got = gpu_rows(fmt, W, rows, K, one, 1)
+        assert np.array_equal(bits(got[0]), bits(allc[c]))
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_long_rows_and_chunked_activation(fmt):
+    """K = 14336 (the down projection) at 16 columns: the activation is staged
+    in several chunks of at most 64 KB."""
+    K, rows, ncols = 14336, 45, 16
+    if fmt == synth.FMT_Q8_0:
+        K = 14336
+    lg, W, x = make_case(fmt, rows, K, ncols, seed=55 + fmt)
+    blk = synth.BLOCK[fmt]
+    codes, m, e, s16, packed = oracle_act(x, blk)
+    want = oracle.gemv(fmt, W, rows, K, codes, m, e)
+    got = gpu_rows(fmt, W, rows, K, gpu_quantize(x, blk), ncols)
+    assert np.array_equal(bits(got), bits(want))
+
+
+# ---------------------------------------------------------------- full-size workloads
+
+def test_q8_0_512x1024_full():
+    lg, W, x = make_case(synth.FMT_Q8_0, 512, 1024, 1, seed=0)
+    codes, m, e, s16, packed = oracle_act(x, 32)
+    want = oracle.gemv(synth.FMT_Q8_0, W, 512, 1024, codes, m, e)
+    got = gpu_rows(synth.FMT_Q8_0, W, 512, 1024, gpu_quantize(x, 32), 1)
+    assert np.array_equal(bits(got), bits(want))
+
+
+def test_q4k_4096x4096_full():
+    mats, x = synth.workload_inputs("q4k_4096x4096")
+    rows, K, lg, W = mats[0]
+    codes, m, e, s16, packed = oracle_act(x, 256)
+    want = oracle.gemv(synth.FMT_Q4K, W, rows, K, codes, m, e)
+    got = gpu_rows(synth.FMT_Q4K, W, rows, K, gpu_quantize(x, 256), 1)
+    assert np.array_equal(bits(got), bits(want))
+
+
+def test_q6k_ffn_full():
+    """gate and up (14336x4096, one shared activation) and down (4096x14336)."""
+    rng = np.random.default_rng(2)
+    gate = synth.draw_q6k(rng, 14336, 4096)
+    up = synth.draw_q6k(rng, 14336, 4096)
+    down = synth.draw_q6k(rng, 4096, 14336)
+    x = synth.draw_act(rng, 1, 4096)
+    h = synth.draw_act(rng, 1, 14336)
+    for lg, xx in ((gate, x), (up, x), (down, h)):
+        rows, K = lg["q"].shape
+        W = synth.pack_q6k(**lg)
+        codes, m, e, s16, packed = oracle_act(xx, 256)
+        want = oracle.gemv(synth.FMT_Q6K, W, rows, K, codes, m, e)
+        got = gpu_rows(synth.FMT_Q6K, W, rows, K, gpu_quantize(xx, 256), 1)
+        assert np.array_equal(bits(got), bits(want)), (rows, K)
+
+
+@pytest.mark.parametrize("ncols", [1, 4, 16])
+def test_8b_stack_shapes_sampled(ncols):
+    """The decode-stack shapes at 1, 4 and 16 columns, in the launch shape the
+    benchmark uses; the oracle checks a sample of rows of each matrix."""
+    import torch
+    rng = np.random.default_rng(5 + ncols)
+    shapes = [(synth.FMT_Q4K, 6144, 4096), (synth.FMT_Q4K, 4096, 4096), (synth.FMT_Q4K, 28672, 4096),
+              (synth.FMT_Q4K, 4096, 14336), (synth.FMT_Q6K, 128256, 4096)]
+    for fmt, rows, K in shapes:
+        lg = synth.draw(fmt, rng, rows, K)
+        W = synth.pack(fmt, lg)
+        x = synth.draw_act(rng, ncols, K)
+        codes, m, e, s16, packed = oracle_act(x, 256)
+        got = gpu_rows(fmt, W, rows, K, gpu_quantize(x, 256), ncols)
+        sample = np.unique(np.concatenate([rng.integers(0, rows, 48), [0, rows - 1]]))
+        rec = synth.record_bytes(fmt, K)
+        Ws = np.concatenate([W[r * rec:(r + 1) * rec] for r in sample])
+        want = oracle.gemv(fmt, Ws, len(sample), K, codes, m, e)
+        assert np.array_equal(bits(got[:, sample]), bits(want)), (fmt, rows, K)
+        del W, lg
+        torch.cuda.empty_cache()
+
+
+# ---------------------------------------------------------------- edge cases
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_edge_shapes(fmt):
+    blk = synth.BLOCK[fmt]
+    K1 = blk if fmt == synth.FMT_Q8_0 else 256
+    for rows, K in ((1, K1), (2, K1), (33, K1), (1, 4096), (7, 3 * 256)):
+        lg, W, x = make_case(fmt, rows, K, 2, seed=rows * 13 + K)
+        codes, m, e, s16, packed = oracle_act(x, blk)
+        want = oracle.gemv(fmt, W, rows, K, codes, m, e)
+        got = gpu_rows(fmt, W, rows, K, gpu_quantize(x, blk), 2)
+        assert np.array_equal(bits(got), bits(want)), (rows, K)
+        if K == blk:   # one block: the row is that block's value
+            _, _, v = oracle.block_values(fmt, W, rows, K, codes, m, e)
+            assert np.array_equal(bits(got), bits(v[:, :, 0]))
+
+
+def test_empty_and_degenerate():
+    import torch
+    act = qb.alloc_act(1, 256, 256)
+    out = torch.full((1, 4), 7.0, device="cuda")
+    W = torch.zeros(144 * 4, dtype=torch.uint8, device="cuda")
+    qb.q_gemv(qb.Q4K, W, 0, 256, act, 1, out)               # no rows: nothing written
+    torch.cuda.synchronize()
+    assert torch.all(out == 7.0)
+    qb.q_gemv(qb.Q4K, W, 4, 0, act, 1, out)                 # rows of no blocks: +0
+    torch.cuda.synchronize()
+    assert np.all(bits(host(out)) == 0)
+    # an all-zero activation gives +0 in every row
+    lg, Wn, _ = make_case(synth.FMT_Q4K, 9, 512, 1, seed=3)
+    z = np.zeros((1, 512), np.float32)
+    got = gpu_rows(synth.FMT_Q4K, Wn, 9, 512, gpu_quantize(z, 256), 1)
+    assert np.all(bits(got) == 0)
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_unreadable_scales_and_nonfinite_activation(fmt):
+    rows, K = 6, 512
+    lg, _, x = make_case(fmt, rows, K, 2, seed=91 + fmt)
+    lg["d"][2, 1] = 0x7C00
+    lg["d"][4, 0] = 0xFE01
+    if fmt == synth.FMT_Q4K:
+        lg["dmin"][5, 0] = 0x7C00
+    W = synth.pack(fmt, lg)
+    blk = synth.BLOCK[fmt]
+    x[1, 3] = np.inf                                         # column 1: a block with no scale
+    codes, m, e, s16, packed = oracle_act(x, blk)
+    want = oracle.gemv(fmt, W, rows, K, codes, m, e)
+    got = gpu_rows(fmt, W, rows, K, gpu_quantize(x, blk), 2)
+    assert np.array_equal(bits(got), bits(want))
+    assert np.all(bits(got[1]) == 0x7FC00000)
+    assert bits(got[0, 2]) == 0x7FC00000 and bits(got[0, 4]) == 0x7FC00000
+    assert qb.q_check_weights(fmt, dev(W), rows, K) == qb.QB_E_UNREADABLE
+    assert oracle.count_unreadable(fmt, W, rows, K) >= 2
+    lg2, W2, _ = make_case(fmt, rows, K, 1, seed=5)
+    assert qb.q_check_weights(fmt, dev(W2), rows, K) == qb.QB_OK
+
+
+# ---------------------------------------------------------------- F16
+
+def test_quantize_act_f16_bit_exact():
+    import torch
+    rng = np.random.default_rng(21)
+    x = synth.draw_act(rng, 3, 4096)
+    x[0, :64] *= np.float32(1e-6)     # binary16 subnormals
+    x[0, 64:128] *= np.float32(4000)  # past the top
+    x[1, 7] = np.nan
+    x[1, 8] = -np.inf
+    x[2, :] = np.round(x[2, :] * 1024) / 1024 + np.float32(2.0 ** -11)   # ties
+    want = oracle.quantize_f16(x)
+    g = torch.empty((3, 4096), dtype=torch.int16, device="cuda")
+    qb.quantize_act_f16(dev(x), g)
+    torch.cuda.synchronize()
+    assert np.array_equal(host(g).view(np.uint16), want)
+
+
+@pytest.mark.parametrize("rows,K", [(49152, 576), (1536, 576), (13, 8), (129, 1536), (300, 64)])
+@pytest.mark.parametrize("ncols", [1, 2, 3, 6])
+def test_f16_gemv_bit_exact(rows, K, ncols):
+    import torch
+    rng = np.random.default_rng(rows + K + ncols)
+    W = synth.draw_f16(rng, rows, K)
+    x = synth.draw_act(rng, ncols, K)
+    x16 = oracle.quantize_f16(x)
+    want = oracle.gemv_f16(W, rows, K, x16)
+    gx = torch.empty((ncols, K), dtype=torch.int16, device="cuda")
+    qb.quantize_act_f16(dev(x), gx)
+    out = torch.empty((ncols, rows), dtype=torch.float32, device="cuda")
+    qb.q_gemv_f16(dev(W), rows, K, gx, ncols, out)
+    torch.cuda.synchronize()
+    assert np.array_equal(bits(host(out)), bits(want))
+
+
+def test_f16_sixteen_columns_and_nonfinite():
+    import torch
+    rng = np.random.default_rng(8)
+    rows, K = 200, 512
+    W = synth.draw_f16(rng, rows, K)
+    W[3, 9] = 0x7C00                      # +inf weight
+    W[4, 0] = 0x7E00                      # NaN weight
+    x = synth.draw_act(rng, 16, K)
+    x[2, 9] = 0.0                         # inf * 0 -> NaN in column 2, row 3
+    x16 = oracle.quantize_f16(x)
+    want = oracle.gemv_f16(W, rows, K, x16)
+    out = torch.empty((16, rows), dtype=torch.float32, device="cuda")
+    qb.q_gemv_f16(dev(W), rows, K, dev(x16.view(np.int16)), 16, out)
+    torch.cuda.synchronize()
+    assert np.array_equal(bits(host(out)), bits(want))
