@@ -216,7 +216,7 @@ def run_ours(args, rank, world):
     clocks = clk.summary()
 
     # ---- roofline: the product kernel alone, live, over rotating copies
-    n_roof = 2000
+    n_roof = args.roof_launches
     g_roof = capture(gemv_only, n_roof)
     with torch.cuda.stream(stream):
         g_roof.replay()
@@ -410,6 +410,8 @@ def main():
     ap.add_argument("--workload", default="q4k_4096x4096", choices=sorted(WORKLOADS))
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--roof-launches", type=int, default=2000,
+                    help="product-kernel launches per graph in the roofline timing (x3)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     rank = int(os.environ.get("RANK", 0))

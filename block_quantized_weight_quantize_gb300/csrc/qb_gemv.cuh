@@ -25,6 +25,7 @@
 #include <algorithm>
 
 #include "qb_common.cuh"
+#include "qb_gemv2.cuh"
 #include "qb_launch.h"
 
 namespace qb {
@@ -377,6 +378,10 @@ inline int gcd_int(int a, int b) { while (b) { int t = a % b; a = b; b = t; } re
 template <int F>
 int launch_gemv_fmt(const GemvArgs &a, cudaStream_t stream) {
     constexpr int blk = fmt_block(F);
+    if (a.mode == 0 && a.ncols == 1) {  // the streaming kernel, where it applies
+        const int rc = launch_gemv2<F>(a, stream);
+        if (rc != QB_E_ARG) return rc;
+    }
     GemvK k;
     k.W = static_cast<const uint8_t *>(a.W);
     k.rows = a.rows;
