@@ -28,7 +28,7 @@ LIB_PATH = os.path.join(_HERE, "libqgemv.so")
 
 # every entry point include/qgemv.h declares
 EXPORTS = ("quantize_act", "q_gemv", "quantize_act_f16", "q_gemv_f16", "q_check_weights", "q_weight_bytes",
-           "q_block_values", "q_device_status", "q_strerror")
+           "q_block_values", "q_device_status", "q_strerror", "q_matvec", "q_matvec_workspace_bytes")
 
 
 class QbError(RuntimeError):
@@ -64,6 +64,9 @@ def lib() -> ctypes.CDLL:
         L.q_block_values.restype = i32
         L.q_device_status.argtypes, L.q_device_status.restype = [P], i32
         L.q_strerror.argtypes, L.q_strerror.restype = [i32], ctypes.c_char_p
+        L.q_matvec_workspace_bytes.argtypes, L.q_matvec_workspace_bytes.restype = [i32, i64, i32], i64
+        L.q_matvec.argtypes = [i32, P, i64, i64, P, i32, P, P, ctypes.c_size_t, P]
+        L.q_matvec.restype = i32
         _lib = L
     return _lib
 
@@ -153,6 +156,24 @@ def q_device_status(stream=None) -> int:
 
 
 # ------------------------------------------------------------------ one call
+
+def q_matvec_workspace_bytes(fmt: int, K: int, ncols: int) -> int:
+    n = lib().q_matvec_workspace_bytes(fmt, K, ncols)
+    if n < 0:
+        raise QbError(int(n), "q_matvec_workspace_bytes")
+    return int(n)
+
+
+def q_matvec(fmt: int, W, rows: int, K: int, x, out, workspace=None, stream=None) -> None:
+    """The whole product from an f32 activation x [ncols, K]: out f32 [ncols, rows].
+    One launch for a single column of a block format (K % 256 == 0); otherwise
+    `workspace` (a uint8 device tensor of q_matvec_workspace_bytes) holds the
+    quantized activation between the two launches."""
+    ncols = x.shape[0]
+    nbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(lib().q_matvec(fmt, _ptr(W), rows, K, _ptr(x), ncols, _ptr(out), _ptr(workspace), nbytes,
+                          _stream(stream)), "q_matvec")
+
 
 def matvec(fmt: int, W, rows: int, K: int, x, out=None, act=None, stream=None):
     """quantize_act then q_gemv (or quantize_act_f16 then q_gemv_f16): x f32

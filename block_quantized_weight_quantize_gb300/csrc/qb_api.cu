@@ -226,6 +226,64 @@ int q_device_status(void *stream) {
     return h ? QB_E_DEVICE : QB_OK;
 }
 
+static int64_t align16(int64_t n) { return (n + 15) / 16 * 16; }
+
+int64_t q_matvec_workspace_bytes(qb_fmt fmt, int64_t K, int ncols) {
+    if (K < 0 || ncols < 1 || ncols > 16) return QB_E_ARG;
+    if (fmt == QB_F16) return K % 8 ? QB_E_ARG : align16(2 * K * ncols);
+    const int f = fmt_index(fmt);
+    if (f < 0) return QB_E_FORMAT;
+    const int blk = fmt_block(f);
+    if (K % blk) return QB_E_ARG;
+    return align16(K * ncols) + align16(4 * (K / blk) * ncols) + align16(2 * (K / 16) * ncols);
+}
+
+int q_matvec(qb_fmt fmt, const void *W, int64_t rows, int64_t K, const float *x, int ncols, float *out,
+             void *workspace, size_t workspace_bytes, void *stream) {
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (!x || !out || !W) return QB_E_ARG;
+    if (misaligned(x)) return QB_E_ARG;
+    const int64_t need = q_matvec_workspace_bytes(fmt, K, ncols);
+    if (need < 0) return (int)need;
+    if (fmt != QB_F16) {
+        const int f = fmt_index(fmt);
+        // argument checks of the product itself (with a stand-in activation)
+        qb_act probe = {fmt_block(f), reinterpret_cast<const int8_t *>(x), reinterpret_cast<const qb_scale *>(x),
+                        reinterpret_cast<const int16_t *>(x)};
+        const int rc = check_gemv_args(fmt, W, rows, K, &probe, ncols, out);
+        if (rc) return rc;
+        if (rows == 0) return QB_OK;
+        if (K == 0)
+            return cudaMemsetAsync(out, 0, (size_t)ncols * rows * sizeof(float), s) == cudaSuccess ? QB_OK : QB_E_CUDA;
+        if (ncols == 1) {
+            GemvArgs a = {};
+            a.W = W; a.rows = rows; a.K = K; a.ncols = 1; a.out = out; a.mode = 0;
+            const int r = f == kQ8_0 ? launch_matvec_q8_0(a, x, s)
+                        : f == kQ4K  ? launch_matvec_q4k(a, x, s)
+                                     : launch_matvec_q6k(a, x, s);
+            if (r != QB_E_ARG) return r;  // QB_E_ARG: the single-launch kernel does not take this shape
+        }
+    }
+    if (!workspace || (int64_t)workspace_bytes < need || misaligned(workspace)) return QB_E_ARG;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    if (fmt == QB_F16) {
+        uint16_t *x16 = reinterpret_cast<uint16_t *>(ws);
+        int rc = quantize_act_f16(x, K, ncols, x16, stream);
+        if (rc) return rc;
+        return q_gemv_f16(static_cast<const uint16_t *>(W), rows, K, x16, ncols, out, stream);
+    }
+    const int blk = fmt_block(fmt_index(fmt));
+    qb_act act;
+    act.block = blk;
+    act.codes = reinterpret_cast<const int8_t *>(ws);
+    act.scales = reinterpret_cast<const qb_scale *>(ws + align16(K * ncols));
+    act.sums16 = reinterpret_cast<const int16_t *>(ws + align16(K * ncols) + align16(4 * (K / blk) * ncols));
+    int rc = quantize_act(blk, x, K, ncols, const_cast<int8_t *>(act.codes), const_cast<qb_scale *>(act.scales),
+                          const_cast<int16_t *>(act.sums16), stream);
+    if (rc) return rc;
+    return q_gemv(fmt, W, rows, K, &act, ncols, out, stream);
+}
+
 const char *q_strerror(int status) {
     switch (status) {
     case QB_OK: return "ok";

@@ -4,4 +4,7 @@
 
 namespace qb {
 int launch_gemv_q8_0(const GemvArgs &a, cudaStream_t stream) { return launch_gemv_fmt<kQ8_0>(a, stream); }
+int launch_matvec_q8_0(const GemvArgs &a, const float *x, cudaStream_t stream) {
+    return launch_gemv2<kQ8_0>(a, stream, x);
+}
 }  // namespace qb

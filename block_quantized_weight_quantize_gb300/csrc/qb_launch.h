@@ -51,6 +51,11 @@ struct GemvArgs {
 int launch_gemv_q8_0(const GemvArgs &a, cudaStream_t stream);
 int launch_gemv_q4k(const GemvArgs &a, cudaStream_t stream);
 int launch_gemv_q6k(const GemvArgs &a, cudaStream_t stream);
+// The single-launch product (activation quantized inside the kernel); returns
+// QB_E_ARG when that kernel does not apply to the shape.
+int launch_matvec_q8_0(const GemvArgs &a, const float *x, cudaStream_t stream);
+int launch_matvec_q4k(const GemvArgs &a, const float *x, cudaStream_t stream);
+int launch_matvec_q6k(const GemvArgs &a, const float *x, cudaStream_t stream);
 int launch_gemv_f16(const uint16_t *W, int64_t rows, int64_t K, const uint16_t *x16, int ncols, float *out,
                     cudaStream_t stream);
 int launch_check_weights(int fmt, const void *W, int64_t rows, int64_t K, int *flag, cudaStream_t stream);

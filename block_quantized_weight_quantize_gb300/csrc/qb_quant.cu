@@ -14,6 +14,7 @@
 
 #include "qb_common.cuh"
 #include "qb_launch.h"
+#include "qb_quant.cuh"
 
 namespace qb {
 
@@ -40,73 +41,14 @@ __global__ void __launch_bounds__(256) quantize_act_kernel(const float *__restri
 #pragma unroll
         for (int i = 0; i < 8; ++i) xb[i] = 0;
     }
-    // absmax on magnitudes' bits: denormal -> 0, NaN skipped, +inf kept
-    uint32_t amax = 0;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        uint32_t a = xb[i] & 0x7FFFFFFFu;
-        if (a < 0x00800000u || a > 0x7F800000u) a = 0;
-        amax = a > amax ? a : amax;
-    }
-#pragma unroll
-    for (int o = L / 2; o > 0; o >>= 1) {
-        const uint32_t u = __shfl_xor_sync(0xFFFFFFFFu, amax, o);
-        amax = u > amax ? u : amax;
-    }
-    // wide_scale on amax = M * 2^(E8-150): the least 8-bit significand at
-    // e = E8-141 is ceil(M / (127*2^9)); past 255 the next exponent is taken.
-    int m, e;
-    if (amax == 0x7F800000u) {
-        m = 0; e = 0;  // an infinity: no scale
-    } else if (amax == 0) {
-        m = 128; e = 0;
-    } else {
-        const uint32_t E8 = amax >> 23, M = (amax & 0x7FFFFFu) | 0x800000u;
-        uint32_t mm = (M + 65023u) / 65024u;
-        int ee = (int)E8 - 141;
-        if (mm > 255u) { mm = (M + 130047u) / 130048u; ++ee; }
-        m = (int)mm; e = ee;
-    }
-    // rne_div per element: |x| = mant * 2^(E8x-150); x/s = mant / (m * 2^k), k = e - (E8x-150) >= 9
-    int q[8];
-    int usum = 0;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const uint32_t a = xb[i] & 0x7FFFFFFFu;
-        int c = 0;
-        if (m != 0 && a >= 0x00800000u && a < 0x7F800000u) {
-            const uint32_t mant = (a & 0x7FFFFFu) | 0x800000u;
-            const int k = e - ((int)(a >> 23) - 150);
-            if (k < 32) {
-                const uint32_t hi = mant >> k, lo = mant & ((1u << k) - 1u), half = 1u << (k - 1);
-                const uint32_t qq = hi / (uint32_t)m;
-                const int t2 = 2 * (int)(hi - qq * (uint32_t)m) - m;  // (2R - m*2^k) = t2*2^k + 2*lo
-                bool up;
-                if (t2 >= 1) up = true;
-                else if (t2 <= -2) up = false;
-                else if (t2 == -1) up = lo > half || (lo == half && (qq & 1u));
-                else up = lo > 0 || (qq & 1u);
-                c = (int)qq + (up ? 1 : 0);
-            }
-            if (xb[i] & 0x80000000u) c = -c;
-        }
-        q[i] = c;
-        usum += c;
-    }
-    // unit sums: two lanes (16 elements) per unit
-    usum += __shfl_xor_sync(0xFFFFFFFFu, usum, 1);
+    uint2 c;
+    int usum;
+    uint32_t scale;
+    quantize8<L>(xb, c, usum, scale);
     if (live) {
-        const uint32_t w0 = (uint32_t)(q[0] & 0xFF) | ((uint32_t)(q[1] & 0xFF) << 8) |
-                            ((uint32_t)(q[2] & 0xFF) << 16) | ((uint32_t)(q[3] & 0xFF) << 24);
-        const uint32_t w1 = (uint32_t)(q[4] & 0xFF) | ((uint32_t)(q[5] & 0xFF) << 8) |
-                            ((uint32_t)(q[6] & 0xFF) << 16) | ((uint32_t)(q[7] & 0xFF) << 24);
-        *reinterpret_cast<uint2 *>(codes + t * 8) = make_uint2(w0, w1);
+        *reinterpret_cast<uint2 *>(codes + t * 8) = c;
         if ((t & 1) == 0) sums16[t >> 1] = (int16_t)usum;
-        if ((t & (L - 1)) == 0) {
-            qb_scale s;
-            s.m = (uint8_t)m; s._pad = 0; s.e = (int16_t)e;
-            scales[t / L] = s;
-        }
+        if ((t & (L - 1)) == 0) reinterpret_cast<uint32_t *>(scales)[t / L] = scale;
     }
 }
 

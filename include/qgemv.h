@@ -121,6 +121,22 @@ QB_API int quantize_act(int block, const float *x, int64_t K, int ncols, int8_t 
 QB_API int q_gemv(qb_fmt fmt, const void *W, int64_t rows, int64_t K, const qb_act *act, int ncols, float *out,
            void *stream);
 
+/* Bytes of the workspace q_matvec needs for a K x ncols activation: its
+ * quantized form (codes, scales, unit sums; or the f16 rounding for QB_F16),
+ * each part 16-byte aligned.  Negative QB_E_* for bad arguments. */
+QB_API int64_t q_matvec_workspace_bytes(qb_fmt fmt, int64_t K, int ncols);
+
+/* The whole product from an f32 activation: quantize_act (or
+ * quantize_act_f16) then q_gemv (or q_gemv_f16), out[c*rows + r], bit for bit
+ * the same results.  For one column of a Q8_0/Q4_K/Q6_K matrix with
+ * K % 256 == 0 it is a single launch that quantizes the activation inside the
+ * product kernel and needs no workspace (`workspace` may be NULL); otherwise
+ * `workspace` must be device memory of at least q_matvec_workspace_bytes()
+ * bytes, 16-byte aligned, owned by the caller and not used by another call
+ * while this one runs.  x must be 16-byte aligned. */
+QB_API int q_matvec(qb_fmt fmt, const void *W, int64_t rows, int64_t K, const float *x, int ncols, float *out,
+                    void *workspace, size_t workspace_bytes, void *stream);
+
 /* f32_to_f16 (numerics page) over x f32 [ncols][K]: round to nearest even,
  * subnormals kept, past the top infinite; NaN becomes 0x7E00. */
 QB_API int quantize_act_f16(const float *x, int64_t K, int ncols, uint16_t *x16, void *stream);

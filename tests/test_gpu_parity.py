@@ -351,3 +351,77 @@ def test_f16_sixteen_columns_and_nonfinite():
     qb.q_gemv_f16(dev(W), rows, K, dev(x16.view(np.int16)), 16, out)
     torch.cuda.synchronize()
     assert np.array_equal(bits(host(out)), bits(want))
+
+
+# ---------------------------------------------------------------- q_matvec (one call from f32)
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("ncols", [1, 3])
+@pytest.mark.parametrize("rows,K", [(261, 4096), (1000, 1024), (7, 256), (152 * 3 + 5, 2048)])
+def test_matvec_bit_exact(fmt, ncols, rows, K):
+    """q_matvec -- in one launch for one column (the activation quantized inside
+    the product kernel), through a workspace otherwise -- equals the oracle's
+    quantize_blocks + dot, including activation blocks that are zero, hold a
+    NaN, a denormal or an infinity."""
+    import torch
+    blk = synth.BLOCK[fmt]
+    x = _edge_activation(ncols, K, blk, seed=rows + K + ncols + fmt)
+    rng = np.random.default_rng(rows * 3 + fmt)
+    lg = synth.draw(fmt, rng, rows, K)
+    W = synth.pack(fmt, lg)
+    codes, m, e, s16, packed = oracle_act(x, blk)
+    want = oracle.gemv(fmt, W, rows, K, codes, m, e)
+    out = torch.full((ncols, rows), float("nan"), dtype=torch.float32, device="cuda")
+    ws = torch.empty(qb.q_matvec_workspace_bytes(fmt, K, ncols), dtype=torch.uint8, device="cuda")
+    qb.q_matvec(fmt, dev(W), rows, K, dev(x), out, workspace=ws if ncols > 1 else None)
+    torch.cuda.synchronize()
+    assert np.array_equal(bits(host(out)), bits(want))
+    if ncols > 1:
+        with pytest.raises(qb.QbError):
+            qb.q_matvec(fmt, dev(W), rows, K, dev(x), out, workspace=None)
+
+
+def test_matvec_repeated_launches_graph():
+    """Many single-launch products back to back (programmatic dependent launch
+    overlapping each launch's weight stream with the previous one) on distinct
+    weights and activations, replayed from a CUDA graph: every output exact."""
+    import torch
+    rng = np.random.default_rng(99)
+    rows, K, n = 777, 4096, 6
+    Ws = [synth.pack_q4k(**synth.draw_q4k(rng, rows, K)) for _ in range(n)]
+    xs = [synth.draw_act(rng, 1, K, outlier_frac=0.001) for _ in range(n)]
+    Wd = [dev(w) for w in Ws]
+    xd = [dev(x) for x in xs]
+    outs = [torch.empty((1, rows), dtype=torch.float32, device="cuda") for _ in range(n)]
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        qb.q_matvec(qb.Q4K, Wd[0], rows, K, xd[0], outs[0], stream=s)
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        g.capture_begin()
+        for i in range(n):
+            qb.q_matvec(qb.Q4K, Wd[i], rows, K, xd[i], outs[i], stream=s)
+        g.capture_end()
+    for o in outs:
+        o.fill_(float("nan"))
+    g.replay()
+    s.synchronize()
+    for i in range(n):
+        codes, m, e, _, _ = oracle_act(xs[i], 256)
+        want = oracle.gemv(synth.FMT_Q4K, Ws[i], rows, K, codes, m, e)
+        assert np.array_equal(bits(host(outs[i])), bits(want)), i
+
+
+def test_matvec_f16():
+    import torch
+    rng = np.random.default_rng(4)
+    rows, K = 1536, 576
+    W = synth.draw_f16(rng, rows, K)
+    x = synth.draw_act(rng, 2, K)
+    want = oracle.gemv_f16(W, rows, K, oracle.quantize_f16(x))
+    out = torch.empty((2, rows), dtype=torch.float32, device="cuda")
+    ws = torch.empty(qb.q_matvec_workspace_bytes(qb.F16, K, 2), dtype=torch.uint8, device="cuda")
+    qb.q_matvec(qb.F16, dev(W), rows, K, dev(x), out, workspace=ws)
+    torch.cuda.synchronize()
+    assert np.array_equal(bits(host(out)), bits(want))
