@@ -7,12 +7,12 @@
  * never does.  It shares no code, header, table or helper with the CUDA path.
  *
  * Sources (the decode engine's documentation pages):
- *   numerics page  -- "The decode engine's arithmetic, bit for bit":
+ *   numerics page  -- the decode engine's numerics module page:
  *                     ActScaling::PerBlock, absmax, wide_scale, rne_div,
  *                     quantize_blocks, exact_sum, scaled_to_f32, dot, fdot,
  *                     tree, f32_to_f16, ftz, structs Scale / Segment /
  *                     CodedRow / Unreadable, constants NAN, COEF_BOUND.
- *   lane page       -- "The block-scale lane": block_sums, deliver, lane, and
+ *   lane page       -- its lane module page: block_sums, deliver, lane, and
  *                     the excess-form identity of the unit sums.
  *
  * Readings taken where the pages are silent (each restated where used):
