@@ -22,13 +22,16 @@ BLOCK = {Q8_0: 32, Q4K: 256, Q6K: 256}
 FORMATS = {"f16": F16, "q8_0": Q8_0, "q4k": Q4K, "q6k": Q6K}
 
 QB_OK, QB_E_ARG, QB_E_FORMAT, QB_E_BLOCK, QB_E_CUDA, QB_E_UNREADABLE, QB_E_DEVICE = 0, -1, -2, -3, -4, -5, -6
+QB_E_SCRATCH = -7
+STATIC_SCRATCH_BYTES = 1 << 20  # QB_STATIC_SCRATCH_BYTES
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libqgemv.so")
 
 # every entry point include/qgemv.h declares
 EXPORTS = ("quantize_act", "q_gemv", "quantize_act_f16", "q_gemv_f16", "q_check_weights", "q_weight_bytes",
-           "q_block_values", "q_device_status", "q_strerror", "q_matvec", "q_matvec_workspace_bytes")
+           "q_block_values", "q_device_status", "q_strerror", "q_matvec", "q_matvec_workspace_bytes",
+           "q_matvec_static")
 
 
 class QbError(RuntimeError):
@@ -67,6 +70,7 @@ def lib() -> ctypes.CDLL:
         L.q_matvec_workspace_bytes.argtypes, L.q_matvec_workspace_bytes.restype = [i32, i64, i32], i64
         L.q_matvec.argtypes = [i32, P, i64, i64, P, i32, P, P, ctypes.c_size_t, P]
         L.q_matvec.restype = i32
+        L.q_matvec_static.argtypes, L.q_matvec_static.restype = [i32, P, i64, i64, P, i32, P, P], i32
         _lib = L
     return _lib
 
@@ -173,6 +177,18 @@ def q_matvec(fmt: int, W, rows: int, K: int, x, out, workspace=None, stream=None
     nbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     _check(lib().q_matvec(fmt, _ptr(W), rows, K, _ptr(x), ncols, _ptr(out), _ptr(workspace), nbytes,
                           _stream(stream)), "q_matvec")
+
+
+def q_matvec_static(fmt: int, W, rows: int, K: int, x, out, stream=None) -> None:
+    """q_matvec for callers that cannot allocate device memory: the quantized
+    activation goes through a fixed 1 MiB array inside the library (no
+    workspace argument, nothing allocated).  Calls on one device share that
+    array, so calls that may run at the same time on the GPU must be ordered
+    (one stream, or events).  The first call on a device looks up the array's
+    address; make it before any stream capture."""
+    ncols = x.shape[0]
+    _check(lib().q_matvec_static(fmt, _ptr(W), rows, K, _ptr(x), ncols, _ptr(out), _stream(stream)),
+           "q_matvec_static")
 
 
 def matvec(fmt: int, W, rows: int, K: int, x, out=None, act=None, stream=None):

@@ -293,6 +293,7 @@ const char *q_strerror(int status) {
     case QB_E_CUDA: return "CUDA call or launch failed";
     case QB_E_UNREADABLE: return "weights hold an infinite or NaN block scale";
     case QB_E_DEVICE: return "a kernel gave up a bounded wait";
+    case QB_E_SCRATCH: return "request needs more than the library's static scratch (QB_STATIC_SCRATCH_BYTES)";
     default: return "unknown status";
     }
 }

@@ -83,8 +83,12 @@ enum {
     QB_E_BLOCK = -3,      /* act->block differs from the format's block */
     QB_E_CUDA = -4,       /* a CUDA call or launch failed */
     QB_E_UNREADABLE = -5, /* q_check_weights found an inf/NaN block scale (numerics page, Unreadable) */
-    QB_E_DEVICE = -6      /* a kernel gave up a bounded wait (q_device_status) */
+    QB_E_DEVICE = -6,     /* a kernel gave up a bounded wait (q_device_status) */
+    QB_E_SCRATCH = -7     /* q_matvec_static: the request needs more than the library's static scratch */
 };
+
+/* Size of the library's static scratch array used by q_matvec_static. */
+#define QB_STATIC_SCRATCH_BYTES (1 << 20)
 
 /* An activation block's scale m*2^e, m in 128..255 (numerics page, ActScale
  * under PerBlock).  m == 0 marks a block holding an infinity: it has no scale,
@@ -136,6 +140,30 @@ QB_API int64_t q_matvec_workspace_bytes(qb_fmt fmt, int64_t K, int ncols);
  * while this one runs.  x must be 16-byte aligned. */
 QB_API int q_matvec(qb_fmt fmt, const void *W, int64_t rows, int64_t K, const float *x, int ncols, float *out,
                     void *workspace, size_t workspace_bytes, void *stream);
+
+/* q_matvec for callers that cannot allocate device memory -- for example a
+ * serving process whose device memory all belongs to its own pool after
+ * start-up, or a latency-critical loop that must not call cudaMalloc (it can
+ * synchronize the device).  (The pages have no counterpart: this is a usage
+ * variant, not part of the method.)  Same arguments and results as q_matvec
+ * without the workspace: the quantized activation always goes through a
+ * QB_STATIC_SCRATCH_BYTES (1 MiB) array inside the library, in two launches
+ * (quantize, then multiply).  A request whose q_matvec_workspace_bytes()
+ * exceeds that returns QB_E_SCRATCH and launches nothing.  Nothing is
+ * allocated, by the library or by any routine it calls.
+ * - Set-up: the first call on a device (with that device current) looks up
+ *   the array's device address (cudaGetSymbolAddress) and caches it; make
+ *   that first call before any stream capture.
+ * - Sharing: every call on a device uses the same array.  Its contents are
+ *   whatever the last call left; nothing in it needs to start at zero, since
+ *   each call writes all of the quantized activation it then reads.  Calls
+ *   whose launches may overlap on the GPU (different streams, or different
+ *   host threads, without ordering between them) race on the array; order them
+ *   on one stream or with events.
+ * - The array lives on every GPU that loads the library until the process
+ *   exits. */
+QB_API int q_matvec_static(qb_fmt fmt, const void *W, int64_t rows, int64_t K, const float *x, int ncols,
+                           float *out, void *stream);
 
 /* f32_to_f16 (numerics page) over x f32 [ncols][K]: round to nearest even,
  * subnormals kept, past the top infinite; NaN becomes 0x7E00. */
