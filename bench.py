@@ -221,19 +221,27 @@ def run_ours(args, rank, world):
         ms = float(t.item())
     clocks = clk.summary()
 
-    # ---- roofline: the product kernel alone, live, over rotating copies
-    n_roof = args.roof_launches
-    g_roof = capture(gemv_only, n_roof)
-    with torch.cuda.stream(stream):
-        g_roof.replay()
-        e0.record(stream)
-        for _ in range(3):
+    # ---- roofline: the step's dominant kernel, live, over rotating copies.  For a
+    # single-launch step that is the step's own kernel (reading the f32
+    # activation); otherwise the product kernel.  The product kernel alone (a
+    # pre-quantized activation) is timed too, as context.
+    def time_launches(fn):
+        n_roof = args.roof_launches
+        g_roof = capture(fn, n_roof)
+        with torch.cuda.stream(stream):
             g_roof.replay()
-        e1.record(stream)
-    stream.synchronize()
-    per_launch_s = e0.elapsed_time(e1) / 1e3 / (3 * n_roof)
+            e0.record(stream)
+            for _ in range(3):
+                g_roof.replay()
+            e1.record(stream)
+        stream.synchronize()
+        return e0.elapsed_time(e1) / 1e3 / (3 * n_roof)
+
+    prod_s = time_launches(gemv_only)
+    per_launch_s = time_launches(step) if single else prod_s
+    roof_bytes = (wbytes + 4 * K * ncols + 4 * rows * ncols) if single else abytes
     peak, peak_kind = measured_peaks()
-    achieved = abytes / per_launch_s / 1e9
+    achieved = roof_bytes / per_launch_s / 1e9
     traffic = None
     tp = os.path.join(ROOT, "profiles", "traffic.json")
     if os.path.exists(tp):
@@ -304,7 +312,7 @@ def run_ours(args, rank, world):
         "roofline": {
             "bound": "hbm",
             "kernel": ("gemv_f16_kernel" if fmt == synth.FMT_F16 else
-                       f"gemv2_kernel<{synth.FORMAT_NAMES[fmt]}> (streaming, one column)" if single else
+                       f"gemv2_kernel<{synth.FORMAT_NAMES[fmt]}, single launch> (quantize + product)" if single else
                        f"gemv_kernel<{synth.FORMAT_NAMES[fmt]}, {ncols} columns>"),
             "achieved": round(achieved, 1),
             "peak": peak,
@@ -312,9 +320,13 @@ def run_ours(args, rank, world):
             "unit": "GB/s",
             "frac": round(achieved / peak, 4),
             "traffic": traffic,
-            "algorithmic_bytes_per_launch": abytes,
+            "algorithmic_bytes_per_launch": roof_bytes,
             "avg_launch_us": round(per_launch_s * 1e6, 4),
-            "launches_timed": 3 * n_roof,
+            "launches_timed": 3 * args.roof_launches,
+            "product_kernel_only": {"avg_launch_us": round(prod_s * 1e6, 4),
+                                    "achieved_gbs": round(abytes / prod_s / 1e9, 1),
+                                    "frac": round(abytes / prod_s / 1e9 / peak, 4),
+                                    "note": "activation quantized beforehand (q_gemv)"},
         },
         "e2e": {
             "value": round(world * wbytes * n_e2e / e2e_s / 1e9, 2),
