@@ -235,8 +235,12 @@ __device__ __forceinline__ void issue_fill(const Gemv2K &p, uint8_t *ring, uint6
     if (bytes) bulk_g2s(ring + (int64_t)slot * 2 * p.nt * p.rec, p.W + (row0 + first) * p.rec, bytes, bars + slot);
 }
 
+// Two CTAs per SM (<= 64 registers) for the product with a staged activation,
+// so a following launch's CTA fits beside this one and streams its weights
+// early; one (more registers, more overlap inside a warp) for the
+// single-launch form, which measures faster that way.
 template <int F, bool FUSED>
-__global__ void __launch_bounds__(512, 2) gemv2_kernel(const Gemv2K p) {
+__global__ void __launch_bounds__(512, FUSED ? 1 : 2) gemv2_kernel(const Gemv2K p) {
     extern __shared__ __align__(128) uint8_t smem[];
     const Gemv2Smem L = gemv2_smem(p.K, p.rec, p.nt, p.D, p.H, p.vstride);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L.bars);
@@ -378,13 +382,14 @@ __global__ void __launch_bounds__(512, 2) gemv2_kernel(const Gemv2K p) {
                                             : make_uint4(0, 0, 0, 0);
 
     // ---- the row loop: two rows per team per iteration
+    int hpos = 0;  // iterations of block values held since the last fold
     for (int it = 0; it < p.n_iter; ++it) {
         const int slot = it % p.D;
         const int64_t lA = (int64_t)it * 2 * p.nt + 2 * team;  // row index within the CTA's range
         const bool haveA = live && lA < count, hasB = live && lA + 1 < count;
         const uint8_t *rA = ring + ((int64_t)(slot * p.nt + team) * 2) * p.rec;
         const uint8_t *rB = rA + p.rec;
-        float *vA = val + (((it % p.H) * p.nt + team) * 2) * p.vstride;
+        float *vA = val + ((hpos * p.nt + team) * 2) * p.vstride;
         float *vB = vA + p.vstride;
         bool ok = true;
         if (haveA) ok = mbar_wait_bounded(bars + slot, (uint32_t)((it / p.D) & 1), p.fault);
@@ -429,14 +434,12 @@ __global__ void __launch_bounds__(512, 2) gemv2_kernel(const Gemv2K p) {
             issue_fill(p, ring, bars, it + p.D, row0, count);
         }
         // ---- fold H iterations' rows: one thread per row, blocks in order
-        // (rows of teams wider than a warp, and Q8_0 rows)
-        if ((it % p.H) == p.H - 1 || it == p.n_iter - 1) {
-            const int h0 = it - (it % p.H);
-            const int nline = (it - h0 + 1) * p.nt * 2;
-            for (int f = tid; f < nline; f += blockDim.x) {
-                const int64_t l = (int64_t)h0 * 2 * p.nt + f;  // line f holds row l of the CTA's range
+        if (++hpos == p.H || it == p.n_iter - 1) {
+            const int nline = hpos * p.nt * 2;
+            if (tid < nline) {
+                const int64_t l = (int64_t)(it + 1 - hpos) * 2 * p.nt + tid;  // row of the CTA's range
                 if (l < count) {
-                    const float4 *v4 = reinterpret_cast<const float4 *>(val + (int64_t)f * p.vstride);
+                    const float4 *v4 = reinterpret_cast<const float4 *>(val + tid * p.vstride);
                     float acc = 0.0f;
                     const int n4 = p.nb >> 2;
                     int q = 0;
@@ -451,19 +454,18 @@ __global__ void __launch_bounds__(512, 2) gemv2_kernel(const Gemv2K p) {
                         const float4 x = v4[q];
                         acc = fadd_ftz(fadd_ftz(fadd_ftz(fadd_ftz(acc, x.x), x.y), x.z), x.w);
                     }
-                    const float *vt = val + (int64_t)f * p.vstride;
+                    const float *vt = val + tid * p.vstride;
                     for (int b = 4 * n4; b < p.nb; ++b) acc = fadd_ftz(acc, vt[b]);
                     if (acc != acc) acc = __uint_as_float(kEngineNaN);
                     p.out[row0 + l] = acc;
                 }
             }
-            __syncthreads();  // before the history is overwritten
+            hpos = 0;
+            if (it != p.n_iter - 1) __syncthreads();  // before the history is overwritten
         }
     }
 }
 
-// Host: the launch shape.  Returns QB_E_ARG when the streaming kernel does not
-// apply (the caller then uses the general kernel).
 template <int F>
 int launch_gemv2(const GemvArgs &a, cudaStream_t stream, const float *x = nullptr) {
     if (a.ncols != 1 || a.mode != 0 || a.K % 256 != 0) return QB_E_ARG;
@@ -494,7 +496,7 @@ int launch_gemv2(const GemvArgs &a, cudaStream_t stream, const float *x = nullpt
     k.base = a.rows / grid;
     k.rem = a.rows % grid;
     const int slot = 2 * k.nt * k.rec;
-    k.H = std::max(1, std::min(k.n_iter, 8));
+    k.H = std::max(1, std::min({k.n_iter, 8, ts / 2}));  // one fold line per thread: H * 2 * nt <= nt * ts
     k.D = std::max(1, std::min(k.n_iter, 98304 / std::max(1, slot)));
     if (k.D < 2 && k.n_iter > 1) k.D = 2;
     k.codes = a.codes;
