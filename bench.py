@@ -349,26 +349,35 @@ def _oracle_threads():
     return max(1, os.cpu_count() or 1)
 
 
+_POOL = None
+
+
+def _pool(n):
+    global _POOL
+    if _POOL is None:
+        import concurrent.futures as cf
+        _POOL = cf.ThreadPoolExecutor(n)
+    return _POOL
+
+
 def oracle_pass(fmt, rows, K, Wh, x, nthreads, row_limit=None):
     """quantize + product over (a sample of) rows, rows split across threads
     (ctypes releases the GIL; the oracle is reentrant)."""
-    import concurrent.futures as cf
     import oracle
     r_end = rows if row_limit is None else min(rows, row_limit)
+    ex = _pool(nthreads)
     if fmt == synth.FMT_F16:
         x16 = oracle.quantize_f16(x)
         W16 = Wh.view(np.uint16).reshape(rows, K)[:r_end]
         chunks = np.array_split(np.arange(r_end), nthreads)
-        with cf.ThreadPoolExecutor(nthreads) as ex:
-            list(ex.map(lambda c: oracle.gemv_f16(np.ascontiguousarray(W16[c]), len(c), K, x16)
-                        if len(c) else None, chunks))
+        list(ex.map(lambda c: oracle.gemv_f16(np.ascontiguousarray(W16[c]), len(c), K, x16)
+                    if len(c) else None, chunks))
         return r_end
     codes, m, e, _ = oracle.quantize_blocks(x, synth.BLOCK[fmt])
     out = np.zeros((x.shape[0], rows), np.float32)
     bounds = np.linspace(0, r_end, nthreads + 1).astype(int)
-    with cf.ThreadPoolExecutor(nthreads) as ex:
-        list(ex.map(lambda i: oracle.gemv(fmt, Wh, rows, K, codes, m, e, int(bounds[i]), int(bounds[i + 1]), out),
-                    range(nthreads)))
+    list(ex.map(lambda i: oracle.gemv(fmt, Wh, rows, K, codes, m, e, int(bounds[i]), int(bounds[i + 1]), out),
+                range(nthreads)))
     return r_end
 
 

@@ -490,14 +490,22 @@ int launch_gemv2(const GemvArgs &a, cudaStream_t stream, const float *x = nullpt
     const int64_t rpc = (a.rows + grid - 1) / grid;  // most rows any CTA owns
     const int64_t need = (rpc + 1) / 2;
     k.nt = (int)std::min<int64_t>(max_nt, std::max<int64_t>(1, need));
-    if (k.nt < need) k.nt = std::min(k.nt, std::max(1, 49152 / (2 * k.rec)));
-    if (x) k.nt = std::max(k.nt, std::min(16, max_nt));  // the in-kernel quantizer: one 8-element group a thread
+    const bool multi = k.nt < need;  // more than one iteration per CTA
+    // Shared memory: a single-iteration product with a staged activation stays
+    // under ~110 KB so the next launch's CTA fits beside it and streams early;
+    // otherwise the whole 225 KB serves a two-slot ring with as many teams as fit.
+    const int fixed = gemv2_smem(K, k.rec, 0, 0, 1, k.vstride).total + 8 * 2 * 20 * 4 * 16;
+    const int budget = (x || multi) ? 225 * 1024 : 110 * 1024;
+    if (multi) k.nt = std::min(k.nt, std::max(1, (budget - fixed) / (2 * 2 * k.rec)));
+    // the in-kernel quantizer needs K/8 <= 4 * threads (nt >= 4); one 8-element
+    // group a thread (nt >= 16) is fastest
+    if (x) k.nt = std::max(k.nt, std::min(multi ? 4 : 16, max_nt));
     k.n_iter = (int)((rpc + 2LL * k.nt - 1) / (2LL * k.nt));
     k.base = a.rows / grid;
     k.rem = a.rows % grid;
     const int slot = 2 * k.nt * k.rec;
     k.H = std::max(1, std::min({k.n_iter, 8, ts / 2}));  // one fold line per thread: H * 2 * nt <= nt * ts
-    k.D = std::max(1, std::min(k.n_iter, 98304 / std::max(1, slot)));
+    k.D = std::max(1, std::min({k.n_iter, 4, (budget - fixed) / std::max(1, slot)}));
     if (k.D < 2 && k.n_iter > 1) k.D = 2;
     k.codes = a.codes;
     k.scales = a.scales;
@@ -507,7 +515,7 @@ int launch_gemv2(const GemvArgs &a, cudaStream_t stream, const float *x = nullpt
     k.fault = fault_word();
     if (!k.fault) return QB_E_CUDA;
     Gemv2Smem L = gemv2_smem(K, k.rec, k.nt, k.D, k.H, k.vstride);
-    while (L.total > 200 * 1024 && (k.D > 1 || k.H > 1)) {
+    while (L.total > 225 * 1024 && (k.D > 1 || k.H > 1)) {
         if (k.D > 1) --k.D; else --k.H;
         L = gemv2_smem(K, k.rec, k.nt, k.D, k.H, k.vstride);
     }

@@ -1,21 +1,133 @@
 // qb_gemv_f16.cu -- F16 weights against an f16-rounded activation (numerics
-// page, fdot / tree / f32_to_f16).
+// page: fdot, tree, f32_to_f16).
 //
-// Each thread owns one row and keeps its 8 lane accumulators in registers:
-// element i's product -- exact in f32, since two binary16 values multiply to
-// at most 22 significant bits -- is added to lane i mod 8 in index order from
-// +0, and the lanes fold as ((l0+l1)+(l2+l3))+((l4+l5)+(l6+l7)).  An FMA of an
-// exact product rounds exactly as the separate multiply and add do.  The
-// activation, widened to f32 (exactly), sits in shared memory and is read as
-// broadcasts; the row streams through 16-byte non-coherent loads, four in
-// flight per thread.
+// Element i's product -- exact in f32, since two binary16 values multiply to at
+// most 22 significant bits -- goes to lane i mod 8, each lane adding in index
+// order from +0; the lanes fold as ((l0+l1)+(l2+l3))+((l4+l5)+(l6+l7)).  An FMA
+// of an exact product rounds exactly as the separate multiply and add do.
+//
+// Streaming organisation (persistent CTAs, one per SM):
+//   * a CTA owns a contiguous range of rows; they reach shared memory through
+//     a ring of D slots of R rows, one bulk asynchronous copy per row (the TMA
+//     engine) into a row pitch padded to an odd number of 16-B units, so the
+//     threads reading consecutive rows hit different banks; the first fills
+//     are issued before the programmatic-dependent-launch wait;
+//   * four threads per row: thread p owns lanes 2p and 2p+1 for every column
+//     and walks the row's 16-byte chunks in order (chunk c holds elements
+//     8c..8c+7, one per lane), so each lane's sum keeps index order;
+//   * the tree is finished with two shuffles: (l0+l1) + (l2+l3) on the pair of
+//     threads 0,1, (l4+l5) + (l6+l7) on 2,3, then the two halves.
 #include <cuda_fp16.h>
+
+#include <algorithm>
 
 #include "qb_common.cuh"
 #include "qb_launch.h"
 
 namespace qb {
 
+struct F16K {
+    const uint16_t *W;
+    int64_t rows;
+    int K;
+    int pitch;     // bytes per row in shared memory (2K padded)
+    int R;         // rows per ring slot
+    int D;         // ring slots
+    int n_iter;    // slots a CTA consumes
+    int64_t base;  // rows per CTA, and how many CTAs own one more
+    int64_t rem;
+    const uint16_t *x16;
+    float *out;
+    int *fault;
+};
+
+__host__ __device__ inline int f16_xs_bytes(int K, int nc) { return (nc * K * 4 + 127) & ~127; }
+
+// rows of iteration `it` into slot it % D: one bulk copy per row
+__device__ __forceinline__ void f16_fill(const F16K &p, uint8_t *ring, uint64_t *bars, int it, int64_t row0,
+                                         int64_t count, int lane) {
+    const int slot = it % p.D;
+    const int64_t first = (int64_t)it * p.R;
+    const int n = (int)((count - first < p.R) ? count - first : (int64_t)p.R);
+    if (lane == 0) mbar_arrive_expect_tx(bars + slot, n > 0 ? (uint32_t)n * (uint32_t)(2 * p.K) : 0u);
+    __syncwarp();
+    for (int r = lane; r < n; r += 32)
+        bulk_g2s(ring + ((int64_t)slot * p.R + r) * p.pitch, p.W + (row0 + first + r) * p.K, (uint32_t)(2 * p.K),
+                 bars + slot);
+}
+
+template <int NC>
+__global__ void __launch_bounds__(256) gemv_f16_kernel(const F16K p) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem);
+    float *xs = reinterpret_cast<float *>(smem + 128);  // [NC][K], exact widening of x16
+    uint8_t *ring = smem + 128 + f16_xs_bytes(p.K, NC);
+
+    const int tid = threadIdx.x, lane = tid & 31;
+    const int rr = tid >> 2, pp = tid & 3;  // row within the slot, lane pair
+    const int64_t c = blockIdx.x;
+    const int64_t row0 = c * p.base + (c < p.rem ? c : p.rem);
+    const int64_t count = p.base + (c < p.rem ? 1 : 0);
+
+    if (tid == 0) {
+        for (int s = 0; s < p.D; ++s) mbar_init(bars + s, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (tid < 32)
+        for (int it = 0; it < p.D && it < p.n_iter; ++it) f16_fill(p, ring, bars, it, row0, count, lane);
+    pdl_wait();
+    for (int i = tid; i < NC * p.K; i += blockDim.x) xs[i] = __half2float(__ushort_as_half(p.x16[i]));
+    __syncthreads();
+    pdl_launch_dependents();
+
+    const int n8 = p.K / 8;
+    for (int it = 0; it < p.n_iter; ++it) {
+        const int slot = it % p.D;
+        const int64_t l = (int64_t)it * p.R + rr;  // row within the CTA's range
+        const bool have = l < count;
+        bool ok = true;
+        if (have) ok = mbar_wait_bounded(bars + slot, (uint32_t)((it / p.D) & 1), p.fault);
+        float acc0[NC], acc1[NC];
+#pragma unroll
+        for (int q = 0; q < NC; ++q) { acc0[q] = 0.0f; acc1[q] = 0.0f; }
+        if (have && ok) {
+            const uint32_t *wr = reinterpret_cast<const uint32_t *>(ring + ((int64_t)slot * p.R + rr) * p.pitch) + pp;
+#pragma unroll 4
+            for (int k = 0; k < n8; ++k) {
+                const uint32_t w2 = wr[4 * k];  // elements 8k+2pp, 8k+2pp+1: lanes 2pp, 2pp+1
+                const float2 wf = __half22float2(*reinterpret_cast<const __half2 *>(&w2));
+#pragma unroll
+                for (int q = 0; q < NC; ++q) {
+                    const float2 xv = *reinterpret_cast<const float2 *>(xs + q * p.K + 8 * k + 2 * pp);
+                    acc0[q] = fmaf(wf.x, xv.x, acc0[q]);
+                    acc1[q] = fmaf(wf.y, xv.y, acc1[q]);
+                }
+            }
+        }
+        // tree: thread pp holds lanes (2pp, 2pp+1)
+#pragma unroll
+        for (int q = 0; q < NC; ++q) {
+            const float pair = __fadd_rn(acc0[q], acc1[q]);              // (l0+l1), (l2+l3), (l4+l5), (l6+l7)
+            const float quad = __fadd_rn(pair, __shfl_xor_sync(0xFFFFFFFFu, pair, 1));  // on even pp
+            const float all = __fadd_rn(quad, __shfl_xor_sync(0xFFFFFFFFu, quad, 2));   // on pp == 0
+            if (have && ok && pp == 0) {
+                float r = all;
+                if (r != r) r = __uint_as_float(kEngineNaN);
+                p.out[(int64_t)q * p.rows + row0 + l] = r;
+            }
+        }
+        if (!__syncthreads_and(ok)) return;  // a fill never completed: fault word raised
+        if (tid < 32 && it + p.D < p.n_iter) {
+            if (tid == 0) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+            f16_fill(p, ring, bars, it + p.D, row0, count, lane);
+        }
+    }
+}
+
+// Rows longer than the streaming kernel's shared-memory ring allows: one
+// thread per row, the row read straight from global memory in 16-byte chunks.
 __device__ __forceinline__ uint4 ldg_nc16(const void *p) {
     uint4 v;
     asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
@@ -35,7 +147,7 @@ __device__ __forceinline__ void widen8(const uint4 w, float (&f)[8]) {
 }
 
 template <int NC>
-__global__ void __launch_bounds__(128) gemv_f16_kernel(const uint16_t *__restrict__ W, int64_t rows, int K,
+__global__ void __launch_bounds__(128) gemv_f16_rowthread_kernel(const uint16_t *__restrict__ W, int64_t rows, int K,
                                                        const uint16_t *__restrict__ x16, float *__restrict__ out) {
     extern __shared__ __align__(16) float xs[];  // [NC][K], exact widening of x16
     const int64_t row = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -85,9 +197,22 @@ __global__ void __launch_bounds__(128) gemv_f16_kernel(const uint16_t *__restric
 }
 
 template <int NC>
-static int launch_f16_nc(const uint16_t *W, int64_t rows, int64_t K, const uint16_t *x16, float *out,
-                         cudaStream_t stream) {
+static int launch_f16_rowthread(const uint16_t *W, int64_t rows, int64_t K, const uint16_t *x16, float *out,
+                                cudaStream_t stream) {
     const size_t smem = (size_t)NC * K * sizeof(float);
+    static bool attr_set = false;
+    if (!attr_set) {
+        if (cudaFuncSetAttribute(gemv_f16_rowthread_kernel<NC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 227 * 1024) != cudaSuccess)
+            return QB_E_CUDA;
+        attr_set = true;
+    }
+    const unsigned grid = (unsigned)((rows + 127) / 128);
+    return launch_pdl(gemv_f16_rowthread_kernel<NC>, dim3(grid), dim3(128), smem, stream, W, rows, (int)K, x16, out);
+}
+
+template <int NC>
+static int launch_f16_nc(const F16K &k, int smem, unsigned grid, int threads, cudaStream_t stream) {
     static bool attr_set = false;
     if (!attr_set) {
         if (cudaFuncSetAttribute(gemv_f16_kernel<NC>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) !=
@@ -95,16 +220,48 @@ static int launch_f16_nc(const uint16_t *W, int64_t rows, int64_t K, const uint1
             return QB_E_CUDA;
         attr_set = true;
     }
-    const unsigned grid = (unsigned)((rows + 127) / 128);
-    return launch_pdl(gemv_f16_kernel<NC>, dim3(grid), dim3(128), smem, stream, W, rows, (int)K, x16, out);
+    return launch_pdl(gemv_f16_kernel<NC>, dim3(grid), dim3(threads), (size_t)smem, stream, k);
 }
 
 int launch_gemv_f16(const uint16_t *W, int64_t rows, int64_t K, const uint16_t *x16, int ncols, float *out,
                     cudaStream_t stream) {
-    if ((int64_t)ncols * K * 4 > 227 * 1024) return QB_E_ARG;
+    F16K k;
+    k.W = W;
+    k.rows = rows;
+    k.K = (int)K;
+    const int units = (int)(K / 8);  // 16-B units per row
+    k.pitch = 16 * (units + ((units & 1) ? 2 : 1));  // odd number of units
+    const int sms = num_sms();
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(sms, (rows + 31) / 32));
+    k.base = rows / grid;
+    k.rem = rows % grid;
+    const int64_t rpc = (rows + grid - 1) / grid;
+    const int xsb = f16_xs_bytes((int)K, ncols);
+    const int budget = 200 * 1024 - 128 - xsb;
+    if (budget < 8 * k.pitch) {  // a slot of 8 rows does not fit: the row-per-thread kernel
+        switch (ncols) {
+#define QB_CASE(N) \
+    case N: return launch_f16_rowthread<N>(W, rows, K, x16, out, stream);
+            QB_CASE(1) QB_CASE(2) QB_CASE(3) QB_CASE(4) QB_CASE(5) QB_CASE(6) QB_CASE(7) QB_CASE(8)
+            QB_CASE(9) QB_CASE(10) QB_CASE(11) QB_CASE(12) QB_CASE(13) QB_CASE(14) QB_CASE(15) QB_CASE(16)
+#undef QB_CASE
+        }
+        return QB_E_ARG;
+    }
+    // rows per slot: a multiple of 8 (whole warps), at most 64, at least two slots
+    k.R = (int)std::min<int64_t>(64, std::max<int64_t>(8, (rpc + 7) / 8 * 8));
+    while (k.R > 8 && 2 * k.R * k.pitch > budget) k.R -= 8;
+    k.n_iter = (int)((rpc + k.R - 1) / k.R);
+    k.D = std::max(1, std::min(k.n_iter, std::min(4, budget / (k.R * k.pitch))));
+    k.x16 = x16;
+    k.out = out;
+    k.fault = fault_word();
+    if (!k.fault) return QB_E_CUDA;
+    const int smem = 128 + xsb + k.D * k.R * k.pitch;
+    const int threads = 4 * k.R;
     switch (ncols) {
 #define QB_CASE(N) \
-    case N: return launch_f16_nc<N>(W, rows, K, x16, out, stream);
+    case N: return launch_f16_nc<N>(k, smem, (unsigned)grid, threads, stream);
         QB_CASE(1) QB_CASE(2) QB_CASE(3) QB_CASE(4) QB_CASE(5) QB_CASE(6) QB_CASE(7) QB_CASE(8)
         QB_CASE(9) QB_CASE(10) QB_CASE(11) QB_CASE(12) QB_CASE(13) QB_CASE(14) QB_CASE(15) QB_CASE(16)
 #undef QB_CASE

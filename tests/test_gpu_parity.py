@@ -319,7 +319,8 @@ def test_quantize_act_f16_bit_exact():
     assert np.array_equal(host(g).view(np.uint16), want)
 
 
-@pytest.mark.parametrize("rows,K", [(49152, 576), (1536, 576), (13, 8), (129, 1536), (300, 64)])
+@pytest.mark.parametrize("rows,K", [(49152, 576), (1536, 576), (13, 8), (129, 1536), (300, 64), (40, 8192),
+                                    (1000, 56), (151 * 64 + 3, 128)])
 @pytest.mark.parametrize("ncols", [1, 2, 3, 6])
 def test_f16_gemv_bit_exact(rows, K, ncols):
     import torch
