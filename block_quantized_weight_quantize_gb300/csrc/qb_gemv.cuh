@@ -369,6 +369,10 @@ int dispatch_range(int nc, const GemvK &k, int threads, int smem, unsigned grid,
 }
 template <int F>
 int dispatch_hi(int nc, const GemvK &k, int threads, int smem, unsigned grid, cudaStream_t s);
+// The streaming kernel for 2..16 columns (qb_gemv3.cuh, instantiated in
+// qb_skinny_*.cu); QB_E_ARG when it does not apply to the shape.
+template <int F>
+int launch_skinny(const GemvArgs &a, cudaStream_t stream);
 
 inline int gcd_int(int a, int b) { while (b) { int t = a % b; a = b; b = t; } return a; }
 
@@ -380,6 +384,10 @@ int launch_gemv_fmt(const GemvArgs &a, cudaStream_t stream) {
     constexpr int blk = fmt_block(F);
     if (a.mode == 0 && a.ncols == 1) {  // the streaming kernel, where it applies
         const int rc = launch_gemv2<F>(a, stream);
+        if (rc != QB_E_ARG) return rc;
+    }
+    if (a.mode == 0 && a.ncols >= 2) {
+        const int rc = launch_skinny<F>(a, stream);
         if (rc != QB_E_ARG) return rc;
     }
     GemvK k;

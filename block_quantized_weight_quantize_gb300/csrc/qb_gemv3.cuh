@@ -1,0 +1,452 @@
+// qb_gemv3.cuh -- the streaming product kernel for 2..16 activation columns.
+//
+// The organisation of the one-column streaming kernel (qb_gemv2.cuh:
+// persistent CTAs over contiguous row ranges, teams of K/128 threads owning
+// 128-element half-slices of K, weights through a ring of bulk-copy slots,
+// two rows per team per iteration, in-order fold from shared memory), with the
+// columns split into groups of CG: a team is NCG groups of K/128 threads, and
+// thread (g, j) keeps the activation codes of columns CG*g .. CG*g+CG-1 over
+// half-slice j in registers (staged once per CTA through shared memory) and
+// reads each weight once for its CG columns.  Columns past the launch's count
+// (padding of the last group) run on zeros and are never written.  Per column
+// every block value and every row are the bits the one-column product gives:
+// the same integer sums, the same exact combine, the same fold order.
+//
+// A launch covers as many column groups as fit in one CTA; more columns take
+// further launches over the same weights (the weights then stream again; at
+// these column counts the integer work, not the weight stream, bounds the
+// product).
+#pragma once
+
+#include <algorithm>
+
+#include "qb_common.cuh"
+#include "qb_gemv2.cuh"
+#include "qb_launch.h"
+
+namespace qb {
+
+struct Gemv3K {
+    const uint8_t *W;
+    int64_t rows;
+    int K;
+    int rec;
+    int nt;     // teams per CTA
+    int ts;     // threads per group = K / 128 (one half-slice each)
+    int ncg;    // column groups per team
+    int ncols;  // real columns of this launch
+    int D;      // ring slots
+    int H;      // iterations of block values held before a fold
+    int nb;     // blocks per row
+    int vstride;
+    int n_iter;
+    int64_t base;
+    int64_t rem;
+    const int8_t *codes;  // column 0 of this launch
+    const qb_scale *scales;
+    const int16_t *sums16;
+    float *out;
+    int *fault;
+};
+
+struct Gemv3Smem {
+    int bars, act, val, ring, total;
+};
+
+// act: the launch's activation codes (ncols * K bytes); val: the block values
+// of H iterations; ring: D slots of 2*nt weight rows.
+__host__ __device__ inline Gemv3Smem gemv3_smem(int K, int ncols, int rec, int nt, int ncp, int D, int H,
+                                                int vstride) {
+    Gemv3Smem s;
+    s.bars = 0;
+    s.act = 128;
+    s.val = s.act + ((ncols * K + 127) & ~127);
+    s.ring = s.val + ((H * nt * 2 * ncp * vstride * 4 + 127) & ~127);
+    s.total = s.ring + D * nt * 2 * rec;
+    return s;
+}
+
+// Q4_K-like half block h for CG columns: 16*C[c] and O[c] over sub-blocks
+// 4h..4h+3.  a[c][k] holds unit 8j+k of column c.
+template <int CG>
+__device__ __forceinline__ void half_q4k_cg(const uint8_t *blk, int h, const uint4 (&a)[CG][8],
+                                            const uint32_t (&S)[CG][4], int (&C)[CG], int (&O)[CG], uint32_t &dd) {
+    const uint4 meta = *reinterpret_cast<const uint4 *>(blk);
+    dd = meta.x;
+    const unsigned long long sc48 = (unsigned long long)meta.y | ((unsigned long long)(meta.z & 0xFFFFu) << 32);
+    const unsigned long long mn48 = (unsigned long long)(meta.z >> 16) | ((unsigned long long)meta.w << 16);
+    const uint32_t scm = (uint32_t)(sc48 >> (24 * h)), mnm = (uint32_t)(mn48 >> (24 * h));
+    const uint8_t *qs = blk + 16 + 64 * h;
+#pragma unroll
+    for (int c = 0; c < CG; ++c) { C[c] = 0; O[c] = 0; }
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+        const uint4 w = *reinterpret_cast<const uint4 *>(qs + 16 * s);
+        // both nibbles as 16*q (the low one shifted up), so one chain of
+        // eight dp4a gives 16 * (the sub-block's sum); C is returned as 16*C
+        // (|16*C| <= 16 * 63 * 15 * 127 * 256 < 2^31 over a whole block)
+        const uint32_t l0 = (w.x << 4) & 0xF0F0F0F0u, l1 = (w.y << 4) & 0xF0F0F0F0u;
+        const uint32_t l2 = (w.z << 4) & 0xF0F0F0F0u, l3 = (w.w << 4) & 0xF0F0F0F0u;
+        const uint32_t g0 = w.x & 0xF0F0F0F0u, g1 = w.y & 0xF0F0F0F0u, g2 = w.z & 0xF0F0F0F0u, g3 = w.w & 0xF0F0F0F0u;
+        const int sc = (int)((scm >> (6 * s)) & 63u), mn = (int)((mnm >> (6 * s)) & 63u);
+#pragma unroll
+        for (int c = 0; c < CG; ++c) {
+            int p = dp4a_us(l0, a[c][2 * s].x, 0);
+            p = dp4a_us(l1, a[c][2 * s].y, p);
+            p = dp4a_us(l2, a[c][2 * s].z, p);
+            p = dp4a_us(l3, a[c][2 * s].w, p);
+            p = dp4a_us(g0, a[c][2 * s + 1].x, p);
+            p = dp4a_us(g1, a[c][2 * s + 1].y, p);
+            p = dp4a_us(g2, a[c][2 * s + 1].z, p);
+            p = dp4a_us(g3, a[c][2 * s + 1].w, p);
+            C[c] += sc * p;
+            O[c] += mn * (int)(int16_t)((S[c][s >> 1] >> (16 * (s & 1))) & 0xFFFFu);
+        }
+    }
+}
+
+// Q6_K-like half block h (32-element chunks 4h..4h+3) for CG columns.
+template <int CG>
+__device__ __forceinline__ void half_q6k_cg(const uint8_t *blk, int h, const uint4 (&a)[CG][8],
+                                            const uint32_t (&S)[CG][4], int (&C)[CG]) {
+    const uint2 scw = *reinterpret_cast<const uint2 *>(blk + 192 + 8 * h);
+#pragma unroll
+    for (int c = 0; c < CG; ++c) C[c] = 0;
+#pragma unroll
+    for (int ch = 0; ch < 4; ++ch) {
+        const uint4 w = *reinterpret_cast<const uint4 *>(blk + 64 * h + 16 * ch);
+        const uint2 hb = *reinterpret_cast<const uint2 *>(blk + 128 + 32 * h + 8 * ch);
+        const uint32_t wl[4] = {w.x, w.y, w.z, w.w};
+        uint32_t ql[4], qh[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const uint32_t hl = (k < 3) ? (hb.x << (4 - 2 * k)) : (hb.x >> 2);
+            const uint32_t hh = (k < 3) ? (hb.y << (4 - 2 * k)) : (hb.y >> 2);
+            ql[k] = (wl[k] & 0x0F0F0F0Fu) | (hl & 0x30303030u);
+            qh[k] = ((wl[k] >> 4) & 0x0F0F0F0Fu) | (hh & 0x30303030u);
+        }
+        const uint32_t sw = (ch < 2) ? scw.x : scw.y;
+        const int sc_lo = (int)(int8_t)((sw >> (16 * (ch & 1))) & 0xFFu);
+        const int sc_hi = (int)(int8_t)((sw >> (16 * (ch & 1) + 8)) & 0xFFu);
+#pragma unroll
+        for (int c = 0; c < CG; ++c) {
+            int pl = dp4a_ss(ql[0], a[c][2 * ch].x, 0);
+            pl = dp4a_ss(ql[1], a[c][2 * ch].y, pl);
+            pl = dp4a_ss(ql[2], a[c][2 * ch].z, pl);
+            pl = dp4a_ss(ql[3], a[c][2 * ch].w, pl);
+            int ph = dp4a_ss(qh[0], a[c][2 * ch + 1].x, 0);
+            ph = dp4a_ss(qh[1], a[c][2 * ch + 1].y, ph);
+            ph = dp4a_ss(qh[2], a[c][2 * ch + 1].z, ph);
+            ph = dp4a_ss(qh[3], a[c][2 * ch + 1].w, ph);
+            // sum over a unit of (q - 32) * a = sum q*a - 32 * S_u
+            C[c] += sc_lo * (pl - 32 * (int)(int16_t)(S[c][ch] & 0xFFFFu)) +
+                    sc_hi * (ph - 32 * (int)(int16_t)(S[c][ch] >> 16));
+        }
+    }
+}
+
+// Q8_0 half-slice (blocks 4j..4j+3) for CG columns.  The thread visits its
+// eight 16-B weight units in the order k ^ jj, so the eight lanes of a
+// shared-memory phase hit eight banks; a[c][k] holds unit 8j + (k ^ jj) of
+// column c to match.  Block i's value for column c goes to vl[c*vcol + i].
+template <int CG>
+__device__ __forceinline__ void half_q8_0_cg(const uint8_t *q, const uint8_t *dptr, const uint4 (&scl)[CG],
+                                             const uint4 (&a)[CG][8], int jj, float *vl, int vcol) {
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+        const int u0 = (2 * kk) ^ jj, u1 = u0 ^ 1;
+        const int i = u0 >> 1;
+        const uint4 w0 = *reinterpret_cast<const uint4 *>(q + 16 * u0);
+        const uint4 w1 = *reinterpret_cast<const uint4 *>(q + 16 * u1);
+        const uint32_t d = *reinterpret_cast<const uint16_t *>(dptr + 2 * i);
+#pragma unroll
+        for (int c = 0; c < CG; ++c) {
+            int p = dp4a_ss(w0.x, a[c][2 * kk].x, 0);
+            p = dp4a_ss(w0.y, a[c][2 * kk].y, p);
+            p = dp4a_ss(w0.z, a[c][2 * kk].z, p);
+            p = dp4a_ss(w0.w, a[c][2 * kk].w, p);
+            p = dp4a_ss(w1.x, a[c][2 * kk + 1].x, p);
+            p = dp4a_ss(w1.y, a[c][2 * kk + 1].y, p);
+            p = dp4a_ss(w1.z, a[c][2 * kk + 1].z, p);
+            p = dp4a_ss(w1.w, a[c][2 * kk + 1].w, p);
+            const uint32_t sw = i == 0 ? scl[c].x : i == 1 ? scl[c].y : i == 2 ? scl[c].z : scl[c].w;
+            vl[c * vcol + i] = lane_value_fast<0>(p, 0, d, 0, (int)(sw & 0xFFu), (int)(int16_t)(sw >> 16));
+        }
+    }
+}
+
+// Threads a CTA: two columns of codes (64 registers) fit 512 threads at the
+// 128-register bound; four would need 256 threads.
+template <int CG>
+constexpr int gemv3_threads() { return CG >= 4 ? 256 : 512; }
+
+template <int F, int CG>
+__global__ void __launch_bounds__(gemv3_threads<CG>(), 1) gemv3_kernel(const Gemv3K p) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int ncp = p.ncg * CG;  // padded columns
+    const Gemv3Smem L = gemv3_smem(p.K, p.ncols, p.rec, p.nt, ncp, p.D, p.H, p.vstride);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L.bars);
+    uint8_t *act = smem + L.act;
+    float *val = reinterpret_cast<float *>(smem + L.val);
+    uint8_t *ring = smem + L.ring;
+
+    const int tid = threadIdx.x;
+    const int tpt = p.ncg * p.ts;  // threads per team
+    const int team = tid / tpt, tr = tid - team * tpt;
+    const int g = tr / p.ts, j = tr - g * p.ts;
+    const bool live = team < p.nt;
+    const int sb = j >> 1, h = j & 1, jj = j & 7;
+
+    const int64_t cta = blockIdx.x;
+    const int64_t row0 = cta * p.base + (cta < p.rem ? cta : p.rem);
+    const int64_t count = p.base + (cta < p.rem ? 1 : 0);
+    const int64_t per_it = 2LL * p.nt;
+    if (tid == 0) {
+        for (int s = 0; s < p.D; ++s) mbar_init(bars + s, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    // the fill of iteration `it`: its rows are contiguous, one bulk copy into slot it % D
+    auto fill = [&](int it) {
+        const int slot = it % p.D;
+        const int64_t first = (int64_t)it * per_it;
+        const int64_t n = (count - first < per_it) ? count - first : per_it;
+        const uint32_t bytes = n > 0 ? (uint32_t)(n * p.rec) : 0u;
+        mbar_arrive_expect_tx(bars + slot, bytes);
+        if (bytes) bulk_g2s(ring + (int64_t)slot * per_it * p.rec, p.W + (row0 + first) * p.rec, bytes, bars + slot);
+    };
+    if (tid == 0)
+        for (int it = 0; it < p.D && it < p.n_iter; ++it) fill(it);  // weights depend on no earlier kernel
+    pdl_wait();
+
+    // ---- the activation codes of every column, once per CTA: coalesced
+    // loads, stored in shared memory with 16-B unit u of the launch's codes at
+    // (u & ~7) | ((u & 7) ^ ((u >> 3) & 7)) (Q8_0: at u), so that the register
+    // loads below hit eight banks per phase
+    {
+        const int nu = p.ncols * (p.K / 16);
+        const uint4 *src = reinterpret_cast<const uint4 *>(p.codes);
+        constexpr int kU = 4;
+        for (int u0 = tid; u0 < nu; u0 += kU * (int)blockDim.x) {
+            uint4 v[kU];
+#pragma unroll
+            for (int q = 0; q < kU; ++q) {
+                const int u = u0 + q * (int)blockDim.x;
+                v[q] = u < nu ? ldg_v4_ordered(src + u) : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int q = 0; q < kU; ++q) {
+                const int u = u0 + q * (int)blockDim.x;
+                const int pos = (F == kQ8_0) ? u : ((u & ~7) | ((u & 7) ^ ((u >> 3) & 7)));
+                if (u < nu) *reinterpret_cast<uint4 *>(act + 16 * pos) = v[q];
+            }
+        }
+    }
+    // my columns' unit sums and scales (global memory; small)
+    uint4 a[CG][8];
+    uint32_t S[CG][4];
+    uint4 scl[CG];  // Q8_0: the scales of blocks 4j..4j+3
+    int m0[CG], e0[CG];
+#pragma unroll
+    for (int c = 0; c < CG; ++c) {
+        const int col = g * CG + c;
+        const bool in = live && col < p.ncols;
+        S[c][0] = S[c][1] = S[c][2] = S[c][3] = 0;
+        scl[c] = make_uint4(128, 128, 128, 128);
+        m0[c] = 128;
+        e0[c] = 0;
+        if (in && F == kQ8_0) {
+            scl[c] = __ldg(reinterpret_cast<const uint4 *>(p.scales + (int64_t)col * (p.K / 32)) + j);
+        } else if (in) {
+            const uint4 sw = __ldg(reinterpret_cast<const uint4 *>(p.sums16 + (int64_t)col * (p.K / 16)) + j);
+            const uint32_t pw[4] = {sw.x, sw.y, sw.z, sw.w};
+            if (F == kQ4K) {  // per-32 sums of my four sub-blocks from the per-16 ones
+#pragma unroll
+                for (int s2 = 0; s2 < 4; ++s2) {
+                    const int Sv = (int)(int16_t)(pw[s2] & 0xFFFFu) + (int)(int16_t)(pw[s2] >> 16);
+                    S[c][s2 >> 1] |= ((uint32_t)Sv & 0xFFFFu) << (16 * (s2 & 1));
+                }
+            } else {
+                S[c][0] = pw[0]; S[c][1] = pw[1]; S[c][2] = pw[2]; S[c][3] = pw[3];
+            }
+            const uint32_t sv = __ldg(reinterpret_cast<const uint32_t *>(p.scales) + (int64_t)col * (p.K / 256) + sb);
+            m0[c] = (int)(sv & 0xFFu);
+            e0[c] = (int)(int16_t)(sv >> 16);
+        }
+    }
+    __syncthreads();
+    pdl_launch_dependents();
+    // codes of half-slice j (Q4_K/Q6_K: a[c][k] = unit 8j+k; Q8_0: unit 8j + (k ^ jj))
+#pragma unroll
+    for (int c = 0; c < CG; ++c) {
+        const int col = g * CG + c;
+        const bool in = live && col < p.ncols;
+        const uint8_t *base = act + (int64_t)col * p.K + 128 * j;
+        const int key = (F == kQ8_0) ? jj : ((col * p.ts + j) & 7);
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            a[c][k] = in ? *reinterpret_cast<const uint4 *>(base + 16 * (k ^ key)) : make_uint4(0, 0, 0, 0);
+    }
+
+    // value lines: [history][team][row A/B][padded column][vstride]
+    const int vcol = p.vstride;
+    int hpos = 0;
+    for (int it = 0; it < p.n_iter; ++it) {
+        const int slot = it % p.D;
+        const int64_t lA = (int64_t)it * per_it + 2 * team;  // row index within the CTA's range
+        const bool haveA = live && lA < count, hasB = live && lA + 1 < count;
+        const uint8_t *rA = ring + ((int64_t)(slot * p.nt + team) * 2) * p.rec;
+        const uint8_t *rB = rA + p.rec;
+        float *vA = val + (((hpos * p.nt + team) * 2) * ncp + g * CG) * p.vstride;
+        float *vB = vA + ncp * p.vstride;
+        bool ok = true;
+        if (haveA) ok = mbar_wait_bounded(bars + slot, (uint32_t)((it / p.D) & 1), p.fault);
+        const bool go = haveA && ok;
+        if (F == kQ8_0) {
+            if (go) {
+                half_q8_0_cg<CG>(rA + 128 * j, rA + p.K + 8 * j, scl, a, jj, vA + 4 * j, vcol);
+                if (hasB) half_q8_0_cg<CG>(rB + 128 * j, rB + p.K + 8 * j, scl, a, jj, vB + 4 * j, vcol);
+            }
+        } else {
+            // partial sums of my half for both rows; each lane then swaps one
+            // pair per column with its partner (lane ^ 1, the block's other half)
+            int CA[CG], CB[CG], OA[CG], OB[CG];
+            uint32_t dA = 0, dB = 0;
+#pragma unroll
+            for (int c = 0; c < CG; ++c) { CA[c] = 0; CB[c] = 0; OA[c] = 0; OB[c] = 0; }
+            if (go) {
+                if (F == kQ4K) {
+                    half_q4k_cg<CG>(rA + 144 * sb, h, a, S, CA, OA, dA);
+                    if (hasB) half_q4k_cg<CG>(rB + 144 * sb, h, a, S, CB, OB, dB);
+                } else {
+                    half_q6k_cg<CG>(rA + 208 * sb, h, a, S, CA);
+                    dA = *reinterpret_cast<const uint16_t *>(rA + 208 * p.nb + 2 * sb);
+                    if (hasB) {
+                        half_q6k_cg<CG>(rB + 208 * sb, h, a, S, CB);
+                        dB = *reinterpret_cast<const uint16_t *>(rB + 208 * p.nb + 2 * sb);
+                    }
+                }
+            }
+#pragma unroll
+            for (int c = 0; c < CG; ++c) {
+                const int rC = __shfl_xor_sync(0xFFFFFFFFu, h ? CA[c] : CB[c], 1);
+                const int rO = (F == kQ4K) ? __shfl_xor_sync(0xFFFFFFFFu, h ? OA[c] : OB[c], 1) : 0;
+                if (go && (!h || hasB)) {
+                    const int Cs = (h ? CB[c] : CA[c]) + rC, O = (h ? OB[c] : OA[c]) + rO;
+                    const int C = (F == kQ4K) ? (Cs >> 4) : Cs;  // Q4_K: the halves hold 16*C (exact shift)
+                    const uint32_t dd = h ? dB : dA;
+                    float v;
+                    if (F == kQ4K) v = lane_value_fast<1>(C, O, dd & 0xFFFFu, dd >> 16, m0[c], e0[c]);
+                    else v = lane_value_fast<0>(C, 0, dd, 0, m0[c], e0[c]);
+                    (h ? vB : vA)[c * vcol + sb] = v;
+                }
+            }
+        }
+        if (!__syncthreads_and(ok)) return;  // a fill never completed: fault word raised
+        if (tid == 0 && it + p.D < p.n_iter) {
+            fence_proxy_async_smem();
+            fill(it + p.D);
+        }
+        // ---- fold: one thread per (row, column) line, blocks in order
+        if (++hpos == p.H || it == p.n_iter - 1) {
+            const int nline = hpos * p.nt * 2 * ncp;
+            for (int f = tid; f < nline; f += blockDim.x) {
+                const int c = f % ncp;
+                const int64_t l = (int64_t)(it + 1 - hpos) * per_it + f / ncp;  // row of the CTA's range
+                if (c < p.ncols && l < count) {
+                    const float *vt = val + (int64_t)f * p.vstride;
+                    float acc = 0.0f;
+                    for (int b = 0; b < p.nb; ++b) acc = fadd_ftz(acc, vt[b]);
+                    if (acc != acc) acc = __uint_as_float(kEngineNaN);
+                    p.out[(int64_t)c * p.rows + row0 + l] = acc;
+                }
+            }
+            hpos = 0;
+            if (it != p.n_iter - 1) __syncthreads();  // before the history is overwritten
+        }
+    }
+}
+
+// The shape of one launch over `ncols` columns; false when it does not fit.
+template <int F, int CG>
+bool gemv3_shape(int64_t rows, int64_t K, int ncols, Gemv3K &k, int &grid, int &threads, int &smem) {
+    constexpr int kThreads = gemv3_threads<CG>();
+    const int ts = (int)(K / 128);
+    const int ncg = (ncols + CG - 1) / CG, ncp = ncg * CG;
+    const int tpt = ncg * ts;
+    if (tpt > kThreads) return false;
+    k.rows = rows;
+    k.K = (int)K;
+    k.rec = (int)record_bytes(F, K);
+    k.ts = ts;
+    k.ncg = ncg;
+    k.ncols = ncols;
+    k.nb = (int)(K / fmt_block(F));
+    k.vstride = (k.nb & 1) ? k.nb : k.nb + 1;  // odd: the fold's lines fall in distinct banks
+    grid = (int)std::max<int64_t>(1, std::min<int64_t>(num_sms(), rows));
+    const int64_t rpc = (rows + grid - 1) / grid;  // most rows any CTA owns
+    const int budget = 225 * 1024;
+    k.nt = (int)std::min<int64_t>(kThreads / tpt, std::max<int64_t>(1, (rpc + 1) / 2));
+    // room for two ring slots and one history step
+    while (k.nt > 1 && gemv3_smem(k.K, ncols, k.rec, k.nt, ncp, 2, 1, k.vstride).total > budget) --k.nt;
+    if (gemv3_smem(k.K, ncols, k.rec, k.nt, ncp, 1, 1, k.vstride).total > budget) return false;
+    k.n_iter = (int)((rpc + 2LL * k.nt - 1) / (2LL * k.nt));
+    k.base = rows / grid;
+    k.rem = rows % grid;
+    threads = (k.nt * tpt + 31) / 32 * 32;
+    k.H = std::max(1, std::min({k.n_iter, 8, threads / (k.nt * 2 * ncp)}));  // about one fold line a thread
+    const int hist = gemv3_smem(k.K, ncols, k.rec, k.nt, ncp, 0, k.H, k.vstride).total;
+    k.D = std::max(1, std::min({k.n_iter, 4, (budget - hist) / (2 * k.nt * k.rec)}));
+    while (gemv3_smem(k.K, ncols, k.rec, k.nt, ncp, k.D, k.H, k.vstride).total > budget && k.H > 1) --k.H;
+    smem = gemv3_smem(k.K, ncols, k.rec, k.nt, ncp, k.D, k.H, k.vstride).total;
+    return smem <= 227 * 1024;
+}
+
+// The product for 2..16 columns: as many columns a launch as one CTA holds,
+// launches in column order.  QB_E_ARG (nothing launched) when the kernel does
+// not apply to the shape.
+template <int F, int CG>
+int launch_gemv3_cg(const GemvArgs &a, cudaStream_t stream) {
+    constexpr int blk = fmt_block(F);
+    const int ts = (int)(a.K / 128);
+    const int per = (gemv3_threads<CG>() / ts) / CG * CG;  // columns one launch holds
+    if (per < 1) return QB_E_ARG;
+    int *fault = fault_word();
+    if (!fault) return QB_E_CUDA;
+    for (int c0 = 0; c0 < a.ncols; c0 += per) {  // every launch's shape fits before the first is issued
+        Gemv3K k;
+        int grid, threads, smem;
+        if (!gemv3_shape<F, CG>(a.rows, a.K, std::min(per, a.ncols - c0), k, grid, threads, smem)) return QB_E_ARG;
+    }
+    static bool attr_set = false;
+    if (!attr_set) {
+        if (cudaFuncSetAttribute(gemv3_kernel<F, CG>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) !=
+            cudaSuccess)
+            return QB_E_CUDA;
+        attr_set = true;
+    }
+    for (int c0 = 0; c0 < a.ncols; c0 += per) {
+        Gemv3K k;
+        int grid, threads, smem;
+        gemv3_shape<F, CG>(a.rows, a.K, std::min(per, a.ncols - c0), k, grid, threads, smem);
+        k.W = static_cast<const uint8_t *>(a.W);
+        k.codes = a.codes + (int64_t)c0 * a.K;
+        k.scales = a.scales + (int64_t)c0 * (a.K / blk);
+        k.sums16 = a.sums16 ? a.sums16 + (int64_t)c0 * (a.K / 16) : nullptr;
+        k.out = a.out + (int64_t)c0 * a.rows;
+        k.fault = fault;
+        const int rc = launch_pdl(gemv3_kernel<F, CG>, dim3(grid), dim3(threads), (size_t)smem, stream, k);
+        if (rc) return rc;
+    }
+    return QB_OK;
+}
+
+template <int F>
+int launch_gemv3(const GemvArgs &a, cudaStream_t stream) {
+    if (a.ncols < 2 || a.ncols > 16 || a.mode != 0 || a.K % 256 != 0 || a.rows < 1) return QB_E_ARG;
+    // two-column groups at 512 threads measure faster than four-column groups
+    // at 256 (more warps to hide the integer pipeline's latency) at 2..16 columns
+    return launch_gemv3_cg<F, 2>(a, stream);
+}
+
+}  // namespace qb

@@ -1,0 +1,11 @@
+// qb_skinny_q8_0.cu -- the 2..16-column streaming kernel for one weight format
+// (a translation unit of its own so the formats compile in parallel).
+#include "qb_gemv.cuh"
+#include "qb_gemv3.cuh"
+
+namespace qb {
+template <>
+int launch_skinny<kQ8_0>(const GemvArgs &a, cudaStream_t stream) {
+    return launch_gemv3<kQ8_0>(a, stream);
+}
+}  // namespace qb

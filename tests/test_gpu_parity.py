@@ -184,6 +184,27 @@ def test_long_rows_and_chunked_activation(fmt):
     assert np.array_equal(bits(got), bits(want))
 
 
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("ncols", [2, 6, 16])
+@pytest.mark.parametrize("rows,K", [(152 * 9 + 77, 1024), (700, 8192), (300, 12288)])
+def test_skinny_launch_shapes(fmt, ncols, rows, K):
+    """2..16 columns through the multi-column streaming kernel: several ring
+    iterations per CTA with a ragged last one, four- and two-column groups,
+    and (K = 8192, 12288 at 16 columns) several launches over column chunks.
+    Non-finite and unreadable cases ride along in one column and one row."""
+    lg, W, x = make_case(fmt, rows, K, ncols, seed=rows + K + 17 * ncols + fmt, outliers=0.001)
+    blk = synth.BLOCK[fmt]
+    lg["d"][rows // 2, 1] = 0x7C00                           # one unreadable block scale
+    W = synth.pack(fmt, lg)
+    x[ncols - 1, 2 * blk + 5] = np.inf                       # last column: a block with no scale
+    codes, m, e, s16, packed = oracle_act(x, blk)
+    want = oracle.gemv(fmt, W, rows, K, codes, m, e)
+    got = gpu_rows(fmt, W, rows, K, gpu_quantize(x, blk), ncols)
+    assert np.array_equal(bits(got), bits(want))
+    assert np.all(bits(got[ncols - 1]) == 0x7FC00000)
+    assert np.all(bits(got[:, rows // 2]) == 0x7FC00000)
+
+
 # ---------------------------------------------------------------- full-size workloads
 
 def test_q8_0_512x1024_full():
