@@ -40,35 +40,51 @@ __device__ __forceinline__ void wide_scale_bits(uint32_t amax, int &m, int &e) {
     e = ee;
 }
 
-// rne_div for 8 elements under m*2^e.  |x| = mant * 2^(E8x-150), so
-// x/s = mant / (m * 2^k) with k = e - (E8x-150) >= 9 for every |x| <= amax
-// (|x/s| <= 127 forces it), hence hi = mant >> k < 2^15.  floor(hi / m) is
-// (hi * ceil(2^24/m)) >> 24: the product overestimates hi/m by less than
-// hi/2^24 < 2^-9 < 1/m, so the floor is exact for m < 512.  The remainder
-// R = (hi - q*m)*2^k + lo against half the divisor decides the rounding,
-// ties to even.  A denormal, NaN or (m = 0) element gets code 0.
+// rne_div of one element, exactly, on the integer fields: |x| = mant *
+// 2^(E8x-150), so x/s = mant / (m * 2^k) with k = e - (E8x-150).  Every
+// |x| <= amax has k >= 9 (|x/s| <= 127 forces it); k >= 18 puts |x/s| below
+// 1/2, code 0.  Otherwise hi = mant >> k < 2^15, and floor(hi / m) is
+// (hi * ceil(2^24/m)) >> 24 (the product overestimates hi/m by less than
+// hi/2^24 < 2^-9 < 1/m, so the floor is exact for m < 512; the product fits
+// 32 bits).  With rem = hi - q*m and lo = mant mod 2^k, the remainder is
+// R = rem*2^k + lo, and 2R - m*2^k = (2*rem - m)*2^k + 2*lo decides the
+// rounding, ties to even.  A denormal, NaN or (m = 0) element gets code 0.
+__device__ __forceinline__ int rne_div1_exact(uint32_t xbits, int m, int e) {
+    const uint32_t a = xbits & 0x7FFFFFFFu;
+    const int k = e - ((int)(a >> 23) - 150);
+    const bool valid = (m != 0) & (a >= 0x00800000u) & (a < 0x7F800000u) & (k <= 17);
+    const int kc = valid ? k : 9;
+    const uint32_t mu = valid ? (uint32_t)m : 128u;
+    const uint32_t magic = ((1u << 24) + mu - 1u) / mu;
+    const uint32_t mant = (a & 0x7FFFFFu) | 0x800000u;
+    const uint32_t hi = mant >> kc, lo = mant & ((1u << kc) - 1u), half = 1u << (kc - 1);
+    const uint32_t qq = (hi * magic) >> 24;
+    const int t2 = 2 * (int)(hi - qq * mu) - (int)mu;  // in [-m, m-2]
+    const uint32_t thr = t2 == 0 ? 0u : half;           // t2 = 0: up iff lo > 0; t2 = -1: iff lo > half
+    const bool up = (t2 >= 1) | ((t2 >= -1) & ((lo > thr) | ((lo == thr) & (qq & 1u))));
+    const int c = valid ? (int)qq + (up ? 1 : 0) : 0;
+    return (xbits & 0x80000000u) ? -c : c;
+}
+
+// rne_div for 8 elements under m*2^e.  Fast path in f32: x' = x * 2^-e is
+// exact (an exponent-field subtraction; x' < 2^-126 means |x/s| < 1/2, code
+// 0), and qf = RN(x' * RN(1/m)) is within |x/s| * 2^-23 (1 + 2^-23) < 2^-16
+// of x/s (|x/s| <= 127).  So unless qf lies within 2^-16 of a half-integer,
+// x/s lies on the same side of every half-integer as qf and its nearest
+// integer is rint(qf).  The few elements in that band (exact ties among
+// them) take the exact integer routine above.
 __device__ __forceinline__ void rne_div8(const uint32_t (&xb)[8], int m, int e, int (&q)[8]) {
-    const uint32_t magic = m ? (((1u << 24) + (uint32_t)m - 1u) / (uint32_t)m) : 0u;
+    const float inv_m = __frcp_rn((float)(m ? m : 1));
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const uint32_t a = xb[i] & 0x7FFFFFFFu;
-        int c = 0;
-        if (m != 0 && a >= 0x00800000u && a < 0x7F800000u) {
-            const uint32_t mant = (a & 0x7FFFFFu) | 0x800000u;
-            const int k = e - ((int)(a >> 23) - 150);
-            if (k < 32) {
-                const uint32_t hi = mant >> k, lo = mant & ((1u << k) - 1u), half = 1u << (k - 1);
-                const uint32_t qq = (uint32_t)(((unsigned long long)hi * magic) >> 24);
-                const int t2 = 2 * (int)(hi - qq * (uint32_t)m) - m;  // 2R - m*2^k = t2*2^k + 2*lo
-                bool up;
-                if (t2 >= 1) up = true;
-                else if (t2 <= -2) up = false;
-                else if (t2 == -1) up = lo > half || (lo == half && (qq & 1u));
-                else up = lo > 0 || (qq & 1u);
-                c = (int)qq + (up ? 1 : 0);
-            }
-            if (xb[i] & 0x80000000u) c = -c;
-        }
+        const int Ep = (int)(a >> 23) - e;  // exponent field of x * 2^-e
+        const bool valid = (m != 0) & (a >= 0x00800000u) & (a < 0x7F800000u) & (Ep >= 1);
+        const float xs = __uint_as_float((xb[i] & 0x807FFFFFu) | ((uint32_t)(valid ? Ep : 1) << 23));
+        const float qf = __fmul_rn(xs, inv_m);
+        const float r = rintf(qf);
+        int c = valid ? (int)r : 0;
+        if (valid && fabsf(__fsub_rn(qf, r)) >= 0.5f - 0x1p-16f) c = rne_div1_exact(xb[i], m, e);
         q[i] = c;
     }
 }
