@@ -78,12 +78,14 @@ __host__ __device__ inline Gemv2Smem gemv2_smem(int K, int rec, int nt, int D, i
 // the exponent field, which is exact while the result stays a normal f32;
 // any other case (zero, a subnormal or infinite result) goes to the exact
 // integer routine round_to_f32.
+static __device__ __noinline__ float round_to_f32_cold(long long n, int E) { return round_to_f32(n, E); }
+
 __device__ __forceinline__ float round_fast(long long n, int E) {
     const float f = __ll2float_rn(n);
     const uint32_t b = __float_as_uint(f);
     const int ex = (int)((b >> 23) & 0xFFu) + E;
     if (n != 0 && ex >= 1 && ex <= 254) return __uint_as_float(b + ((uint32_t)E << 23));
-    return round_to_f32(n, E);
+    return round_to_f32_cold(n, E);  // out of line: rare
 }
 
 template <int KIND>

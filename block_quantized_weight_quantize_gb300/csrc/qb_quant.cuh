@@ -4,26 +4,16 @@
 // The decode engine's quantize_blocks under ActScaling::PerBlock (numerics
 // page): per block, absmax (a denormal read as zero, NaN passed over),
 // wide_scale (the least m*2^e, m in 128..255, with 127*m*2^e >= amax) and
-// rne_div (the nearest integer of x/(m*2^e), ties to even, exactly), all on
-// the integer fields of the f32 values.  A thread holds 8 consecutive
-// elements; a block of B elements spans B/8 consecutive lanes of a warp.
+// rne_div (the nearest integer of x/(m*2^e), ties to even, exactly).  The
+// scale comes from the integer fields of amax; the division takes an f32
+// path whose result is certain away from half-integers and an exact integer
+// routine otherwise.  A thread holds 8 consecutive elements; a block of B
+// elements spans B/8 consecutive lanes of a warp.
 #pragma once
 
 #include "qb_common.cuh"
 
 namespace qb {
-
-// |x| bits for absmax: a denormal reads as 0, NaN is passed over, +inf kept.
-__device__ __forceinline__ uint32_t absmax_bits8(const uint32_t (&xb)[8]) {
-    uint32_t amax = 0;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        uint32_t a = xb[i] & 0x7FFFFFFFu;
-        if (a < 0x00800000u || a > 0x7F800000u) a = 0;
-        amax = a > amax ? a : amax;
-    }
-    return amax;
-}
 
 // wide_scale of amax = M * 2^(E8-150) (M the 24-bit significand): at
 // e = E8-141 the least 8-bit significand is ceil(M / (127*2^9)), which lies in
@@ -49,7 +39,9 @@ __device__ __forceinline__ void wide_scale_bits(uint32_t amax, int &m, int &e) {
 // 32 bits).  With rem = hi - q*m and lo = mant mod 2^k, the remainder is
 // R = rem*2^k + lo, and 2R - m*2^k = (2*rem - m)*2^k + 2*lo decides the
 // rounding, ties to even.  A denormal, NaN or (m = 0) element gets code 0.
-__device__ __forceinline__ int rne_div1_exact(uint32_t xbits, int m, int e) {
+// Out of line: only the rare elements the fast path below cannot decide
+// come here, and keeping it out of the hot code keeps that code short.
+static __device__ __noinline__ int rne_div1_exact(uint32_t xbits, int m, int e) {
     const uint32_t a = xbits & 0x7FFFFFFFu;
     const int k = e - ((int)(a >> 23) - 150);
     const bool valid = (m != 0) & (a >= 0x00800000u) & (a < 0x7F800000u) & (k <= 17);
@@ -66,36 +58,31 @@ __device__ __forceinline__ int rne_div1_exact(uint32_t xbits, int m, int e) {
     return (xbits & 0x80000000u) ? -c : c;
 }
 
-// rne_div for 8 elements under m*2^e.  Fast path in f32: x' = x * 2^-e is
-// exact (an exponent-field subtraction; x' < 2^-126 means |x/s| < 1/2, code
-// 0), and qf = RN(x' * RN(1/m)) is within |x/s| * 2^-23 (1 + 2^-23) < 2^-16
-// of x/s (|x/s| <= 127).  So unless qf lies within 2^-16 of a half-integer,
-// x/s lies on the same side of every half-integer as qf and its nearest
-// integer is rint(qf).  The few elements in that band (exact ties among
-// them) take the exact integer routine above.
-__device__ __forceinline__ void rne_div8(const uint32_t (&xb)[8], int m, int e, int (&q)[8]) {
-    const float inv_m = __frcp_rn((float)(m ? m : 1));
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const uint32_t a = xb[i] & 0x7FFFFFFFu;
-        const int Ep = (int)(a >> 23) - e;  // exponent field of x * 2^-e
-        const bool valid = (m != 0) & (a >= 0x00800000u) & (a < 0x7F800000u) & (Ep >= 1);
-        const float xs = __uint_as_float((xb[i] & 0x807FFFFFu) | ((uint32_t)(valid ? Ep : 1) << 23));
-        const float qf = __fmul_rn(xs, inv_m);
-        const float r = rintf(qf);
-        int c = valid ? (int)r : 0;
-        if (valid && fabsf(__fsub_rn(qf, r)) >= 0.5f - 0x1p-16f) c = rne_div1_exact(xb[i], m, e);
-        q[i] = c;
-    }
-}
-
 // Quantize the 8 elements xb of a block spanning L lanes: returns the codes
 // packed in two words, the sum of the 16-element unit this lane pair forms,
 // and the block's scale packed as m | e << 16 (identical on the L lanes).
 // Every lane of the warp must call it (shuffles).
+//
+// absmax: max of |x| with denormal inputs flushed to zero (abs.ftz), NaN
+// passed over (max returns the other operand), +inf kept.
+// rne_div fast path in f32: c = RN(1/m) * 2^-e is exact (an exponent-field
+// subtraction; a normal number for e in [-134, 118]), and qf = RN(x * c) with
+// denormal inputs and results flushed (both mean |x/s| < 1/2, code 0) is
+// RN(x' * RN(1/m)) for x' = x * 2^-e, within |x/s| * 2^-23 (1 + 2^-23) <
+// 2^-16 of x/s (|x/s| <= 127).  So unless qf lies within 2^-16 of a
+// half-integer, x/s lies on the same side of every half-integer as qf and its
+// nearest integer is rint(qf).  Elements in that band (exact ties among
+// them), and blocks with e outside the range, take the exact routine.
 template <int L>
 __device__ __forceinline__ void quantize8(const uint32_t (&xb)[8], uint2 &codes, int &unit_sum, uint32_t &scale) {
-    uint32_t amax = absmax_bits8(xb);
+    float am = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        float ax;
+        asm("abs.ftz.f32 %0, %1;" : "=f"(ax) : "f"(__uint_as_float(xb[i])));
+        am = fmaxf(am, ax);
+    }
+    uint32_t amax = __float_as_uint(am);
 #pragma unroll
     for (int o = L / 2; o > 0; o >>= 1) {
         const uint32_t u = __shfl_xor_sync(0xFFFFFFFFu, amax, o);
@@ -104,15 +91,25 @@ __device__ __forceinline__ void quantize8(const uint32_t (&xb)[8], uint2 &codes,
     int m, e;
     wide_scale_bits(amax, m, e);
     int q[8];
-    rne_div8(xb, m, e, q);
-    int s = 0;
+    if ((m != 0) & (e >= -134) & (e <= 118)) {
+        const float inv_m = __frcp_rn((float)m);
+        const float c = __uint_as_float(__float_as_uint(inv_m) - ((uint32_t)e << 23));
 #pragma unroll
-    for (int i = 0; i < 8; ++i) s += q[i];
+        for (int i = 0; i < 8; ++i) {
+            float qf;
+            asm("mul.rn.ftz.f32 %0, %1, %2;" : "=f"(qf) : "f"(__uint_as_float(xb[i])), "f"(c));
+            int v = __float2int_rn(qf);  // NaN: 0
+            if (fabsf(qf - rintf(qf)) >= 0.5f - 0x1p-16f) v = rne_div1_exact(xb[i], m, e);
+            q[i] = v;
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) q[i] = rne_div1_exact(xb[i], m, e);
+    }
+    codes.x = __byte_perm(__byte_perm(q[0], q[1], 0x0040), __byte_perm(q[2], q[3], 0x0040), 0x5410);
+    codes.y = __byte_perm(__byte_perm(q[4], q[5], 0x0040), __byte_perm(q[6], q[7], 0x0040), 0x5410);
+    const int s = dp4a_ss(codes.y, 0x01010101u, dp4a_ss(codes.x, 0x01010101u, 0));
     unit_sum = s + __shfl_xor_sync(0xFFFFFFFFu, s, 1);
-    codes.x = (uint32_t)(q[0] & 0xFF) | ((uint32_t)(q[1] & 0xFF) << 8) | ((uint32_t)(q[2] & 0xFF) << 16) |
-              ((uint32_t)(q[3] & 0xFF) << 24);
-    codes.y = (uint32_t)(q[4] & 0xFF) | ((uint32_t)(q[5] & 0xFF) << 8) | ((uint32_t)(q[6] & 0xFF) << 16) |
-              ((uint32_t)(q[7] & 0xFF) << 24);
     scale = (uint32_t)(m & 0xFF) | ((uint32_t)(uint16_t)(int16_t)e << 16);
 }
 
