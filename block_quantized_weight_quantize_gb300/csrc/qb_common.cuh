@@ -104,6 +104,24 @@ __device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
     return d;
 }
 
+// a: two signed 16-bit halves, b: four unsigned bytes; lo: a.h0*b.b0 + a.h1*b.b1
+// + c, hi: a.h0*b.b2 + a.h1*b.b3 + c
+__device__ __forceinline__ int dp2a_lo_su(uint32_t a, uint32_t b, int c) {
+    int d;
+    asm("dp2a.lo.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+__device__ __forceinline__ int dp2a_hi_su(uint32_t a, uint32_t b, int c) {
+    int d;
+    asm("dp2a.hi.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+// Four 6-bit fields f[i] = (v >> 6i) & 63 spread to the four bytes of a word.
+__device__ __forceinline__ uint32_t spread6(uint32_t v) {
+    return (v & 0x3Fu) | ((v << 2) & 0x3F00u) | ((v << 4) & 0x3F0000u) | ((v << 6) & 0x3F000000u);
+}
+
 __device__ __forceinline__ float fadd_ftz(float a, float b) {
     float d;
     asm("add.rn.ftz.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));

@@ -46,6 +46,7 @@ struct Gemv2K {
     int nb;        // weight blocks per row
     int vstride;   // floats per row line of block values (an odd number of 16-B units)
     int n_iter;    // iterations (two rows per team each)
+    int wfold;     // one iteration and whole teams per warp: each warp folds its own rows
     int64_t base;  // rows per CTA, and how many CTAs own one more
     int64_t rem;
     const int8_t *codes;
@@ -113,16 +114,20 @@ __device__ __forceinline__ float lane_value_fast(int C, int O, uint32_t s1, uint
 // a[k] holds activation 16-B unit 8j+k of the thread's half-slice j (elements
 // 128j + 16k .. +15).
 
-// Q4_K-like half block h of the block at blk: sub-blocks 4h..4h+3.
+// Q4_K-like half block h of the block at blk: sub-blocks 4h..4h+3.  C is
+// returned as 16*C: per sub-block 16*(sum lo*a) + (sum 16*hi*a) in one
+// multiply-add (|16*C| <= 16 * 63 * 15 * 127 * 256 < 2^31 over a whole
+// block).  O = sum mn_s * S_s by two dp2a over the packed 16-bit sub-block
+// sums S01, S23 and the four mn fields spread to bytes.
 __device__ __forceinline__ void half_q4k(const uint8_t *blk, int h, const uint4 (&a)[8], uint32_t S01, uint32_t S23,
-                                         int &C, int &O, uint32_t &dd) {
+                                         int &C16, int &O, uint32_t &dd) {
     const uint4 meta = *reinterpret_cast<const uint4 *>(blk);
     dd = meta.x;
     const unsigned long long sc48 = (unsigned long long)meta.y | ((unsigned long long)(meta.z & 0xFFFFu) << 32);
     const unsigned long long mn48 = (unsigned long long)(meta.z >> 16) | ((unsigned long long)meta.w << 16);
     const uint32_t scm = (uint32_t)(sc48 >> (24 * h)), mnm = (uint32_t)(mn48 >> (24 * h));  // my four fields
     const uint8_t *qs = blk + 16 + 64 * h;
-    int c = 0, o = 0;
+    int c = 0;
 #pragma unroll
     for (int s = 0; s < 4; ++s) {
         const uint4 w = *reinterpret_cast<const uint4 *>(qs + 16 * s);
@@ -134,12 +139,11 @@ __device__ __forceinline__ void half_q4k(const uint8_t *blk, int h, const uint4 
         ph = dp4a_us(w.y & 0xF0F0F0F0u, a[2 * s + 1].y, ph);
         ph = dp4a_us(w.z & 0xF0F0F0F0u, a[2 * s + 1].z, ph);
         ph = dp4a_us(w.w & 0xF0F0F0F0u, a[2 * s + 1].w, ph);
-        c += (int)((scm >> (6 * s)) & 63u) * (pl + (ph >> 4));
-        const uint32_t Sw = (s < 2) ? S01 : S23;
-        o += (int)((mnm >> (6 * s)) & 63u) * (int)(int16_t)((Sw >> (16 * (s & 1))) & 0xFFFFu);
+        c += (int)((scm >> (6 * s)) & 63u) * (16 * pl + ph);
     }
-    C = c;
-    O = o;
+    const uint32_t mnb = spread6(mnm);
+    C16 = c;
+    O = dp2a_hi_su(S23, mnb, dp2a_lo_su(S01, mnb, 0));
 }
 
 // Q6_K-like half block h: 32-element chunks 4h..4h+3 (units 8h..8h+7).
@@ -423,12 +427,35 @@ __global__ void __launch_bounds__(512, FUSED ? 1 : 2) gemv2_kernel(const Gemv2K 
             const int rO = (F == kQ4K) ? __shfl_xor_sync(0xFFFFFFFFu, h ? OA : OB, 1) : 0;
             if (go && (!h || hasB)) {
                 float v;
-                const int C = (h ? CB : CA) + rC, O = (h ? OB : OA) + rO;
+                const int Cs = (h ? CB : CA) + rC, O = (h ? OB : OA) + rO;
+                const int C = (F == kQ4K) ? (Cs >> 4) : Cs;  // Q4_K: the halves hold 16*C (exact shift)
                 const uint32_t dd = h ? dB : dA;
                 if (F == kQ4K) v = lane_value_fast<1>(C, O, dd & 0xFFFFu, dd >> 16, m0, e0);
                 else v = lane_value_fast<0>(C, 0, dd, 0, m0, e0);
                 (h ? vB : vA)[sb] = v;
             }
+        }
+        if (p.wfold) {
+            // a single iteration: each warp folds its own teams' rows (lane r
+            // folds line r of the warp) as soon as its lanes have written
+            // them -- no CTA-wide barrier
+            if (!__all_sync(0xFFFFFFFFu, ok)) return;  // a fill never completed: fault word raised
+            __syncwarp();
+            const int lane = tid & 31, line = 2 * (tid >> 5) * (32 / p.ts) + lane;
+            if (lane < 2 * (32 / p.ts) && line < 2 * p.nt && line < count) {
+                const float4 *v4 = reinterpret_cast<const float4 *>(val + line * p.vstride);
+                float acc = 0.0f;
+                const int n4 = p.nb >> 2;
+                for (int q = 0; q < n4; ++q) {
+                    const float4 x = v4[q];
+                    acc = fadd_ftz(fadd_ftz(fadd_ftz(fadd_ftz(acc, x.x), x.y), x.z), x.w);
+                }
+                const float *vt = val + line * p.vstride;
+                for (int b = 4 * n4; b < p.nb; ++b) acc = fadd_ftz(acc, vt[b]);
+                if (acc != acc) acc = __uint_as_float(kEngineNaN);
+                p.out[row0 + line] = acc;
+            }
+            continue;
         }
         if (!__syncthreads_and(ok)) return;  // a fill never completed: fault word raised
         if (tid == 0 && it + p.D < p.n_iter) {
@@ -503,6 +530,7 @@ int launch_gemv2(const GemvArgs &a, cudaStream_t stream, const float *x = nullpt
     // group a thread (nt >= 16) is fastest
     if (x) k.nt = std::max(k.nt, std::min(multi ? 4 : 16, max_nt));
     k.n_iter = (int)((rpc + 2LL * k.nt - 1) / (2LL * k.nt));
+    k.wfold = (k.n_iter == 1 && 32 % ts == 0) ? 1 : 0;
     k.base = a.rows / grid;
     k.rem = a.rows % grid;
     const int slot = 2 * k.nt * k.rec;
