@@ -124,6 +124,37 @@ def algorithmic_bytes(fmt, rows, K, ncols):
     return wb, wb + ncols * (K + 4 * (K // blk) + 2 * (K // 16)) + 4 * rows * ncols
 
 
+# The multi-column product is bound by the integer pipeline, not by HBM: its
+# roofline is the dp4a issue rate, 64 lanes a clock per SM (two warp
+# instructions a clock; a throughput probe on this GPU measured 1.885) x 8 ops
+# (4 multiply-adds) x 152 SMs x 2.07 GHz (the maximum SM clock).
+DP4A_PEAK_TOPS = 64 * 8 * 152 * 2.07e9 / 1e12
+
+
+def roofline(fmt, ncols, single, achieved, peak, peak_kind, traffic, roof_bytes, per_launch_s, prod_s, abytes,
+             ops_per_step, roof_launches):
+    name = ("gemv_f16_kernel" if fmt == synth.FMT_F16 else
+            f"gemv2_kernel<{synth.FORMAT_NAMES[fmt]}, single launch> (quantize + product)" if single else
+            f"gemv3_kernel<{synth.FORMAT_NAMES[fmt]}, {ncols} columns>")
+    prod = {"avg_launch_us": round(prod_s * 1e6, 4),
+            "achieved_gbs": round(abytes / prod_s / 1e9, 1),
+            "frac_of_hbm": round(abytes / prod_s / 1e9 / peak, 4),
+            "note": "activation quantized beforehand (q_gemv)"}
+    if fmt != synth.FMT_F16 and ncols > 1:
+        tops = ops_per_step / prod_s / 1e12
+        return {"bound": "alu", "kernel": name, "achieved": round(tops, 2), "peak": round(DP4A_PEAK_TOPS, 1),
+                "peak_kind": "dp4a issue rate from unit counts and the maximum clock (64 lanes/clk/SM x 8 ops x "
+                             "152 SMs x 2.07 GHz)",
+                "unit": "TOPS", "frac": round(tops / DP4A_PEAK_TOPS, 4), "traffic": traffic,
+                "algorithmic_ops_per_launch": ops_per_step, "avg_launch_us": round(prod_s * 1e6, 4),
+                "launches_timed": 3 * roof_launches, "hbm_side": prod}
+    return {"bound": "hbm", "kernel": name, "achieved": round(achieved, 1), "peak": peak,
+            "peak_kind": f"{peak_kind} (HBM copy, burst)", "unit": "GB/s", "frac": round(achieved / peak, 4),
+            "traffic": traffic, "algorithmic_bytes_per_launch": roof_bytes,
+            "avg_launch_us": round(per_launch_s * 1e6, 4), "launches_timed": 3 * roof_launches,
+            "product_kernel_only": prod}
+
+
 # ---------------------------------------------------------------- our arm
 
 def run_ours(args, rank, world):
@@ -242,6 +273,7 @@ def run_ours(args, rank, world):
     roof_bytes = (wbytes + 4 * K * ncols + 4 * rows * ncols) if single else abytes
     peak, peak_kind = measured_peaks()
     achieved = roof_bytes / per_launch_s / 1e9
+    ops_per_step = 2 * rows * K * ncols
     traffic = None
     tp = os.path.join(ROOT, "profiles", "traffic.json")
     if os.path.exists(tp):
@@ -305,29 +337,13 @@ def run_ours(args, rank, world):
             "parallelism": "replicas" if world > 1 else "single GPU",
         },
         "rows_per_s": round(world * rows / step_s, 1),
+        "tops": round(world * ops_per_step / step_s / 1e12, 3),
         "frac_of_8tbs": round(value / 8000.0, 4),
         "frac_of_measured_copy": round(value / peak, 4),
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
-        "roofline": {
-            "bound": "hbm",
-            "kernel": ("gemv_f16_kernel" if fmt == synth.FMT_F16 else
-                       f"gemv2_kernel<{synth.FORMAT_NAMES[fmt]}, single launch> (quantize + product)" if single else
-                       f"gemv_kernel<{synth.FORMAT_NAMES[fmt]}, {ncols} columns>"),
-            "achieved": round(achieved, 1),
-            "peak": peak,
-            "peak_kind": f"{peak_kind} (HBM copy, burst)",
-            "unit": "GB/s",
-            "frac": round(achieved / peak, 4),
-            "traffic": traffic,
-            "algorithmic_bytes_per_launch": roof_bytes,
-            "avg_launch_us": round(per_launch_s * 1e6, 4),
-            "launches_timed": 3 * args.roof_launches,
-            "product_kernel_only": {"avg_launch_us": round(prod_s * 1e6, 4),
-                                    "achieved_gbs": round(abytes / prod_s / 1e9, 1),
-                                    "frac": round(abytes / prod_s / 1e9 / peak, 4),
-                                    "note": "activation quantized beforehand (q_gemv)"},
-        },
+        "roofline": roofline(fmt, ncols, single, achieved, peak, peak_kind, traffic, roof_bytes, per_launch_s,
+                             prod_s, abytes, ops_per_step, args.roof_launches),
         "e2e": {
             "value": round(world * wbytes * n_e2e / e2e_s / 1e9, 2),
             "unit": "GB/s",
