@@ -126,7 +126,7 @@ def algorithmic_bytes(fmt, rows, K, ncols):
 
 # The multi-column product is bound by the integer pipeline, not by HBM: its
 # roofline is the dp4a issue rate, 64 lanes a clock per SM (two warp
-# instructions a clock; a throughput probe on this GPU measured 1.885) x 8 ops
+# instructions a clock; a throughput probe on a GB300 measured 1.885) x 8 ops
 # (4 multiply-adds) x 152 SMs x 2.07 GHz (the maximum SM clock).
 DP4A_PEAK_TOPS = 64 * 8 * 152 * 2.07e9 / 1e12
 

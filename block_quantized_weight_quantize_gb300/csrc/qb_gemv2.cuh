@@ -78,7 +78,9 @@ __host__ __device__ inline Gemv2Smem gemv2_smem(int K, int rec, int nt, int D, i
 // round-to-nearest-even int64 -> f32 conversion, then scaled by 2^E through
 // the exponent field, which is exact while the result stays a normal f32;
 // any other case (zero, a subnormal or infinite result) goes to the exact
-// integer routine round_to_f32.
+// integer routine round_to_f32.  (That conversion issues at 2 a clock per SM
+// on this part, but it overlaps other issue: an equivalent built from 32-bit
+// operations measured slower.)
 static __device__ __noinline__ float round_to_f32_cold(long long n, int E) { return round_to_f32(n, E); }
 
 __device__ __forceinline__ float round_fast(long long n, int E) {

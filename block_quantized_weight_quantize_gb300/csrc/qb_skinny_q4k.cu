@@ -1,11 +1,14 @@
-// qb_skinny_q4k.cu -- the 2..16-column streaming kernel for one weight format
-// (a translation unit of its own so the formats compile in parallel).
+// qb_skinny_q4k.cu -- the 2..16-column kernels for the Q4_K-like format (a
+// translation unit of its own so the formats compile in parallel): the
+// tensor-core kernel from 11 columns, the dp4a streaming kernel otherwise.
 #include "qb_gemv.cuh"
 #include "qb_gemv3.cuh"
+#include "qb_gemv5.cuh"
 
 namespace qb {
 template <>
 int launch_skinny<kQ4K>(const GemvArgs &a, cudaStream_t stream) {
-    return launch_gemv3<kQ4K>(a, stream);
+    const int rc = launch_gemv5<kQ4K>(a, stream);
+    return rc == QB_E_ARG ? launch_gemv3<kQ4K>(a, stream) : rc;
 }
 }  // namespace qb

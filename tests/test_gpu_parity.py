@@ -205,6 +205,31 @@ def test_skinny_launch_shapes(fmt, ncols, rows, K):
     assert np.all(bits(got[:, rows // 2]) == 0x7FC00000)
 
 
+@pytest.mark.parametrize("ncols", [11, 12, 16])
+@pytest.mark.parametrize("rows,K", [(152 * 33 + 5, 4096), (300, 256), (1000, 2304)])
+def test_tensor_path_shapes(ncols, rows, K):
+    """Q4_K-like at 11..16 columns, the tensor-core sub-block path: several
+    row chunks per CTA, one block per row (one busy warp), nine blocks (idle
+    warps); rows whose two scales' exponents differ by 29 (the combine's
+    out-of-line exact path), an unreadable dmin, and a column with an
+    infinite activation."""
+    fmt = synth.FMT_Q4K
+    lg, W, x = make_case(fmt, rows, K, ncols, seed=rows + K + ncols, outliers=0.001)
+    nb = K // 256
+    for r in range(3, rows, max(1, rows // 7)):      # d subnormal, dmin near the top: spread 29
+        lg["d"][r, r % nb] = 0x0001
+        lg["dmin"][r, r % nb] = 0x7BFF
+    lg["dmin"][rows // 2, nb - 1] = 0x7E00               # unreadable
+    W = synth.pack(fmt, lg)
+    x[ncols // 2, 5] = -np.inf                           # that column: a block with no scale
+    codes, m, e, s16, packed = oracle_act(x, 256)
+    want = oracle.gemv(fmt, W, rows, K, codes, m, e)
+    got = gpu_rows(fmt, W, rows, K, gpu_quantize(x, 256), ncols)
+    assert np.array_equal(bits(got), bits(want))
+    assert np.all(bits(got[ncols // 2]) == 0x7FC00000)
+    assert np.all(bits(got[:, rows // 2]) == 0x7FC00000)
+
+
 # ---------------------------------------------------------------- full-size workloads
 
 def test_q8_0_512x1024_full():
