@@ -24,6 +24,7 @@ FORMATS = {"f16": F16, "q8_0": Q8_0, "q4k": Q4K, "q6k": Q6K}
 QB_OK, QB_E_ARG, QB_E_FORMAT, QB_E_BLOCK, QB_E_CUDA, QB_E_UNREADABLE, QB_E_DEVICE = 0, -1, -2, -3, -4, -5, -6
 QB_E_SCRATCH = -7
 STATIC_SCRATCH_BYTES = 1 << 20  # QB_STATIC_SCRATCH_BYTES
+MAX_MATS = 4  # QB_MAX_MATS
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libqgemv.so")
@@ -31,7 +32,7 @@ LIB_PATH = os.path.join(_HERE, "libqgemv.so")
 # every entry point include/qgemv.h declares
 EXPORTS = ("quantize_act", "q_gemv", "quantize_act_f16", "q_gemv_f16", "q_check_weights", "q_weight_bytes",
            "q_block_values", "q_device_status", "q_strerror", "q_matvec", "q_matvec_workspace_bytes",
-           "q_matvec_static")
+           "q_matvec_static", "q_gemv_many", "q_gemv_f16_many", "q_matvec_many")
 
 
 class QbError(RuntimeError):
@@ -71,6 +72,11 @@ def lib() -> ctypes.CDLL:
         L.q_matvec.argtypes = [i32, P, i64, i64, P, i32, P, P, ctypes.c_size_t, P]
         L.q_matvec.restype = i32
         L.q_matvec_static.argtypes, L.q_matvec_static.restype = [i32, P, i64, i64, P, i32, P, P], i32
+        L.q_gemv_many.argtypes = [i32, i32, P, P, i64, ctypes.POINTER(_Act), i32, P, P]
+        L.q_gemv_many.restype = i32
+        L.q_gemv_f16_many.argtypes, L.q_gemv_f16_many.restype = [i32, P, P, i64, P, i32, P, P], i32
+        L.q_matvec_many.argtypes = [i32, i32, P, P, i64, P, i32, P, P, ctypes.c_size_t, P]
+        L.q_matvec_many.restype = i32
         _lib = L
     return _lib
 
@@ -188,7 +194,42 @@ def q_matvec_static(fmt: int, W, rows: int, K: int, x, out, stream=None) -> None
     address; make it before any stream capture."""
     ncols = x.shape[0]
     _check(lib().q_matvec_static(fmt, _ptr(W), rows, K, _ptr(x), ncols, _ptr(out), _stream(stream)),
-           "q_matvec_static")
+           "q_matvec_static", "q_gemv_many", "q_gemv_f16_many", "q_matvec_many")
+
+
+# ------------------------------------------------------------------ several matrices, one activation
+
+def _tables(Ws, rows, outs):
+    n = len(Ws)
+    if not (len(rows) == n == len(outs)):
+        raise ValueError("Ws, rows and outs must have the same length")
+    Wa = (ctypes.c_void_p * n)(*[W.data_ptr() for W in Ws])
+    Ra = (ctypes.c_int64 * n)(*[int(r) for r in rows])
+    Oa = (ctypes.c_void_p * n)(*[o.data_ptr() for o in outs])
+    return n, Wa, Ra, Oa
+
+
+def q_gemv_many(fmt: int, Ws, rows, K: int, act, ncols: int, outs, stream=None) -> None:
+    """q_gemv for several matrices sharing one quantized activation (one launch
+    where the shape allows): outs[i] f32 [ncols, rows[i]]."""
+    n, Wa, Ra, Oa = _tables(Ws, rows, outs)
+    codes, scales, sums16 = act
+    a = _act(BLOCK[fmt], codes, scales, sums16)
+    _check(lib().q_gemv_many(fmt, n, Wa, Ra, K, ctypes.byref(a), ncols, Oa, _stream(stream)), "q_gemv_many")
+
+
+def q_gemv_f16_many(Ws, rows, K: int, x16, ncols: int, outs, stream=None) -> None:
+    n, Wa, Ra, Oa = _tables(Ws, rows, outs)
+    _check(lib().q_gemv_f16_many(n, Wa, Ra, K, _ptr(x16), ncols, Oa, _stream(stream)), "q_gemv_f16_many")
+
+
+def q_matvec_many(fmt: int, Ws, rows, K: int, x, outs, workspace=None, stream=None) -> None:
+    """q_matvec for several matrices sharing the f32 activation x [ncols, K]."""
+    n, Wa, Ra, Oa = _tables(Ws, rows, outs)
+    ncols = x.shape[0]
+    nbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(lib().q_matvec_many(fmt, n, Wa, Ra, K, _ptr(x), ncols, Oa, _ptr(workspace), nbytes, _stream(stream)),
+           "q_matvec_many")
 
 
 def matvec(fmt: int, W, rows: int, K: int, x, out=None, act=None, stream=None):

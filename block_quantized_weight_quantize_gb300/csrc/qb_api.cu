@@ -127,7 +127,7 @@ static int check_gemv_args(qb_fmt fmt, const void *W, int64_t rows, int64_t K, c
 static int gemv_common(qb_fmt fmt, const void *W, int64_t rows, int64_t K, const qb_act *act, int ncols, float *out,
                        int32_t *C, int32_t *O, float *v, int mode, void *stream) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    GemvArgs a;
+    GemvArgs a = {};
     a.W = W;
     a.rows = rows;
     a.K = K;
@@ -282,6 +282,122 @@ int q_matvec(qb_fmt fmt, const void *W, int64_t rows, int64_t K, const float *x,
                           const_cast<int16_t *>(act.sums16), stream);
     if (rc) return rc;
     return q_gemv(fmt, W, rows, K, &act, ncols, out, stream);
+}
+
+// ---------------------------------------------------------------- several matrices, one activation
+
+// The host arrays of a grouped call as a matrix table; QB_E_ARG for a bad
+// count or null arrays.  Per-matrix arguments are checked by the caller.
+static int make_table(int nmat, const void *const *W, const int64_t *rows, float *const *out, MatTable &t) {
+    if (nmat < 1 || nmat > QB_MAX_MATS || !W || !rows || !out) return QB_E_ARG;
+    t = MatTable{};
+    t.n = nmat;
+    t.start[0] = 0;
+    for (int i = 0; i < nmat; ++i) {
+        t.W[i] = static_cast<const uint8_t *>(W[i]);
+        t.out[i] = out[i];
+        t.start[i + 1] = t.start[i] + rows[i];
+    }
+    if (t.start[nmat] > (int64_t(1) << 31)) return QB_E_ARG;
+    return QB_OK;
+}
+
+int q_gemv_many(qb_fmt fmt, int nmat, const void *const *W, const int64_t *rows, int64_t K, const qb_act *act,
+                int ncols, float *const *out, void *stream) {
+    MatTable t;
+    int rc = make_table(nmat, W, rows, out, t);
+    if (rc) return rc;
+    for (int i = 0; i < nmat; ++i)
+        if ((rc = check_gemv_args(fmt, W[i], rows[i], K, act, ncols, out[i])) != QB_OK) return rc;
+    if (t.start[nmat] > 0 && K > 0) {
+        GemvArgs a = {};
+        a.mats = &t;
+        a.K = K;
+        a.codes = act->codes;
+        a.scales = act->scales;
+        a.sums16 = act->sums16;
+        a.ncols = ncols;
+        a.mode = 0;
+        cudaStream_t s = static_cast<cudaStream_t>(stream);
+        const int f = fmt_index(fmt);
+        rc = f == kQ8_0 ? launch_gemv_q8_0(a, s) : f == kQ4K ? launch_gemv_q4k(a, s) : launch_gemv_q6k(a, s);
+        if (rc != QB_E_ARG) return rc;
+    }
+    for (int i = 0; i < nmat; ++i)  // shapes the streaming kernels do not take: one launch per matrix
+        if ((rc = q_gemv(fmt, W[i], rows[i], K, act, ncols, out[i], stream)) != QB_OK) return rc;
+    return QB_OK;
+}
+
+int q_gemv_f16_many(int nmat, const uint16_t *const *W, const int64_t *rows, int64_t K, const uint16_t *x16,
+                    int ncols, float *const *out, void *stream) {
+    MatTable t;
+    int rc = make_table(nmat, reinterpret_cast<const void *const *>(W), rows, out, t);
+    if (rc) return rc;
+    if (!x16 || K < 0 || K % 8 != 0 || ncols < 1 || ncols > 16 || (int64_t)ncols * K * 4 > 227 * 1024) return QB_E_ARG;
+    for (int i = 0; i < nmat; ++i)
+        if (!W[i] || !out[i] || rows[i] < 0 || misaligned(W[i]) || (reinterpret_cast<uintptr_t>(out[i]) & 3u))
+            return QB_E_ARG;
+    if ((reinterpret_cast<uintptr_t>(x16) & 1u)) return QB_E_ARG;
+    if (t.start[nmat] > 0 && K > 0) {
+        rc = launch_gemv_f16_many(t, K, x16, ncols, static_cast<cudaStream_t>(stream));
+        if (rc != QB_E_ARG) return rc;
+    }
+    for (int i = 0; i < nmat; ++i)
+        if ((rc = q_gemv_f16(W[i], rows[i], K, x16, ncols, out[i], stream)) != QB_OK) return rc;
+    return QB_OK;
+}
+
+int q_matvec_many(qb_fmt fmt, int nmat, const void *const *W, const int64_t *rows, int64_t K, const float *x,
+                  int ncols, float *const *out, void *workspace, size_t workspace_bytes, void *stream) {
+    MatTable t;
+    int rc = make_table(nmat, W, rows, out, t);
+    if (rc) return rc;
+    if (!x || misaligned(x)) return QB_E_ARG;
+    const int64_t need = q_matvec_workspace_bytes(fmt, K, ncols);
+    if (need < 0) return (int)need;
+    if (fmt != QB_F16) {
+        const int f = fmt_index(fmt);
+        qb_act probe = {fmt_block(f), reinterpret_cast<const int8_t *>(x), reinterpret_cast<const qb_scale *>(x),
+                        reinterpret_cast<const int16_t *>(x)};
+        for (int i = 0; i < nmat; ++i)
+            if ((rc = check_gemv_args(fmt, W[i], rows[i], K, &probe, ncols, out[i])) != QB_OK) return rc;
+        if (t.start[nmat] == 0) return QB_OK;
+        if (K == 0) {  // rows of no blocks: +0
+            for (int i = 0; i < nmat; ++i)
+                if (rows[i] > 0 && cudaMemsetAsync(out[i], 0, (size_t)ncols * rows[i] * sizeof(float),
+                                                   static_cast<cudaStream_t>(stream)) != cudaSuccess)
+                    return QB_E_CUDA;
+            return QB_OK;
+        }
+        if (ncols == 1) {  // one launch: quantized inside the product kernel
+            GemvArgs a = {};
+            a.mats = &t;
+            a.K = K;
+            a.ncols = 1;
+            a.mode = 0;
+            cudaStream_t s = static_cast<cudaStream_t>(stream);
+            rc = f == kQ8_0 ? launch_matvec_q8_0(a, x, s) : f == kQ4K ? launch_matvec_q4k(a, x, s)
+                                                                      : launch_matvec_q6k(a, x, s);
+            if (rc != QB_E_ARG) return rc;
+        }
+    }
+    if (!workspace || (int64_t)workspace_bytes < need || misaligned(workspace)) return QB_E_ARG;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    if (fmt == QB_F16) {
+        uint16_t *x16 = reinterpret_cast<uint16_t *>(ws);
+        if ((rc = quantize_act_f16(x, K, ncols, x16, stream)) != QB_OK) return rc;
+        return q_gemv_f16_many(nmat, reinterpret_cast<const uint16_t *const *>(W), rows, K, x16, ncols, out, stream);
+    }
+    const int blk = fmt_block(fmt_index(fmt));
+    qb_act act;
+    act.block = blk;
+    act.codes = reinterpret_cast<const int8_t *>(ws);
+    act.scales = reinterpret_cast<const qb_scale *>(ws + align16(K * ncols));
+    act.sums16 = reinterpret_cast<const int16_t *>(ws + align16(K * ncols) + align16(4 * (K / blk) * ncols));
+    rc = quantize_act(blk, x, K, ncols, const_cast<int8_t *>(act.codes), const_cast<qb_scale *>(act.scales),
+                      const_cast<int16_t *>(act.sums16), stream);
+    if (rc) return rc;
+    return q_gemv_many(fmt, nmat, W, rows, K, &act, ncols, out, stream);
 }
 
 const char *q_strerror(int status) {

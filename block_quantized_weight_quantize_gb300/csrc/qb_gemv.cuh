@@ -390,6 +390,7 @@ int launch_gemv_fmt(const GemvArgs &a, cudaStream_t stream) {
         const int rc = launch_skinny<F>(a, stream);
         if (rc != QB_E_ARG) return rc;
     }
+    if (a.mats) return QB_E_ARG;  // a table of matrices: the streaming kernels only (the caller falls back)
     GemvK k;
     k.W = static_cast<const uint8_t *>(a.W);
     k.rows = a.rows;

@@ -27,16 +27,18 @@
 #pragma once
 
 #include <algorithm>
+#include <type_traits>
 
 #include "qb_common.cuh"
 #include "qb_launch.h"
+#include "qb_mats.cuh"
 #include "qb_quant.cuh"
 
 namespace qb {
 
 struct Gemv2K {
-    const uint8_t *W;
-    int64_t rows;
+    const uint8_t *W;  // the matrix (one-matrix launches)
+    int64_t rows;      // rows of the whole range
     int K;
     int rec;       // bytes per row record
     int nt;        // teams per CTA
@@ -53,8 +55,13 @@ struct Gemv2K {
     const qb_scale *scales;
     const int16_t *sums16;
     const float *x;  // single-launch form: the f32 activation, quantized in the kernel
-    float *out;
+    float *out;      // one-matrix launches
     int *fault;
+};
+// A launch over several matrices sharing the activation: the same fields and
+// the matrix table (W and out unused).
+struct Gemv2KM : Gemv2K {
+    MatTable mt;
 };
 
 struct Gemv2Smem {
@@ -233,22 +240,28 @@ __device__ __forceinline__ void cta_rows(const Gemv2K &p, int64_t &row0, int64_t
 
 // Issue the fill of iteration `it` -- its rows are contiguous in memory, so
 // one bulk copy -- into ring slot it % D, completing on that slot's mbarrier.
-__device__ __forceinline__ void issue_fill(const Gemv2K &p, uint8_t *ring, uint64_t *bars, int it, int64_t row0,
+template <bool MULTI, typename P>
+__device__ __forceinline__ void issue_fill(const P &p, uint8_t *ring, uint64_t *bars, int it, int64_t row0,
                                            int64_t count) {
     const int slot = it % p.D;
     const int64_t first = (int64_t)it * 2 * p.nt;
     const int64_t n = (count - first < 2 * p.nt) ? count - first : (int64_t)(2 * p.nt);
     const uint32_t bytes = n > 0 ? (uint32_t)(n * p.rec) : 0u;
     mbar_arrive_expect_tx(bars + slot, bytes);
-    if (bytes) bulk_g2s(ring + (int64_t)slot * 2 * p.nt * p.rec, p.W + (row0 + first) * p.rec, bytes, bars + slot);
+    uint8_t *dst = ring + (int64_t)slot * 2 * p.nt * p.rec;
+    if (!bytes) return;
+    if constexpr (MULTI) fill_rows(p.mt, dst, row0 + first, n, p.rec, bars + slot);
+    else bulk_g2s(dst, p.W + (row0 + first) * p.rec, bytes, bars + slot);
 }
 
 // Two CTAs per SM (<= 64 registers) for the product with a staged activation,
 // so a following launch's CTA fits beside this one and streams its weights
 // early; one (more registers, more overlap inside a warp) for the
 // single-launch form, which measures faster that way.
-template <int F, bool FUSED>
-__global__ void __launch_bounds__(512, FUSED ? 1 : 2) gemv2_kernel(const Gemv2K p) {
+// MULTI: several matrices through the table (mats.cuh); otherwise entry 0
+// alone, with plain address arithmetic.
+template <int F, bool FUSED, bool MULTI>
+__global__ void __launch_bounds__(512, FUSED ? 1 : 2) gemv2_kernel(const typename std::conditional<MULTI, Gemv2KM, Gemv2K>::type p) {
     extern __shared__ __align__(128) uint8_t smem[];
     const Gemv2Smem L = gemv2_smem(p.K, p.rec, p.nt, p.D, p.H, p.vstride);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L.bars);
@@ -271,7 +284,7 @@ __global__ void __launch_bounds__(512, FUSED ? 1 : 2) gemv2_kernel(const Gemv2K 
     int64_t row0, count;
     cta_rows(p, row0, count);
     if (tid == 0)
-        for (int it = 0; it < p.D && it < p.n_iter; ++it) issue_fill(p, ring, bars, it, row0, count);  // no dependency
+        for (int it = 0; it < p.D && it < p.n_iter; ++it) issue_fill<MULTI>(p, ring, bars, it, row0, count);  // no dependency
     pdl_wait();
 
     // ---- the activation, in one round trip: every thread first issues its
@@ -455,14 +468,15 @@ __global__ void __launch_bounds__(512, FUSED ? 1 : 2) gemv2_kernel(const Gemv2K 
                 const float *vt = val + line * p.vstride;
                 for (int b = 4 * n4; b < p.nb; ++b) acc = fadd_ftz(acc, vt[b]);
                 if (acc != acc) acc = __uint_as_float(kEngineNaN);
-                p.out[row0 + line] = acc;
+                if constexpr (MULTI) *out_ptr(p.mt, 0, row0 + line) = acc;
+                else p.out[row0 + line] = acc;
             }
             continue;
         }
         if (!__syncthreads_and(ok)) return;  // a fill never completed: fault word raised
         if (tid == 0 && it + p.D < p.n_iter) {
             fence_proxy_async_smem();
-            issue_fill(p, ring, bars, it + p.D, row0, count);
+            issue_fill<MULTI>(p, ring, bars, it + p.D, row0, count);
         }
         // ---- fold H iterations' rows: one thread per row, blocks in order
         if (++hpos == p.H || it == p.n_iter - 1) {
@@ -488,7 +502,8 @@ __global__ void __launch_bounds__(512, FUSED ? 1 : 2) gemv2_kernel(const Gemv2K 
                     const float *vt = val + tid * p.vstride;
                     for (int b = 4 * n4; b < p.nb; ++b) acc = fadd_ftz(acc, vt[b]);
                     if (acc != acc) acc = __uint_as_float(kEngineNaN);
-                    p.out[row0 + l] = acc;
+                    if constexpr (MULTI) *out_ptr(p.mt, 0, row0 + l) = acc;
+                    else p.out[row0 + l] = acc;
                 }
             }
             hpos = 0;
@@ -503,9 +518,11 @@ int launch_gemv2(const GemvArgs &a, cudaStream_t stream, const float *x = nullpt
     const int K = (int)a.K;
     const int ts = K / 128;
     if (ts > 512) return QB_E_ARG;
-    Gemv2K k;
-    k.W = static_cast<const uint8_t *>(a.W);
-    k.rows = a.rows;
+    Gemv2KM k;
+    k.mt = a.mats ? *a.mats : single_table(a.W, a.rows, a.out);
+    k.rows = k.mt.start[k.mt.n];
+    k.W = k.mt.W[0];
+    k.out = k.mt.out[0];
     k.K = K;
     k.rec = (int)record_bytes(F, a.K);
     k.ts = ts;
@@ -517,8 +534,8 @@ int launch_gemv2(const GemvArgs &a, cudaStream_t stream, const float *x = nullpt
     // one CTA per SM (fewer for a short matrix); teams per CTA: enough for all
     // of the CTA's rows in one iteration when that fits, else as many as leave
     // room for two ring slots
-    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(sms, a.rows));
-    const int64_t rpc = (a.rows + grid - 1) / grid;  // most rows any CTA owns
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(sms, k.rows));
+    const int64_t rpc = (k.rows + grid - 1) / grid;  // most rows any CTA owns
     const int64_t need = (rpc + 1) / 2;
     k.nt = (int)std::min<int64_t>(max_nt, std::max<int64_t>(1, need));
     const bool multi = k.nt < need;  // more than one iteration per CTA
@@ -533,8 +550,8 @@ int launch_gemv2(const GemvArgs &a, cudaStream_t stream, const float *x = nullpt
     if (x) k.nt = std::max(k.nt, std::min(multi ? 4 : 16, max_nt));
     k.n_iter = (int)((rpc + 2LL * k.nt - 1) / (2LL * k.nt));
     k.wfold = (k.n_iter == 1 && 32 % ts == 0) ? 1 : 0;
-    k.base = a.rows / grid;
-    k.rem = a.rows % grid;
+    k.base = k.rows / grid;
+    k.rem = k.rows % grid;
     const int slot = 2 * k.nt * k.rec;
     k.H = std::max(1, std::min({k.n_iter, 8, ts / 2}));  // one fold line per thread: H * 2 * nt <= nt * ts
     k.D = std::max(1, std::min({k.n_iter, 4, (budget - fixed) / std::max(1, slot)}));
@@ -543,7 +560,6 @@ int launch_gemv2(const GemvArgs &a, cudaStream_t stream, const float *x = nullpt
     k.scales = a.scales;
     k.sums16 = a.sums16;
     k.x = x;
-    k.out = a.out;
     k.fault = fault_word();
     if (!k.fault) return QB_E_CUDA;
     Gemv2Smem L = gemv2_smem(K, k.rec, k.nt, k.D, k.H, k.vstride);
@@ -553,25 +569,25 @@ int launch_gemv2(const GemvArgs &a, cudaStream_t stream, const float *x = nullpt
     }
     if (L.total > 227 * 1024) return QB_E_ARG;
     const int threads = (k.nt * ts + 31) / 32 * 32;
-    if (x) {
-        if (K / 8 > 4 * threads) return QB_E_ARG;  // the in-kernel quantizer holds at most 4 groups a thread
-        static bool attr_f = false;
-        if (!attr_f) {
-            if (cudaFuncSetAttribute(gemv2_kernel<F, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     227 * 1024) != cudaSuccess)
-                return QB_E_CUDA;
-            attr_f = true;
-        }
-        return launch_pdl(gemv2_kernel<F, true>, dim3(grid), dim3(threads), (size_t)L.total, stream, k);
+    if (x && K / 8 > 4 * threads) return QB_E_ARG;  // the in-kernel quantizer holds at most 4 groups a thread
+    static bool attr_set[4] = {false, false, false, false};
+    const int ai = (x ? 2 : 0) + (k.mt.n > 1 ? 1 : 0);
+    auto set_attr = [&](const void *f) {
+        if (attr_set[ai]) return true;
+        if (cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) != cudaSuccess)
+            return false;
+        attr_set[ai] = true;
+        return true;
+    };
+    const Gemv2K &k1 = k;  // a one-matrix launch takes the plain parameters
+    if (k.mt.n > 1) {
+        auto kern = x ? gemv2_kernel<F, true, true> : gemv2_kernel<F, false, true>;
+        if (!set_attr(reinterpret_cast<const void *>(kern))) return QB_E_CUDA;
+        return launch_pdl(kern, dim3(grid), dim3(threads), (size_t)L.total, stream, k);
     }
-    static bool attr_set = false;
-    if (!attr_set) {
-        if (cudaFuncSetAttribute(gemv2_kernel<F, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) !=
-            cudaSuccess)
-            return QB_E_CUDA;
-        attr_set = true;
-    }
-    return launch_pdl(gemv2_kernel<F, false>, dim3(grid), dim3(threads), (size_t)L.total, stream, k);
+    auto kern = x ? gemv2_kernel<F, true, false> : gemv2_kernel<F, false, false>;
+    if (!set_attr(reinterpret_cast<const void *>(kern))) return QB_E_CUDA;
+    return launch_pdl(kern, dim3(grid), dim3(threads), (size_t)L.total, stream, k1);
 }
 
 }  // namespace qb

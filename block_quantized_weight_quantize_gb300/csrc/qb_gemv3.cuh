@@ -19,16 +19,19 @@
 #pragma once
 
 #include <algorithm>
+#include <type_traits>
 
 #include "qb_common.cuh"
 #include "qb_gemv2.cuh"
 #include "qb_launch.h"
+#include "qb_mats.cuh"
 
 namespace qb {
 
 struct Gemv3K {
-    const uint8_t *W;
-    int64_t rows;
+    const uint8_t *W;  // the matrix (one-matrix launches)
+    float *out;        // its output at this launch's first column (one-matrix launches)
+    int64_t rows;      // rows of the whole range
     int K;
     int rec;
     int nt;     // teams per CTA
@@ -45,8 +48,12 @@ struct Gemv3K {
     const int8_t *codes;  // column 0 of this launch
     const qb_scale *scales;
     const int16_t *sums16;
-    float *out;
     int *fault;
+};
+// A launch over several matrices sharing the activation: the table, outputs
+// at this launch's first column (W and out unused).
+struct Gemv3KM : Gemv3K {
+    MatTable mt;
 };
 
 struct Gemv3Smem {
@@ -180,8 +187,9 @@ __device__ __forceinline__ void half_q8_0_cg(const uint8_t *q, const uint8_t *dp
 template <int CG>
 constexpr int gemv3_threads() { return CG >= 4 ? 256 : 512; }
 
-template <int F, int CG>
-__global__ void __launch_bounds__(gemv3_threads<CG>(), 1) gemv3_kernel(const Gemv3K p) {
+template <int F, int CG, bool MULTI>
+__global__ void __launch_bounds__(gemv3_threads<CG>(), 1)
+    gemv3_kernel(const typename std::conditional<MULTI, Gemv3KM, Gemv3K>::type p) {
     extern __shared__ __align__(128) uint8_t smem[];
     const int ncp = p.ncg * CG;  // padded columns
     const Gemv3Smem L = gemv3_smem(p.K, p.ncols, p.rec, p.nt, ncp, p.D, p.H, p.vstride);
@@ -213,7 +221,10 @@ __global__ void __launch_bounds__(gemv3_threads<CG>(), 1) gemv3_kernel(const Gem
         const int64_t n = (count - first < per_it) ? count - first : per_it;
         const uint32_t bytes = n > 0 ? (uint32_t)(n * p.rec) : 0u;
         mbar_arrive_expect_tx(bars + slot, bytes);
-        if (bytes) bulk_g2s(ring + (int64_t)slot * per_it * p.rec, p.W + (row0 + first) * p.rec, bytes, bars + slot);
+        if (!bytes) return;
+        uint8_t *dst = ring + (int64_t)slot * per_it * p.rec;
+        if constexpr (MULTI) fill_rows(p.mt, dst, row0 + first, n, p.rec, bars + slot);
+        else bulk_g2s(dst, p.W + (row0 + first) * p.rec, bytes, bars + slot);
     };
     if (tid == 0)
         for (int it = 0; it < p.D && it < p.n_iter; ++it) fill(it);  // weights depend on no earlier kernel
@@ -358,7 +369,8 @@ __global__ void __launch_bounds__(gemv3_threads<CG>(), 1) gemv3_kernel(const Gem
                     float acc = 0.0f;
                     for (int b = 0; b < p.nb; ++b) acc = fadd_ftz(acc, vt[b]);
                     if (acc != acc) acc = __uint_as_float(kEngineNaN);
-                    p.out[(int64_t)c * p.rows + row0 + l] = acc;
+                    if constexpr (MULTI) *out_ptr(p.mt, c, row0 + l) = acc;
+                    else p.out[(int64_t)c * p.rows + row0 + l] = acc;
                 }
             }
             hpos = 0;
@@ -413,29 +425,38 @@ int launch_gemv3_cg(const GemvArgs &a, cudaStream_t stream) {
     if (per < 1) return QB_E_ARG;
     int *fault = fault_word();
     if (!fault) return QB_E_CUDA;
+    const MatTable mt = a.mats ? *a.mats : single_table(a.W, a.rows, a.out);
+    const int64_t rows = mt.start[mt.n];
     for (int c0 = 0; c0 < a.ncols; c0 += per) {  // every launch's shape fits before the first is issued
         Gemv3K k;
         int grid, threads, smem;
-        if (!gemv3_shape<F, CG>(a.rows, a.K, std::min(per, a.ncols - c0), k, grid, threads, smem)) return QB_E_ARG;
+        if (!gemv3_shape<F, CG>(rows, a.K, std::min(per, a.ncols - c0), k, grid, threads, smem)) return QB_E_ARG;
     }
-    static bool attr_set = false;
-    if (!attr_set) {
-        if (cudaFuncSetAttribute(gemv3_kernel<F, CG>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) !=
-            cudaSuccess)
+    const bool multi = mt.n > 1;
+    static bool attr_set[2] = {false, false};
+    if (!attr_set[multi]) {
+        const void *f = multi ? reinterpret_cast<const void *>(gemv3_kernel<F, CG, true>)
+                              : reinterpret_cast<const void *>(gemv3_kernel<F, CG, false>);
+        if (cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) != cudaSuccess)
             return QB_E_CUDA;
-        attr_set = true;
+        attr_set[multi] = true;
     }
     for (int c0 = 0; c0 < a.ncols; c0 += per) {
-        Gemv3K k;
+        Gemv3KM k;
         int grid, threads, smem;
-        gemv3_shape<F, CG>(a.rows, a.K, std::min(per, a.ncols - c0), k, grid, threads, smem);
-        k.W = static_cast<const uint8_t *>(a.W);
+        gemv3_shape<F, CG>(rows, a.K, std::min(per, a.ncols - c0), k, grid, threads, smem);
+        k.mt = mt;  // outputs from column c0: each matrix's own column stride is its row count
+        for (int i = 0; i < mt.n; ++i) k.mt.out[i] = mt.out[i] + (int64_t)c0 * (mt.start[i + 1] - mt.start[i]);
+        k.W = k.mt.W[0];
+        k.out = k.mt.out[0];
         k.codes = a.codes + (int64_t)c0 * a.K;
         k.scales = a.scales + (int64_t)c0 * (a.K / blk);
         k.sums16 = a.sums16 ? a.sums16 + (int64_t)c0 * (a.K / 16) : nullptr;
-        k.out = a.out + (int64_t)c0 * a.rows;
         k.fault = fault;
-        const int rc = launch_pdl(gemv3_kernel<F, CG>, dim3(grid), dim3(threads), (size_t)smem, stream, k);
+        const Gemv3K &k1 = k;
+        const int rc = multi ? launch_pdl(gemv3_kernel<F, CG, true>, dim3(grid), dim3(threads), (size_t)smem, stream, k)
+                             : launch_pdl(gemv3_kernel<F, CG, false>, dim3(grid), dim3(threads), (size_t)smem, stream,
+                                          k1);
         if (rc) return rc;
     }
     return QB_OK;
@@ -443,7 +464,7 @@ int launch_gemv3_cg(const GemvArgs &a, cudaStream_t stream) {
 
 template <int F>
 int launch_gemv3(const GemvArgs &a, cudaStream_t stream) {
-    if (a.ncols < 2 || a.ncols > 16 || a.mode != 0 || a.K % 256 != 0 || a.rows < 1) return QB_E_ARG;
+    if (a.ncols < 2 || a.ncols > 16 || a.mode != 0 || a.K % 256 != 0 || (!a.mats && a.rows < 1)) return QB_E_ARG;
     // two-column groups at 512 threads measure faster than four-column groups
     // at 256 (more warps to hide the integer pipeline's latency) at 2..16 columns
     return launch_gemv3_cg<F, 2>(a, stream);

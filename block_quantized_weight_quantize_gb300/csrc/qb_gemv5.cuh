@@ -45,12 +45,13 @@
 #include "qb_common.cuh"
 #include "qb_gemv2.cuh"
 #include "qb_launch.h"
+#include "qb_mats.cuh"
 
 namespace qb {
 
 struct Gemv5K {
-    const uint8_t *W;
-    int64_t rows;
+    MatTable mt;   // the matrix (or matrices sharing the activation)
+    int64_t rows;  // rows of the whole range
     int K;
     int rec;
     int pitch;    // bytes between rows in a ring slot: rec padded to an odd number of 16-B units
@@ -65,7 +66,6 @@ struct Gemv5K {
     const int8_t *codes;
     const qb_scale *scales;
     const int16_t *sums16;
-    float *out;
     int *fault;
 };
 
@@ -191,8 +191,8 @@ __global__ void __launch_bounds__(512, 1) gemv5_kernel(const Gemv5K p) {
         if (lane == 0) mbar_arrive_expect_tx(bars + slot, n > 0 ? (uint32_t)(n * p.rec) : 0u);
         __syncwarp();
         for (int64_t r = lane; r < n; r += 32)
-            bulk_g2s(ring + ((int64_t)slot * p.R + r) * p.pitch, p.W + (row0 + first + r) * p.rec, (uint32_t)p.rec,
-                     bars + slot);
+            bulk_g2s(ring + ((int64_t)slot * p.R + r) * p.pitch, row_ptr(p.mt, row0 + first + r, p.rec),
+                     (uint32_t)p.rec, bars + slot);
     };
     if (w == 0)
         for (int it = 0; it < p.D && it < p.n_iter; ++it) fill(it);  // weights depend on no earlier kernel
@@ -345,7 +345,7 @@ __global__ void __launch_bounds__(512, 1) gemv5_kernel(const Gemv5K p) {
                 float acc = 0.0f;
                 for (int bb = 0; bb < p.nb; ++bb) acc = fadd_ftz(acc, vt[bb]);
                 if (acc != acc) acc = __uint_as_float(kEngineNaN);
-                p.out[(int64_t)c * p.rows + row0 + first + rr] = acc;
+                *out_ptr(p.mt, c, row0 + first + rr) = acc;
             }
         }
         if (it != p.n_iter - 1) __syncthreads();  // the fold has read the values before they are overwritten
@@ -356,19 +356,20 @@ __global__ void __launch_bounds__(512, 1) gemv5_kernel(const Gemv5K p) {
 // columns, K % 256 == 0 and K <= 4096).
 template <int F>
 int launch_gemv5(const GemvArgs &a, cudaStream_t stream) {
-    if (F != kQ4K || a.ncols < 11 || a.ncols > 16 || a.mode != 0 || a.K % 256 != 0 || a.K > 4096 || a.rows < 1)
+    if (F != kQ4K || a.ncols < 11 || a.ncols > 16 || a.mode != 0 || a.K % 256 != 0 || a.K > 4096 ||
+        (!a.mats && a.rows < 1))
         return QB_E_ARG;
     Gemv5K k;
-    k.W = static_cast<const uint8_t *>(a.W);
-    k.rows = a.rows;
+    k.mt = a.mats ? *a.mats : single_table(a.W, a.rows, a.out);
+    k.rows = k.mt.start[k.mt.n];
     k.K = (int)a.K;
     k.rec = (int)record_bytes(F, a.K);
     k.pitch = gemv5_pitch(k.rec);
     k.nb = (int)(a.K / 256);
     k.ncols = a.ncols;
     k.vstride = (k.nb & 1) ? k.nb : k.nb + 1;
-    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(num_sms(), a.rows));
-    const int64_t rpc = (a.rows + grid - 1) / grid;
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(num_sms(), k.rows));
+    const int64_t rpc = (k.rows + grid - 1) / grid;
     const int budget = 225 * 1024;
     // a chunk of R rows: all of a CTA's rows when they fit one slot, else the
     // largest multiple of 8 (<= 32) that leaves room for two slots
@@ -385,12 +386,11 @@ int launch_gemv5(const GemvArgs &a, cudaStream_t stream) {
     k.n_iter = (int)((rpc + k.R - 1) / k.R);
     if (k.n_iter > 1 && k.D < 2) k.D = std::min(k.n_iter, 2);
     if (gemv5_smem(k.K, k.pitch, k.R, k.D, k.vstride).total > budget) return QB_E_ARG;
-    k.base = a.rows / grid;
-    k.rem = a.rows % grid;
+    k.base = k.rows / grid;
+    k.rem = k.rows % grid;
     k.codes = a.codes;
     k.scales = a.scales;
     k.sums16 = a.sums16;
-    k.out = a.out;
     k.fault = fault_word();
     if (!k.fault) return QB_E_CUDA;
     const int smem = gemv5_smem(k.K, k.pitch, k.R, k.D, k.vstride).total;

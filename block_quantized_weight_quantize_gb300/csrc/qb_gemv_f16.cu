@@ -23,12 +23,13 @@
 
 #include "qb_common.cuh"
 #include "qb_launch.h"
+#include "qb_mats.cuh"
 
 namespace qb {
 
 struct F16K {
-    const uint16_t *W;
-    int64_t rows;
+    MatTable mt;   // the matrix (or matrices sharing x16) as one range of rows
+    int64_t rows;  // rows of the whole range
     int K;
     int pitch;     // bytes per row in shared memory (2K padded)
     int R;         // rows per ring slot
@@ -37,7 +38,6 @@ struct F16K {
     int64_t base;  // rows per CTA, and how many CTAs own one more
     int64_t rem;
     const uint16_t *x16;
-    float *out;
     int *fault;
 };
 
@@ -52,8 +52,8 @@ __device__ __forceinline__ void f16_fill(const F16K &p, uint8_t *ring, uint64_t 
     if (lane == 0) mbar_arrive_expect_tx(bars + slot, n > 0 ? (uint32_t)n * (uint32_t)(2 * p.K) : 0u);
     __syncwarp();
     for (int r = lane; r < n; r += 32)
-        bulk_g2s(ring + ((int64_t)slot * p.R + r) * p.pitch, p.W + (row0 + first + r) * p.K, (uint32_t)(2 * p.K),
-                 bars + slot);
+        bulk_g2s(ring + ((int64_t)slot * p.R + r) * p.pitch, row_ptr(p.mt, row0 + first + r, 2 * p.K),
+                 (uint32_t)(2 * p.K), bars + slot);
 }
 
 template <int NC>
@@ -114,7 +114,7 @@ __global__ void __launch_bounds__(256) gemv_f16_kernel(const F16K p) {
             if (have && ok && pp == 0) {
                 float r = all;
                 if (r != r) r = __uint_as_float(kEngineNaN);
-                p.out[(int64_t)q * p.rows + row0 + l] = r;
+                *out_ptr(p.mt, q, row0 + l) = r;
             }
         }
         if (!__syncthreads_and(ok)) return;  // a fill never completed: fault word raised
@@ -223,11 +223,13 @@ static int launch_f16_nc(const F16K &k, int smem, unsigned grid, int threads, cu
     return launch_pdl(gemv_f16_kernel<NC>, dim3(grid), dim3(threads), (size_t)smem, stream, k);
 }
 
-int launch_gemv_f16(const uint16_t *W, int64_t rows, int64_t K, const uint16_t *x16, int ncols, float *out,
-                    cudaStream_t stream) {
+// The streaming kernel over a table of matrices; QB_E_ARG when a slot of 8
+// rows does not fit (then only the row-per-thread kernel takes the shape).
+static int launch_f16_table(const MatTable &t, int64_t K, const uint16_t *x16, int ncols, cudaStream_t stream) {
     F16K k;
-    k.W = W;
-    k.rows = rows;
+    k.mt = t;
+    k.rows = t.start[t.n];
+    const int64_t rows = k.rows;
     k.K = (int)K;
     const int units = (int)(K / 8);  // 16-B units per row
     k.pitch = 16 * (units + ((units & 1) ? 2 : 1));  // odd number of units
@@ -238,23 +240,13 @@ int launch_gemv_f16(const uint16_t *W, int64_t rows, int64_t K, const uint16_t *
     const int64_t rpc = (rows + grid - 1) / grid;
     const int xsb = f16_xs_bytes((int)K, ncols);
     const int budget = 200 * 1024 - 128 - xsb;
-    if (budget < 8 * k.pitch) {  // a slot of 8 rows does not fit: the row-per-thread kernel
-        switch (ncols) {
-#define QB_CASE(N) \
-    case N: return launch_f16_rowthread<N>(W, rows, K, x16, out, stream);
-            QB_CASE(1) QB_CASE(2) QB_CASE(3) QB_CASE(4) QB_CASE(5) QB_CASE(6) QB_CASE(7) QB_CASE(8)
-            QB_CASE(9) QB_CASE(10) QB_CASE(11) QB_CASE(12) QB_CASE(13) QB_CASE(14) QB_CASE(15) QB_CASE(16)
-#undef QB_CASE
-        }
-        return QB_E_ARG;
-    }
+    if (budget < 8 * k.pitch) return QB_E_ARG;
     // rows per slot: a multiple of 8 (whole warps), at most 64, at least two slots
     k.R = (int)std::min<int64_t>(64, std::max<int64_t>(8, (rpc + 7) / 8 * 8));
     while (k.R > 8 && 2 * k.R * k.pitch > budget) k.R -= 8;
     k.n_iter = (int)((rpc + k.R - 1) / k.R);
     k.D = std::max(1, std::min(k.n_iter, std::min(4, budget / (k.R * k.pitch))));
     k.x16 = x16;
-    k.out = out;
     k.fault = fault_word();
     if (!k.fault) return QB_E_CUDA;
     const int smem = 128 + xsb + k.D * k.R * k.pitch;
@@ -267,6 +259,24 @@ int launch_gemv_f16(const uint16_t *W, int64_t rows, int64_t K, const uint16_t *
 #undef QB_CASE
     }
     return QB_E_ARG;
+}
+
+int launch_gemv_f16(const uint16_t *W, int64_t rows, int64_t K, const uint16_t *x16, int ncols, float *out,
+                    cudaStream_t stream) {
+    const int rc = launch_f16_table(single_table(W, rows, out), K, x16, ncols, stream);
+    if (rc != QB_E_ARG) return rc;
+    switch (ncols) {  // a slot of 8 rows does not fit: the row-per-thread kernel
+#define QB_CASE(N) \
+    case N: return launch_f16_rowthread<N>(W, rows, K, x16, out, stream);
+        QB_CASE(1) QB_CASE(2) QB_CASE(3) QB_CASE(4) QB_CASE(5) QB_CASE(6) QB_CASE(7) QB_CASE(8)
+        QB_CASE(9) QB_CASE(10) QB_CASE(11) QB_CASE(12) QB_CASE(13) QB_CASE(14) QB_CASE(15) QB_CASE(16)
+#undef QB_CASE
+    }
+    return QB_E_ARG;
+}
+
+int launch_gemv_f16_many(const MatTable &t, int64_t K, const uint16_t *x16, int ncols, cudaStream_t stream) {
+    return launch_f16_table(t, K, x16, ncols, stream);
 }
 
 }  // namespace qb

@@ -1,6 +1,7 @@
 // qb_launch.h -- host-side launch helper and the internal launcher prototypes.
 #pragma once
 
+#include <cstdint>
 #include <cuda_runtime.h>
 
 #include "qgemv.h"
@@ -32,8 +33,30 @@ int launch_quantize_act(int block, const float *x, int64_t K, int ncols, int8_t 
                         int16_t *sums16, cudaStream_t stream);
 int launch_quantize_f16(const float *x, int64_t n, uint16_t *x16, cudaStream_t stream);
 
+// Matrices that share one activation (the same K and format), seen by a
+// kernel as one range of rows: matrix i holds rows [start[i], start[i+1]) of
+// the range, reads its records from W[i] and writes its own output out[i]
+// (out[i][c*rows_i + r]).  A single matrix is the table of one.
+constexpr int kMaxMats = QB_MAX_MATS;
+struct MatTable {
+    int n;
+    const uint8_t *W[kMaxMats];
+    float *out[kMaxMats];
+    int64_t start[kMaxMats + 1];
+};
+inline MatTable single_table(const void *W, int64_t rows, float *out) {
+    MatTable t = {};
+    t.n = 1;
+    t.W[0] = static_cast<const uint8_t *>(W);
+    t.out[0] = out;
+    t.start[0] = 0;
+    t.start[1] = rows;
+    return t;
+}
+
 // The per-format product launchers (qb_gemv_*.cu).  mode 0: rows folded into
-// out; mode 1: per-block C, O, v written instead (testing).
+// out; mode 1: per-block C, O, v written instead (testing).  mats, when not
+// null, replaces W / rows / out by a table of matrices (streaming kernels).
 struct GemvArgs {
     const void *W;
     int64_t rows;
@@ -47,6 +70,7 @@ struct GemvArgs {
     int32_t *dbgO;
     float *dbgV;
     int mode;
+    const MatTable *mats;
 };
 int launch_gemv_q8_0(const GemvArgs &a, cudaStream_t stream);
 int launch_gemv_q4k(const GemvArgs &a, cudaStream_t stream);
@@ -58,6 +82,8 @@ int launch_matvec_q4k(const GemvArgs &a, const float *x, cudaStream_t stream);
 int launch_matvec_q6k(const GemvArgs &a, const float *x, cudaStream_t stream);
 int launch_gemv_f16(const uint16_t *W, int64_t rows, int64_t K, const uint16_t *x16, int ncols, float *out,
                     cudaStream_t stream);
+// Several F16 matrices in one launch; QB_E_ARG when the streaming kernel does not take the shape.
+int launch_gemv_f16_many(const MatTable &t, int64_t K, const uint16_t *x16, int ncols, cudaStream_t stream);
 int launch_check_weights(int fmt, const void *W, int64_t rows, int64_t K, int *flag, cudaStream_t stream);
 
 int num_sms();

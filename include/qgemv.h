@@ -196,6 +196,39 @@ QB_API int q_block_values(qb_fmt fmt, const void *W, int64_t rows, int64_t K, co
  * QB_OK or QB_E_DEVICE. */
 QB_API int q_device_status(void *stream);
 
+/* Most matrices one grouped call (q_gemv_many, q_gemv_f16_many,
+ * q_matvec_many) takes. */
+#define QB_MAX_MATS 4
+
+/* Several matrices that share one activation, in one pass where the shape
+ * allows (bankML forward page: mv_many, qkv -- one quantized activation feeds
+ * Q, K and V, another gate and up; bankML f16 page: mat_vec_multi_par --
+ * several matrices by one column in one pass).  W[i] is a rows[i] x K matrix
+ * in `fmt` (all the same format and K), and out[i][c*rows[i] + r] receives
+ * exactly what q_gemv(fmt, W[i], rows[i], K, act, ncols, out[i], stream)
+ * would write.  W, rows and out are HOST arrays of nmat (1..QB_MAX_MATS)
+ * entries, read during the call; the pointers in them follow q_gemv's rules.
+ * One launch where the streaming kernels take the shape (K % 256 == 0; the
+ * rows of all matrices form one range), else one launch per matrix. */
+QB_API int q_gemv_many(qb_fmt fmt, int nmat, const void *const *W, const int64_t *rows, int64_t K,
+                       const qb_act *act, int ncols, float *const *out, void *stream);
+
+/* q_gemv_f16 for several F16 matrices sharing x16 (same host-array
+ * conventions as q_gemv_many): one launch where the streaming F16 kernel
+ * takes the shape, else one per matrix. */
+QB_API int q_gemv_f16_many(int nmat, const uint16_t *const *W, const int64_t *rows, int64_t K,
+                           const uint16_t *x16, int ncols, float *const *out, void *stream);
+
+/* q_matvec for several matrices sharing the f32 activation x (host arrays as
+ * in q_gemv_many): the activation is quantized once; for one column of a
+ * Q8_0/Q4_K/Q6_K format with K % 256 == 0 the whole call is one launch (no
+ * workspace needed), otherwise quantize_act (or quantize_act_f16) into
+ * `workspace` (q_matvec_workspace_bytes(fmt, K, ncols) bytes) and then the
+ * grouped product.  Results are those of q_matvec for each matrix. */
+QB_API int q_matvec_many(qb_fmt fmt, int nmat, const void *const *W, const int64_t *rows, int64_t K,
+                         const float *x, int ncols, float *const *out, void *workspace, size_t workspace_bytes,
+                         void *stream);
+
 /* A static string for a status code. */
 QB_API const char *q_strerror(int status);
 
