@@ -72,6 +72,12 @@ def lib():
         L.or_f16_to_f32.argtypes, L.or_f16_to_f32.restype = [ctypes.c_uint16], ctypes.c_float
         L.or_gemv_f16.argtypes, L.or_gemv_f16.restype = [P, i64, i64, P, i32, P], i32
         L.or_quantize_f16.argtypes, L.or_quantize_f16.restype = [P, i64, P], None
+        L.or_block_scale.argtypes, L.or_block_scale.restype = [ctypes.c_float, P, P], None
+        L.or_quantize_sub32.argtypes, L.or_quantize_sub32.restype = [P, i64, i32, P, P, P, P], None
+        L.or_exact_sum_f32.argtypes, L.or_exact_sum_f32.restype = [P, P, i32], ctypes.c_float
+        L.or_gemv_sub32_rows.argtypes = [i32, P, i64, i64, i64, i64, P, P, P, i32, P]
+        L.or_gemv_sub32_rows.restype = i32
+        L.or_group_values.argtypes, L.or_group_values.restype = [i32, P, i64, i64, P, P, P, i32, P], i32
     return _lib
 
 
@@ -243,3 +249,60 @@ def gemv_f16(W16: np.ndarray, rows: int, K: int, x16: np.ndarray) -> np.ndarray:
     out = np.zeros((ncols, rows), np.float32)
     assert lib().or_gemv_f16(_p(W16), rows, K, _p(x16), ncols, _p(out)) == 0
     return out
+
+
+# ---------------------------------------------------------------- ActScaling::Sub32
+
+def block_scale(amax: float):
+    """The least m*2^e, m in 8..15, with 127*m*2^e >= amax (numerics page, block_scale)."""
+    m, e = ctypes.c_int(), ctypes.c_int()
+    lib().or_block_scale(np.float32(amax), ctypes.byref(m), ctypes.byref(e))
+    return m.value, e.value
+
+
+def quantize_sub32(x: np.ndarray):
+    """quantize (numerics page) per 32 elements: codes [ncols][K], m, e [ncols][K/32], unit sums."""
+    x = np.ascontiguousarray(np.atleast_2d(x), np.float32)
+    ncols, K = x.shape
+    codes = np.zeros((ncols, K), np.int8)
+    m = np.zeros((ncols, K // 32), np.uint8)
+    e = np.zeros((ncols, K // 32), np.int16)
+    s16 = np.zeros((ncols, K // 16), np.int16)
+    lib().or_quantize_sub32(_p(x), K, ncols, _p(codes), _p(m), _p(e), _p(s16))
+    return codes, m, e, s16
+
+
+def exact_sum_f32(sigs, exps) -> np.float32:
+    """exact_sum (numerics page) of sig*2^exp terms (|sig| < 2^63), rounded once to f32."""
+    sg = np.ascontiguousarray(np.asarray(sigs, np.int64))
+    ex = np.ascontiguousarray(np.asarray(exps, np.int32))
+    return np.float32(lib().or_exact_sum_f32(_p(sg), _p(ex), len(sg)))
+
+
+def gemv_sub32(fmt: int, W: np.ndarray, rows: int, K: int, codes, m, e, r0: int = 0, r1: int | None = None,
+               out: np.ndarray | None = None) -> np.ndarray:
+    """dot under ActScaling::Sub32 for every row and column: out f32 [ncols][rows]."""
+    codes = np.ascontiguousarray(np.atleast_2d(codes), np.int8)
+    m = np.ascontiguousarray(np.atleast_2d(m), np.uint8)
+    e = np.ascontiguousarray(np.atleast_2d(e), np.int16)
+    W = np.ascontiguousarray(W, np.uint8)
+    ncols = codes.shape[0]
+    if out is None:
+        out = np.zeros((ncols, rows), np.float32)
+    r1 = rows if r1 is None else r1
+    rc = lib().or_gemv_sub32_rows(fmt, _p(W), rows, r0, r1, K, _p(codes), _p(m), _p(e), ncols, _p(out))
+    assert rc == 0
+    return out
+
+
+def group_values(fmt: int, W: np.ndarray, rows: int, K: int, codes, m, e) -> np.ndarray:
+    """Each group's value rounded once (lane page, group): v f32 [ncols][rows][K/256]."""
+    codes = np.ascontiguousarray(np.atleast_2d(codes), np.int8)
+    m = np.ascontiguousarray(np.atleast_2d(m), np.uint8)
+    e = np.ascontiguousarray(np.atleast_2d(e), np.int16)
+    W = np.ascontiguousarray(W, np.uint8)
+    ncols = codes.shape[0]
+    v = np.zeros((ncols, rows, K // 256), np.float32)
+    rc = lib().or_group_values(fmt, _p(W), rows, K, _p(codes), _p(m), _p(e), ncols, _p(v))
+    assert rc == 0
+    return v

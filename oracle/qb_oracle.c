@@ -13,7 +13,10 @@
  *                     tree, f32_to_f16, ftz, structs Scale / Segment /
  *                     CodedRow / Unreadable, constants NAN, COEF_BOUND.
  *   lane page       -- its lane module page: block_sums, deliver, lane, and
- *                     the excess-form identity of the unit sums.
+ *                     the excess-form identity of the unit sums; group and
+ *                     deliver32 for ActScaling::Sub32 (block_scale,
+ *                     quantize, ACT_BLOCK = 32, GROUP = 256 on the
+ *                     numerics page).
  *
  * Readings taken where the pages are silent (each restated where used):
  *   R1  an activation block whose largest magnitude is 0 gets the scale
@@ -29,6 +32,11 @@
  *       its sign;
  *   R6  LANES = 8 and the tree is ((l0+l1)+(l2+l3))+((l4+l5)+(l6+l7));
  *   R7  a row with any unreadable block (f16 scale inf or NaN) is NAN.
+ *   R13 (Sub32) an all-zero activation block gets the scale 8*2^0 and zero
+ *       codes, a block holding an infinity m = 0 (as R1, R3 for PerBlock);
+ *   R14 (Sub32) SUM_WINDOW never binds here either: a group's terms are
+ *       summed exactly, whatever the spread of their exponents (a 384-bit
+ *       integer holds every case), then rounded once as in R5.
  *
  * Build: gcc -O2 -std=c11 -ffp-contract=off -fno-fast-math -shared -fPIC.
  * Contraction must stay off: the f32 rule multiplies and adds separately.
@@ -607,3 +615,238 @@ float or_scaled_to_f32_2x64(int64_t hi, uint64_t lo, int ex) {
 /* the f32 bits of a float, for ctypes callers */
 uint32_t or_bits(float f) { return f32_bits(f); }
 float or_from_bits(uint32_t b) { return bits_f32(b); }
+
+
+/* =====================================================================
+ * ActScaling::Sub32 (numerics page: block_scale, quantize, ACT_BLOCK,
+ * GROUP, exact_sum, dot; lane page: group, deliver32).
+ * ===================================================================== */
+
+/* ---------------------------------------------------------------------
+ * block_scale: the least m*2^e, m in 8..15, with 127*m*2^e >= amax, for a
+ * finite positive amax (numerics page, block_scale).  The same search as
+ * wide_scale with a 4-bit significand.
+ * ------------------------------------------------------------------- */
+void or_block_scale(float amax, int *m_out, int *e_out) {
+    int64_t M; int E;
+    f32_split(amax, &M, &E);
+    int best_m = 0, best_e = 0;
+    for (int j = -40; j <= 40; j++) {
+        u128 num = (u128)M, den = 127;
+        if (j >= 0) den <<= j; else num <<= -j;
+        u128 mm = (num + den - 1) / den;
+        if (mm < 8 || mm > 15) continue;
+        int e = E + j;
+        if (best_m == 0) { best_m = (int)mm; best_e = e; continue; }
+        int lo = e < best_e ? e : best_e;
+        u128 a = (u128)mm << (e - lo), b = (u128)best_m << (best_e - lo);
+        if (a < b) { best_m = (int)mm; best_e = e; }
+    }
+    *m_out = best_m;
+    *e_out = best_e;
+}
+
+/* ---------------------------------------------------------------------
+ * quantize: x (a whole number of groups) quantized per ACT_BLOCK = 32
+ * elements under block_scale (numerics page, quantize, ActScaling::Sub32),
+ * codes by rne_div; readings R2, R13.  Scales [ncols][K/32]; unit sums as
+ * for quantize_blocks.
+ * ------------------------------------------------------------------- */
+void or_quantize_sub32(const float *x, int64_t K, int ncols, int8_t *codes, uint8_t *m_out, int16_t *e_out,
+                       int16_t *sums16) {
+    int64_t nb = K / 32;
+    for (int c = 0; c < ncols; c++) {
+        for (int64_t b = 0; b < nb; b++) {
+            const float *xb = x + (int64_t)c * K + b * 32;
+            int8_t *cb = codes + (int64_t)c * K + b * 32;
+            float amax = or_absmax(xb, 32);
+            int m, e;
+            if (isinf(amax)) { m = 0; e = 0; }             /* R13 */
+            else if (amax == 0.0f) { m = 8; e = 0; }       /* R13 */
+            else or_block_scale(amax, &m, &e);
+            for (int i = 0; i < 32; i++) cb[i] = (int8_t)((m == 0) ? 0 : or_rne_div(xb[i], m, e));
+            m_out[(int64_t)c * nb + b] = (uint8_t)m;
+            e_out[(int64_t)c * nb + b] = (int16_t)e;
+        }
+        for (int64_t u = 0; u < K / 16; u++) {
+            int sum = 0;
+            for (int i = 0; i < 16; i++) sum += codes[(int64_t)c * K + u * 16 + i];
+            sums16[(int64_t)c * (K / 16) + u] = (int16_t)sum;
+        }
+    }
+}
+
+/* ---------------------------------------------------------------------
+ * exact_sum of sig_k * 2^E_k (|sig_k| < 2^63) rounded once to f32 (numerics
+ * page, exact_sum, scaled_to_f32; readings R5, R14): the terms are added
+ * exactly in a 384-bit two's-complement integer aligned at the least
+ * exponent, then rounded to nearest even on the f32 grid (2^-149 quantum
+ * below 2^-126), a subnormal result flushed to a zero of its sign, past the
+ * top infinite.  No terms, or an exact zero, is +0.
+ * ------------------------------------------------------------------- */
+#define OR_WL 12  /* 32-bit limbs: 384 bits */
+typedef struct { uint32_t w[OR_WL]; } or_wide;
+
+static void wide_add_shifted(or_wide *acc, int64_t sig, int shift) {
+    /* acc += sig * 2^shift, two's complement, shift >= 0, shift + 64 < 384 */
+    uint32_t t[OR_WL];
+    uint64_t mag = sig < 0 ? (uint64_t)0 - (uint64_t)sig : (uint64_t)sig;
+    memset(t, 0, sizeof t);
+    int limb = shift / 32, bit = shift % 32;
+    /* place mag << bit across limbs */
+    u128 v = (u128)mag << bit;
+    for (int i = 0; i < 4 && limb + i < OR_WL; i++) t[limb + i] = (uint32_t)(v >> (32 * i));
+    if (sig < 0) {  /* negate t */
+        uint64_t carry = 1;
+        for (int i = 0; i < OR_WL; i++) {
+            uint64_t x = (uint64_t)(uint32_t)~t[i] + carry;
+            t[i] = (uint32_t)x;
+            carry = x >> 32;
+        }
+    }
+    uint64_t carry = 0;
+    for (int i = 0; i < OR_WL; i++) {
+        uint64_t x = (uint64_t)acc->w[i] + t[i] + carry;
+        acc->w[i] = (uint32_t)x;
+        carry = x >> 32;
+    }
+}
+
+float or_exact_sum_f32(const int64_t *sig, const int *E, int n) {
+    if (n == 0) return 0.0f;
+    int lo = E[0];
+    for (int k = 1; k < n; k++) if (E[k] < lo) lo = E[k];
+    or_wide acc;
+    memset(&acc, 0, sizeof acc);
+    for (int k = 0; k < n; k++) {
+        if (sig[k] == 0) continue;
+        if (E[k] - lo + 64 >= 32 * OR_WL - 2) return engine_nan();  /* cannot occur for f16 x block_scale terms */
+        wide_add_shifted(&acc, sig[k], E[k] - lo);
+    }
+    int neg = (acc.w[OR_WL - 1] >> 31) & 1;
+    if (neg) {  /* magnitude */
+        uint64_t carry = 1;
+        for (int i = 0; i < OR_WL; i++) {
+            uint64_t x = (uint64_t)(uint32_t)~acc.w[i] + carry;
+            acc.w[i] = (uint32_t)x;
+            carry = x >> 32;
+        }
+    }
+    int p = -1;                                      /* leading place of the magnitude */
+    for (int i = OR_WL - 1; i >= 0 && p < 0; i--)
+        if (acc.w[i]) for (int b = 31; b >= 0; b--) if ((acc.w[i] >> b) & 1) { p = 32 * i + b; break; }
+    if (p < 0) return 0.0f;
+    int x = p + lo;
+    int sub = x < -126;
+    int qe = sub ? -149 : x - 23;
+    int shift = qe - lo;                             /* places below the quantum */
+    uint64_t r;
+    if (shift <= 0) {
+        r = 0;                                       /* exact: the magnitude < 2^25 in quanta */
+        for (int i = OR_WL - 1; i >= 0; i--) r = (r << 32) | acc.w[i];  /* p <= 24 here */
+        r <<= -shift;
+    } else {
+        /* r = floor(mag / 2^shift), rem against half */
+        r = 0;
+        for (int bpos = p; bpos >= shift; bpos--) r = (r << 1) | ((acc.w[bpos / 32] >> (bpos % 32)) & 1);
+        int half = (acc.w[(shift - 1) / 32] >> ((shift - 1) % 32)) & 1;
+        int below = 0;
+        for (int bpos = shift - 2; bpos >= 0 && !below; bpos--) below = (acc.w[bpos / 32] >> (bpos % 32)) & 1;
+        if (half && (below || (r & 1))) r += 1;
+    }
+    if (sub && r < ((uint64_t)1 << 23)) return neg ? -0.0f : 0.0f;
+    if (r == 0) return neg ? -0.0f : 0.0f;
+    double d = ldexp((double)r, qe);
+    if (d >= 3.4028236692093846e38) return neg ? -INFINITY : INFINITY;
+    float f = (float)d;
+    return neg ? -f : f;
+}
+
+/* ---------------------------------------------------------------------
+ * group (lane page): group g (GROUP = 256 elements) of a row -- every 32-
+ * element sub-block's two exact sums times its weight block's scales and its
+ * own activation scale, the terms summed exactly and rounded once (numerics
+ * page, dot under ActScaling::Sub32).  Q8_0: the sub-block is a weight
+ * block, term d_s*m_s*2^e_s*C_s.  Q4_K-like: terms d*m_s*C_s and
+ * -dmin*m_s*O_s at the sub-block's activation exponent.  Q6_K-like: the two
+ * 16-element weight sub-blocks of the activation block make one C_s.  NaN for
+ * an unreadable weight scale or an activation block without a scale.
+ * ------------------------------------------------------------------- */
+static float group_value(const or_row *w, int64_t g, const int8_t *a, const uint8_t *am, const int16_t *ae) {
+    int64_t sig[16]; int E[16]; int n = 0;
+    for (int s = 0; s < 8; s++) {
+        int64_t sb = g * 8 + s;                       /* 32-element activation block */
+        int m = am[sb], e = ae[sb];
+        if (m == 0) return engine_nan();
+        int64_t C = 0, O = 0, sg; int ex;
+        uint16_t d1, d2 = 0; int kind = 0;
+        if (w->fmt == OR_Q8_0) {
+            for (int i = 0; i < 32; i++) C += (int64_t)w->q8[sb * 32 + i] * a[sb * 32 + i];
+            d1 = w->d[sb];
+        } else if (w->fmt == OR_Q4K) {
+            for (int i = 0; i < 32; i++) {
+                int64_t el = sb * 32 + i;
+                C += (int64_t)w->sc[sb] * w->q[el] * a[el];
+                O += (int64_t)w->mn[sb] * a[el];
+            }
+            d1 = w->d[g]; d2 = w->dm[g]; kind = 1;
+        } else {
+            for (int i = 0; i < 32; i++) {
+                int64_t el = sb * 32 + i;
+                C += (int64_t)w->sc6[el / 16] * ((int64_t)w->q[el] - 32) * a[el];
+            }
+            d1 = w->d[g];
+        }
+        if (or_f16_scale(d1, &sg, &ex)) return engine_nan();
+        sig[n] = sg * m * C; E[n] = ex + e; n++;
+        if (kind == 1) {
+            if (or_f16_scale(d2, &sg, &ex)) return engine_nan();
+            sig[n] = -sg * m * O; E[n] = ex + e; n++;
+        }
+    }
+    return or_exact_sum_f32(sig, E, n);
+}
+
+/* ---------------------------------------------------------------------
+ * dot under Sub32: the groups' values added in order from +0 in f32 with ftz
+ * (numerics page, dot).  K a whole number of groups; rows [r0, r1);
+ * out[c*rows + r]; activation scales [ncols][K/32].
+ * ------------------------------------------------------------------- */
+int or_gemv_sub32_rows(int fmt, const uint8_t *W, int64_t rows, int64_t r0, int64_t r1, int64_t K,
+                       const int8_t *codes, const uint8_t *am, const int16_t *ae, int ncols, float *out) {
+    or_row w;
+    if (K % 256) return -1;
+    int64_t ng = K / 256, rec = or_record_bytes(fmt, K);
+    if (row_alloc(&w, fmt, K)) { row_free(&w); return -1; }
+    for (int64_t r = r0; r < r1; r++) {
+        row_unpack(&w, W + r * rec);
+        for (int c = 0; c < ncols; c++) {
+            float acc = 0.0f;
+            for (int64_t g = 0; g < ng; g++)
+                acc = or_ftz(acc + group_value(&w, g, codes + (int64_t)c * K, am + (int64_t)c * (K / 32),
+                                               ae + (int64_t)c * (K / 32)));
+            if (isnan(acc)) acc = engine_nan();
+            out[(int64_t)c * rows + r] = acc;
+        }
+    }
+    row_free(&w);
+    return 0;
+}
+
+/* the group values themselves: v[c][r][g] */
+int or_group_values(int fmt, const uint8_t *W, int64_t rows, int64_t K, const int8_t *codes, const uint8_t *am,
+                    const int16_t *ae, int ncols, float *v) {
+    or_row w;
+    if (K % 256) return -1;
+    int64_t ng = K / 256, rec = or_record_bytes(fmt, K);
+    if (row_alloc(&w, fmt, K)) { row_free(&w); return -1; }
+    for (int64_t r = 0; r < rows; r++) {
+        row_unpack(&w, W + r * rec);
+        for (int c = 0; c < ncols; c++)
+            for (int64_t g = 0; g < ng; g++)
+                v[((int64_t)c * rows + r) * ng + g] =
+                    group_value(&w, g, codes + (int64_t)c * K, am + (int64_t)c * (K / 32), ae + (int64_t)c * (K / 32));
+    }
+    row_free(&w);
+    return 0;
+}
