@@ -32,7 +32,8 @@ LIB_PATH = os.path.join(_HERE, "libqgemv.so")
 # every entry point include/qgemv.h declares
 EXPORTS = ("quantize_act", "q_gemv", "quantize_act_f16", "q_gemv_f16", "q_check_weights", "q_weight_bytes",
            "q_block_values", "q_device_status", "q_strerror", "q_matvec", "q_matvec_workspace_bytes",
-           "q_matvec_static", "q_gemv_many", "q_gemv_f16_many", "q_matvec_many")
+           "q_matvec_static", "q_gemv_many", "q_gemv_f16_many", "q_matvec_many", "quantize_act_sub32",
+           "q_gemv_sub32", "q_matvec_sub32_workspace_bytes", "q_matvec_sub32")
 
 
 class QbError(RuntimeError):
@@ -77,6 +78,11 @@ def lib() -> ctypes.CDLL:
         L.q_gemv_f16_many.argtypes, L.q_gemv_f16_many.restype = [i32, P, P, i64, P, i32, P, P], i32
         L.q_matvec_many.argtypes = [i32, i32, P, P, i64, P, i32, P, P, ctypes.c_size_t, P]
         L.q_matvec_many.restype = i32
+        L.quantize_act_sub32.argtypes, L.quantize_act_sub32.restype = [P, i64, i32, P, P, P, P], i32
+        L.q_gemv_sub32.argtypes, L.q_gemv_sub32.restype = [i32, P, i64, i64, ctypes.POINTER(_Act), i32, P, P], i32
+        L.q_matvec_sub32_workspace_bytes.argtypes, L.q_matvec_sub32_workspace_bytes.restype = [i64, i32], i64
+        L.q_matvec_sub32.argtypes = [i32, P, i64, i64, P, i32, P, P, ctypes.c_size_t, P]
+        L.q_matvec_sub32.restype = i32
         _lib = L
     return _lib
 
@@ -116,6 +122,43 @@ def quantize_act(block: int, x, codes, scales, sums16, stream=None) -> None:
     ncols, K = x.shape
     _check(lib().quantize_act(block, _ptr(x), K, ncols, _ptr(codes), _ptr(scales), _ptr(sums16), _stream(stream)),
            "quantize_act")
+
+
+def quantize_act_sub32(x, codes, scales, sums16, stream=None) -> None:
+    """quantize under ActScaling::Sub32: x f32 [ncols, K] -> codes, scales (per
+    32 elements, m in 8..15), sums16.  Buffers from alloc_act(ncols, K, 32)."""
+    ncols, K = x.shape
+    _check(lib().quantize_act_sub32(_ptr(x), K, ncols, _ptr(codes), _ptr(scales), _ptr(sums16), _stream(stream)),
+           "quantize_act_sub32")
+
+
+def q_gemv_sub32(fmt: int, W, rows: int, K: int, act, ncols: int, out, stream=None) -> None:
+    """dot under Sub32 for every row and column: out f32 [ncols, rows].
+    act = (codes, scales, sums16) as written by quantize_act_sub32."""
+    codes, scales, sums16 = act
+    a = _act(32, codes, scales, sums16)
+    _check(lib().q_gemv_sub32(fmt, _ptr(W), rows, K, ctypes.byref(a), ncols, _ptr(out), _stream(stream)),
+           "q_gemv_sub32")
+
+
+def q_matvec_sub32_workspace_bytes(K: int, ncols: int) -> int:
+    n = lib().q_matvec_sub32_workspace_bytes(K, ncols)
+    if n < 0:
+        raise QbError(int(n), "q_matvec_sub32_workspace_bytes")
+    return int(n)
+
+
+def q_matvec_sub32(fmt: int, W, rows: int, K: int, x, out, workspace=None, stream=None) -> None:
+    """quantize_act_sub32 then q_gemv_sub32 in one call: x f32 [ncols, K] ->
+    out f32 [ncols, rows].  workspace: a 16-byte aligned device buffer of at
+    least q_matvec_sub32_workspace_bytes(K, ncols) bytes (allocated here when
+    None)."""
+    import torch
+    ncols = x.shape[0]
+    if workspace is None:
+        workspace = torch.empty(q_matvec_sub32_workspace_bytes(K, ncols), dtype=torch.uint8, device=x.device)
+    _check(lib().q_matvec_sub32(fmt, _ptr(W), rows, K, _ptr(x), ncols, _ptr(out), _ptr(workspace),
+                                workspace.numel() * workspace.element_size(), _stream(stream)), "q_matvec_sub32")
 
 
 def _act(block, codes, scales, sums16):

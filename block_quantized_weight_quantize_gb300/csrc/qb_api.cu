@@ -400,6 +400,84 @@ int q_matvec_many(qb_fmt fmt, int nmat, const void *const *W, const int64_t *row
     return q_gemv_many(fmt, nmat, W, rows, K, &act, ncols, out, stream);
 }
 
+// ---------------------------------------------------------------- ActScaling::Sub32
+
+int quantize_act_sub32(const float *x, int64_t K, int ncols, int8_t *codes, qb_scale *scales, int16_t *sums16,
+                       void *stream) {
+    if (!x || !codes || !scales || !sums16) return QB_E_ARG;
+    if (K < 0 || K % 256 != 0 || K > (int64_t(1) << 24) || ncols < 1 || ncols > 16) return QB_E_ARG;
+    if (misaligned(x) || misaligned(codes) || (reinterpret_cast<uintptr_t>(scales) & 3u) ||
+        (reinterpret_cast<uintptr_t>(sums16) & 3u))
+        return QB_E_ARG;
+    if (K == 0) return QB_OK;
+    return launch_quantize_sub32(x, K, ncols, codes, scales, sums16, static_cast<cudaStream_t>(stream));
+}
+
+static int check_sub32_args(qb_fmt fmt, const void *W, int64_t rows, int64_t K, const qb_act *act, int ncols,
+                            const void *out) {
+    const int f = fmt_index(fmt);
+    if (f < 0) return QB_E_FORMAT;
+    if (!W || !act || !out || !act->codes || !act->scales) return QB_E_ARG;
+    if (f != kQ8_0 && !act->sums16) return QB_E_ARG;
+    if (act->block != 32) return QB_E_BLOCK;
+    if (rows < 0 || K < 0 || K % 256 != 0 || K > kMaxK || ncols < 1 || ncols > 16) return QB_E_ARG;
+    if (rows > (int64_t(1) << 31)) return QB_E_ARG;
+    if (misaligned(W) || misaligned(act->codes) || (act->sums16 && misaligned(act->sums16)) ||
+        misaligned(act->scales) || (reinterpret_cast<uintptr_t>(out) & 3u))
+        return QB_E_ARG;
+    return QB_OK;
+}
+
+int q_gemv_sub32(qb_fmt fmt, const void *W, int64_t rows, int64_t K, const qb_act *act, int ncols, float *out,
+                 void *stream) {
+    const int rc = check_sub32_args(fmt, W, rows, K, act, ncols, out);
+    if (rc) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (rows == 0) return QB_OK;
+    if (K == 0)
+        return cudaMemsetAsync(out, 0, (size_t)ncols * rows * sizeof(float), s) == cudaSuccess ? QB_OK : QB_E_CUDA;
+    GemvArgs a = {};
+    a.W = W;
+    a.rows = rows;
+    a.K = K;
+    a.codes = act->codes;
+    a.scales = act->scales;
+    a.sums16 = act->sums16;
+    a.ncols = ncols;
+    a.out = out;
+    switch (fmt_index(fmt)) {
+    case kQ8_0: return launch_gemv_sub32_q8_0(a, s);
+    case kQ4K: return launch_gemv_sub32_q4k(a, s);
+    default: return launch_gemv_sub32_q6k(a, s);
+    }
+}
+
+int64_t q_matvec_sub32_workspace_bytes(int64_t K, int ncols) {
+    if (K < 0 || K % 256 != 0 || ncols < 1 || ncols > 16) return QB_E_ARG;
+    return align16(K * ncols) + align16(4 * (K / 32) * ncols) + align16(2 * (K / 16) * ncols);
+}
+
+int q_matvec_sub32(qb_fmt fmt, const void *W, int64_t rows, int64_t K, const float *x, int ncols, float *out,
+                   void *workspace, size_t workspace_bytes, void *stream) {
+    if (!x || misaligned(x)) return QB_E_ARG;
+    const int64_t need = q_matvec_sub32_workspace_bytes(K, ncols);
+    if (need < 0) return (int)need;
+    if (!workspace || (int64_t)workspace_bytes < need || misaligned(workspace)) return QB_E_ARG;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    qb_act act;
+    act.block = 32;
+    act.codes = reinterpret_cast<const int8_t *>(ws);
+    act.scales = reinterpret_cast<const qb_scale *>(ws + align16(K * ncols));
+    act.sums16 = reinterpret_cast<const int16_t *>(ws + align16(K * ncols) + align16(4 * (K / 32) * ncols));
+    int rc = check_sub32_args(fmt, W, rows, K, &act, ncols, out);
+    if (rc) return rc;
+    if (rows == 0) return QB_OK;
+    rc = quantize_act_sub32(x, K, ncols, const_cast<int8_t *>(act.codes), const_cast<qb_scale *>(act.scales),
+                            const_cast<int16_t *>(act.sums16), stream);
+    if (rc) return rc;
+    return q_gemv_sub32(fmt, W, rows, K, &act, ncols, out, stream);
+}
+
 const char *q_strerror(int status) {
     switch (status) {
     case QB_OK: return "ok";

@@ -31,6 +31,8 @@ inline int launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t sm
 
 int launch_quantize_act(int block, const float *x, int64_t K, int ncols, int8_t *codes, qb_scale *scales,
                         int16_t *sums16, cudaStream_t stream);
+int launch_quantize_sub32(const float *x, int64_t K, int ncols, int8_t *codes, qb_scale *scales, int16_t *sums16,
+                          cudaStream_t stream);
 int launch_quantize_f16(const float *x, int64_t n, uint16_t *x16, cudaStream_t stream);
 
 // Matrices that share one activation (the same K and format), seen by a
@@ -75,6 +77,11 @@ struct GemvArgs {
 int launch_gemv_q8_0(const GemvArgs &a, cudaStream_t stream);
 int launch_gemv_q4k(const GemvArgs &a, cudaStream_t stream);
 int launch_gemv_q6k(const GemvArgs &a, cudaStream_t stream);
+// The product under ActScaling::Sub32 (activation scales per 32 elements,
+// one rounding per 256-element group).
+int launch_gemv_sub32_q8_0(const GemvArgs &a, cudaStream_t stream);
+int launch_gemv_sub32_q4k(const GemvArgs &a, cudaStream_t stream);
+int launch_gemv_sub32_q6k(const GemvArgs &a, cudaStream_t stream);
 // The single-launch product (activation quantized inside the kernel); returns
 // QB_E_ARG when that kernel does not apply to the shape.
 int launch_matvec_q8_0(const GemvArgs &a, const float *x, cudaStream_t stream);

@@ -8,6 +8,10 @@
 // the codes of every 16-element unit (the activation side's unit sums of the
 // block-scale lane page).
 //
+// quantize_act_sub32: quantize under ActScaling::Sub32 (numerics page): per
+// ACT_BLOCK = 32 elements, block_scale (the least m*2^e, m in 8..15, with
+// 127*m*2^e >= amax), then rne_div as above; the same unit sums.
+//
 // quantize_act_f16: f32_to_f16 (numerics page) by the hardware conversion
 // cvt.rn.f16.f32, NaN canonicalised.
 #include <cuda_fp16.h>
@@ -20,7 +24,7 @@ namespace qb {
 
 // One thread per 8 consecutive elements; a block of B elements spans B/8
 // consecutive lanes of one warp (4 lanes for B = 32, 32 lanes for B = 256).
-template <int B>
+template <int B, bool S32>
 __global__ void __launch_bounds__(256) quantize_act_kernel(const float *__restrict__ x, int64_t n8, int K,
                                                            int8_t *__restrict__ codes, qb_scale *__restrict__ scales,
                                                            int16_t *__restrict__ sums16) {
@@ -44,7 +48,7 @@ __global__ void __launch_bounds__(256) quantize_act_kernel(const float *__restri
     uint2 c;
     int usum;
     uint32_t scale;
-    quantize8<L>(xb, c, usum, scale);
+    quantize8<L, S32>(xb, c, usum, scale);
     if (live) {
         *reinterpret_cast<uint2 *>(codes + t * 8) = c;
         if ((t & 1) == 0) sums16[t >> 1] = (int16_t)usum;
@@ -70,8 +74,15 @@ int launch_quantize_act(int block, const float *x, int64_t K, int ncols, int8_t 
     const unsigned grid = (unsigned)((n8 + 255) / 256);
     // every grid's blocks begin at a multiple of the block's lanes (K % block == 0)
     if (block == 32)
-        return launch_pdl(quantize_act_kernel<32>, grid, 256, 0, stream, x, n8, (int)K, codes, scales, sums16);
-    return launch_pdl(quantize_act_kernel<256>, grid, 256, 0, stream, x, n8, (int)K, codes, scales, sums16);
+        return launch_pdl(quantize_act_kernel<32, false>, grid, 256, 0, stream, x, n8, (int)K, codes, scales, sums16);
+    return launch_pdl(quantize_act_kernel<256, false>, grid, 256, 0, stream, x, n8, (int)K, codes, scales, sums16);
+}
+
+int launch_quantize_sub32(const float *x, int64_t K, int ncols, int8_t *codes, qb_scale *scales, int16_t *sums16,
+                          cudaStream_t stream) {
+    const int64_t n8 = K * ncols / 8;
+    const unsigned grid = (unsigned)((n8 + 255) / 256);
+    return launch_pdl(quantize_act_kernel<32, true>, grid, 256, 0, stream, x, n8, (int)K, codes, scales, sums16);
 }
 
 int launch_quantize_f16(const float *x, int64_t n, uint16_t *x16, cudaStream_t stream) {

@@ -30,13 +30,29 @@ __device__ __forceinline__ void wide_scale_bits(uint32_t amax, int &m, int &e) {
     e = ee;
 }
 
+// block_scale (numerics page, ActScaling::Sub32): the same search with a 4-bit
+// significand.  At e = E8-137 the least m is ceil(M / (127*2^13)), in 9..17;
+// past 15 the next exponent gives ceil(M / (127*2^14)), 8 or 9.  m = 0 marks
+// an infinity, an all-zero block gets 8 * 2^0.
+__device__ __forceinline__ void block_scale_bits(uint32_t amax, int &m, int &e) {
+    if (amax == 0x7F800000u) { m = 0; e = 0; return; }
+    if (amax == 0) { m = 8; e = 0; return; }
+    const uint32_t E8 = amax >> 23, M = (amax & 0x7FFFFFu) | 0x800000u;
+    uint32_t mm = (M + 1040383u) / 1040384u;
+    int ee = (int)E8 - 137;
+    if (mm > 15u) { mm = (M + 2080767u) / 2080768u; ++ee; }
+    m = (int)mm;
+    e = ee;
+}
+
 // rne_div of one element, exactly, on the integer fields: |x| = mant *
 // 2^(E8x-150), so x/s = mant / (m * 2^k) with k = e - (E8x-150).  Every
-// |x| <= amax has k >= 9 (|x/s| <= 127 forces it); k >= 18 puts |x/s| below
-// 1/2, code 0.  Otherwise hi = mant >> k < 2^15, and floor(hi / m) is
-// (hi * ceil(2^24/m)) >> 24 (the product overestimates hi/m by less than
-// hi/2^24 < 2^-9 < 1/m, so the floor is exact for m < 512; the product fits
-// 32 bits).  With rem = hi - q*m and lo = mant mod 2^k, the remainder is
+// |x| <= amax has |x/s| <= 127, which forces k >= 9 for m <= 255 and k >= 13
+// for m <= 15; k >= 22 puts |x/s| below 1/2 for any m >= 8, code 0.
+// Otherwise hi = mant >> k (< 2^15 for m >= 128, < 2^11 for m <= 15), and
+// floor(hi / m) is (hi * ceil(2^24/m)) >> 24: the product overestimates hi/m
+// by less than hi/2^24 < 1/m, so the floor is exact, and it fits 32 bits
+// (hi * ceil(2^24/m) < 2^15 * 2^17 for m >= 128, < 2^11 * 2^21 for m >= 8).  With rem = hi - q*m and lo = mant mod 2^k, the remainder is
 // R = rem*2^k + lo, and 2R - m*2^k = (2*rem - m)*2^k + 2*lo decides the
 // rounding, ties to even.  A denormal, NaN or (m = 0) element gets code 0.
 // Out of line: only the rare elements the fast path below cannot decide
@@ -44,7 +60,7 @@ __device__ __forceinline__ void wide_scale_bits(uint32_t amax, int &m, int &e) {
 static __device__ __noinline__ int rne_div1_exact(uint32_t xbits, int m, int e) {
     const uint32_t a = xbits & 0x7FFFFFFFu;
     const int k = e - ((int)(a >> 23) - 150);
-    const bool valid = (m != 0) & (a >= 0x00800000u) & (a < 0x7F800000u) & (k <= 17);
+    const bool valid = (m != 0) & (a >= 0x00800000u) & (a < 0x7F800000u) & (k <= 21);
     const int kc = valid ? k : 9;
     const uint32_t mu = valid ? (uint32_t)m : 128u;
     const uint32_t magic = ((1u << 24) + mu - 1u) / mu;
@@ -66,14 +82,16 @@ static __device__ __noinline__ int rne_div1_exact(uint32_t xbits, int m, int e) 
 // absmax: max of |x| with denormal inputs flushed to zero (abs.ftz), NaN
 // passed over (max returns the other operand), +inf kept.
 // rne_div fast path in f32: c = RN(1/m) * 2^-e is exact (an exponent-field
-// subtraction; a normal number for e in [-134, 118]), and qf = RN(x * c) with
+// subtraction; a normal number for e in [-134, 118] when m is 128..255, in
+// [-130, 122] when m is 8..15), and qf = RN(x * c) with
 // denormal inputs and results flushed (both mean |x/s| < 1/2, code 0) is
 // RN(x' * RN(1/m)) for x' = x * 2^-e, within |x/s| * 2^-23 (1 + 2^-23) <
 // 2^-16 of x/s (|x/s| <= 127).  So unless qf lies within 2^-16 of a
 // half-integer, x/s lies on the same side of every half-integer as qf and its
 // nearest integer is rint(qf).  Elements in that band (exact ties among
 // them), and blocks with e outside the range, take the exact routine.
-template <int L>
+// S32: the scale is block_scale (ActScaling::Sub32) instead of wide_scale.
+template <int L, bool S32 = false>
 __device__ __forceinline__ void quantize8(const uint32_t (&xb)[8], uint2 &codes, int &unit_sum, uint32_t &scale) {
     float am = 0.0f;
 #pragma unroll
@@ -89,9 +107,10 @@ __device__ __forceinline__ void quantize8(const uint32_t (&xb)[8], uint2 &codes,
         amax = u > amax ? u : amax;
     }
     int m, e;
-    wide_scale_bits(amax, m, e);
+    if (S32) block_scale_bits(amax, m, e);
+    else wide_scale_bits(amax, m, e);
     int q[8];
-    if ((m != 0) & (e >= -134) & (e <= 118)) {
+    if ((m != 0) & (e >= (S32 ? -130 : -134)) & (e <= (S32 ? 122 : 118))) {
         const float inv_m = __frcp_rn((float)m);
         const float c = __uint_as_float(__float_as_uint(inv_m) - ((uint32_t)e << 23));
 #pragma unroll

@@ -1,0 +1,7 @@
+// qb_sub32_q8_0.cu -- the ActScaling::Sub32 product for one weight format (a
+// translation unit of its own so the formats compile in parallel).
+#include "qb_sub32.cuh"
+
+namespace qb {
+int launch_gemv_sub32_q8_0(const GemvArgs &a, cudaStream_t stream) { return launch_gemv_sub32<kQ8_0>(a, stream); }
+}  // namespace qb

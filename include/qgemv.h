@@ -229,6 +229,50 @@ QB_API int q_matvec_many(qb_fmt fmt, int nmat, const void *const *W, const int64
                          const float *x, int ncols, float *const *out, void *workspace, size_t workspace_bytes,
                          void *stream);
 
+/* ---- ActScaling::Sub32 (numerics page: block_scale, quantize, ACT_BLOCK,
+ * GROUP, exact_sum, dot; block-scale lane page: group).
+ *
+ * The activation is quantized per 32 elements with a 4-bit scale
+ * significand; a row's dot is made of groups of 256 elements, each group's
+ * terms (every 32-element sub-block's integer sums times its weight scales
+ * and its own activation scale) summed exactly and rounded once to f32 (the
+ * same rounding as above), the group values then added in group order from +0
+ * (f32, round to nearest even, subnormal results flushed). */
+
+/* quantize (numerics page, ActScaling::Sub32): x f32 [ncols][K] per 32
+ * elements under block_scale -- the least m*2^e, m in 8..15, with
+ * 127*m*2^e >= the block's largest magnitude (a denormal read as zero, NaN
+ * passed over) -- and codes the nearest integers of x/(m*2^e), ties to even
+ * (a denormal or NaN element: 0).  An all-zero block gets m=8, e=0; a block
+ * with an infinity m=0 (no scale).  Writes codes int8 [ncols][K], scales
+ * [ncols][K/32] and sums16 [ncols][K/16] (device memory, caller-owned).
+ * K % 256 == 0 (whole groups), K <= 2^24, ncols in 1..16; x and codes 16-byte
+ * aligned. */
+QB_API int quantize_act_sub32(const float *x, int64_t K, int ncols, int8_t *codes, qb_scale *scales,
+                              int16_t *sums16, void *stream);
+
+/* dot under Sub32 for every row of W (fmt QB_Q8_0, QB_Q4K or QB_Q6K, the
+ * layouts above) and every column of act: out[c*rows + r].  act->block must
+ * be 32 (scales per 32 elements, as quantize_act_sub32 writes them; any m in
+ * 1..255 and e give the exact result, m = 0 gives NaN).  K % 256 == 0,
+ * K <= 2^18, ncols in 1..16; sums16 needed for Q4K and Q6K; weights, codes,
+ * scales and sums16 16-byte aligned.  A group holding an activation block
+ * without a scale or an unreadable weight scale makes the row the engine's
+ * NaN 0x7FC00000, as does (never for block_scale scales with f16 weight
+ * scales) a group whose terms' exponents lie 318 or more places apart. */
+QB_API int q_gemv_sub32(qb_fmt fmt, const void *W, int64_t rows, int64_t K, const qb_act *act, int ncols,
+                        float *out, void *stream);
+
+/* Workspace bytes q_matvec_sub32 needs (codes, scales and unit sums of the
+ * quantized activation), or a negative QB_E_* code. */
+QB_API int64_t q_matvec_sub32_workspace_bytes(int64_t K, int ncols);
+
+/* quantize_act_sub32 into `workspace` (16-byte aligned, at least
+ * q_matvec_sub32_workspace_bytes(K, ncols) bytes), then q_gemv_sub32: two
+ * launches on `stream`. */
+QB_API int q_matvec_sub32(qb_fmt fmt, const void *W, int64_t rows, int64_t K, const float *x, int ncols,
+                          float *out, void *workspace, size_t workspace_bytes, void *stream);
+
 /* A static string for a status code. */
 QB_API const char *q_strerror(int status);
 
