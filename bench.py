@@ -10,7 +10,11 @@ reads a different copy of the matrix, and the copies total more than 4x the
 L2, so every step streams its weights from HBM.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
-                  [--workload q4k_4096x4096|q8_0_512x1024|q6k_14336x4096|f16_49152x576]
+                  [--workload q4k_4096x4096|q8_0_512x1024|q6k_14336x4096|f16_49152x576|...]
+
+Workloads ending in _sub32 run the ActScaling::Sub32 product (activation
+scales per 32 elements, one rounding per 256-element group): quantize_act_sub32
+then q_gemv_sub32, two launches a step.
 
 Prints one JSON line.  --impl reference times the CPU oracle (test
 infrastructure; a deliberately plain scalar C program) on the host cores.
@@ -43,7 +47,17 @@ WORKLOADS = {
     "q6k_14336x4096": (synth.FMT_Q6K, 14336, 4096, 1, 2, 0.0, "Q6_K-like FFN gate 14336x4096, batch 1"),
     "f16_49152x576": (synth.FMT_F16, 49152, 576, 1, 3, 0.0, "F16 tied-embedding logits 49152x576, batch 1"),
     "q4k_4096x4096_b16": (synth.FMT_Q4K, 4096, 4096, 16, 1, 0.001, "Q4_K-like GEMV 4096x4096, 16 columns"),
+    # ActScaling::Sub32: activation scales per 32 elements, one rounding per 256-element group
+    "q4k_4096x4096_sub32": (synth.FMT_Q4K, 4096, 4096, 1, 1, 0.001,
+                            "Q4_K-like GEMV 4096x4096, batch 1, activation scaled per 32 (Sub32)"),
+    "q4k_4096x4096_b16_sub32": (synth.FMT_Q4K, 4096, 4096, 16, 1, 0.001,
+                                "Q4_K-like GEMV 4096x4096, 16 columns, activation scaled per 32 (Sub32)"),
+    "q8_0_4096x4096_sub32": (synth.FMT_Q8_0, 4096, 4096, 1, 5, 0.001,
+                             "Q8_0 GEMV 4096x4096, batch 1, activation scaled per 32 (Sub32)"),
+    "q6k_14336x4096_sub32": (synth.FMT_Q6K, 14336, 4096, 1, 2, 0.0,
+                             "Q6_K-like FFN gate 14336x4096, batch 1, activation scaled per 32 (Sub32)"),
 }
+SUB32 = {k for k in WORKLOADS if k.endswith("_sub32")}
 
 
 # Matrices that share one activation, run as one grouped call (q_matvec_many):
@@ -123,12 +137,12 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def algorithmic_bytes(fmt, rows, K, ncols):
+def algorithmic_bytes(fmt, rows, K, ncols, sub32=False):
     """Weights + activation (codes, 4-B block scales, 2-B unit sums) + outputs."""
     wb = synth.weight_bytes(fmt, rows, K)
     if fmt == synth.FMT_F16:
         return wb, wb + ncols * 2 * K + 4 * rows * ncols
-    blk = synth.BLOCK[fmt]
+    blk = 32 if sub32 else synth.BLOCK[fmt]
     return wb, wb + ncols * (K + 4 * (K // blk) + 2 * (K // 16)) + 4 * rows * ncols
 
 
@@ -140,8 +154,9 @@ DP4A_PEAK_TOPS = 64 * 8 * 152 * 2.07e9 / 1e12
 
 
 def roofline(fmt, ncols, single, achieved, peak, peak_kind, traffic, roof_bytes, per_launch_s, prod_s, abytes,
-             ops_per_step, roof_launches):
+             ops_per_step, roof_launches, sub32=False):
     name = ("gemv_f16_kernel" if fmt == synth.FMT_F16 else
+            f"s32_kernel<{synth.FORMAT_NAMES[fmt]}, {min(ncols, 2)} column(s) a thread group>" if sub32 else
             f"gemv2_kernel<{synth.FORMAT_NAMES[fmt]}, single launch> (quantize + product)" if single else
             f"gemv3_kernel<{synth.FORMAT_NAMES[fmt]}, {ncols} columns>")
     prod = {"avg_launch_us": round(prod_s * 1e6, 4),
@@ -294,13 +309,14 @@ def run_ours(args, rank, world):
     import block_quantized_weight_quantize_gb300 as qb
 
     fmt, rows, K, ncols, seed, outl, desc = WORKLOADS[args.workload]
+    sub32 = args.workload in SUB32
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
     rng = np.random.default_rng(seed + 1000 * rank)
     lg = synth.draw(fmt, rng, rows, K)
     Wh = synth.pack(fmt, lg)
     x = synth.draw_act(rng, ncols, K, outlier_frac=outl)
-    wbytes, abytes = algorithmic_bytes(fmt, rows, K, ncols)
+    wbytes, abytes = algorithmic_bytes(fmt, rows, K, ncols, sub32)
     ncopy = max(2, -(-4 * L2_BYTES // wbytes))        # copies totalling >= 4x L2
     W = torch.empty((ncopy, Wh.size), dtype=torch.uint8, device=dev)
     W[0].copy_(torch.from_numpy(Wh))
@@ -310,20 +326,29 @@ def run_ours(args, rank, world):
     out = torch.empty((ncols, rows), dtype=torch.float32, device=dev)
     if fmt == synth.FMT_F16:
         act = torch.empty((ncols, K), dtype=torch.int16, device=dev)
+    elif sub32:
+        act = qb.alloc_act(ncols, K, 32, dev)
+        qb.quantize_act_sub32(xd, *act)
     else:
         act = qb.alloc_act(ncols, K, synth.BLOCK[fmt], dev)
         qb.quantize_act(synth.BLOCK[fmt], xd, *act)
-    ws = torch.empty(qb.q_matvec_workspace_bytes(fmt, K, ncols), dtype=torch.uint8, device=dev)
+    ws = torch.empty(qb.q_matvec_sub32_workspace_bytes(K, ncols) if sub32 else
+                     qb.q_matvec_workspace_bytes(fmt, K, ncols), dtype=torch.uint8, device=dev)
     # one launch per step where the single-launch product applies, else two
-    single = fmt != synth.FMT_F16 and ncols == 1 and K % 256 == 0
+    single = fmt != synth.FMT_F16 and ncols == 1 and K % 256 == 0 and not sub32
     launches_per_step = 1 if single else 2
     stream = torch.cuda.Stream(dev)
 
     def step(i, s):
-        qb.q_matvec(fmt, W[i % ncopy], rows, K, xd, out, workspace=ws, stream=s)
+        if sub32:
+            qb.q_matvec_sub32(fmt, W[i % ncopy], rows, K, xd, out, workspace=ws, stream=s)
+        else:
+            qb.q_matvec(fmt, W[i % ncopy], rows, K, xd, out, workspace=ws, stream=s)
 
     def gemv_only(i, s):
-        if fmt == synth.FMT_F16:
+        if sub32:
+            qb.q_gemv_sub32(fmt, W[i % ncopy], rows, K, act, ncols, out, s)
+        elif fmt == synth.FMT_F16:
             qb.q_gemv_f16(W[i % ncopy], rows, K, act, ncols, out, s)
         else:
             qb.q_gemv(fmt, W[i % ncopy], rows, K, act, ncols, out, s)
@@ -463,7 +488,8 @@ def run_ours(args, rank, world):
             "weight_bytes_per_step": wbytes,
             "l2": f"each step reads a different one of {ncopy} weight copies ({ncopy * wbytes / 2**20:.0f} MiB "
                   f"> 4x L2); no flush",
-            "timing": f"CUDA graphs of {G} steps (q_matvec: activation quantization + product, "
+            "timing": f"CUDA graphs of {G} steps ({'q_matvec_sub32' if sub32 else 'q_matvec'}: activation "
+                      f"quantization + product, "
                       f"{launches_per_step} launch(es) a step, programmatic dependent launch) replayed; "
                       f"CUDA events on the launching stream",
             "parallelism": "replicas" if world > 1 else "single GPU",
@@ -475,19 +501,21 @@ def run_ours(args, rank, world):
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
         "roofline": roofline(fmt, ncols, single, achieved, peak, peak_kind, traffic, roof_bytes, per_launch_s,
-                             prod_s, abytes, ops_per_step, args.roof_launches),
+                             prod_s, abytes, ops_per_step, args.roof_launches, sub32),
         "e2e": {
             "value": round(world * wbytes * n_e2e / e2e_s / 1e9, 2),
             "unit": "GB/s",
             "h2d_bytes_per_step": int(x.nbytes),
             "d2h_bytes_per_step": int(4 * rows * ncols),
             "steps": n_e2e,
-            "how": "per step: pinned x -> device, q_matvec through the Python binding, out -> pinned host; "
+            "how": f"per step: pinned x -> device, {'q_matvec_sub32' if sub32 else 'q_matvec'} through the Python "
+                   "binding, out -> pinned host; "
                    "host wall clock over all steps",
         },
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        res["cpu_baseline"] = cpu_baseline(fmt, rows, K, ncols, Wh, x, wbytes, budget_s=args.cpu_seconds)
+        res["cpu_baseline"] = cpu_baseline(fmt, rows, K, ncols, Wh, x, wbytes, budget_s=args.cpu_seconds,
+                                           sub32=sub32)
     return res
 
 
@@ -508,7 +536,7 @@ def _pool(n):
     return _POOL
 
 
-def oracle_pass(fmt, rows, K, Wh, x, nthreads, row_limit=None):
+def oracle_pass(fmt, rows, K, Wh, x, nthreads, row_limit=None, sub32=False):
     """quantize + product over (a sample of) rows, rows split across threads
     (ctypes releases the GIL; the oracle is reentrant)."""
     import oracle
@@ -521,20 +549,21 @@ def oracle_pass(fmt, rows, K, Wh, x, nthreads, row_limit=None):
         list(ex.map(lambda c: oracle.gemv_f16(np.ascontiguousarray(W16[c]), len(c), K, x16)
                     if len(c) else None, chunks))
         return r_end
-    codes, m, e, _ = oracle.quantize_blocks(x, synth.BLOCK[fmt])
+    codes, m, e, _ = oracle.quantize_sub32(x) if sub32 else oracle.quantize_blocks(x, synth.BLOCK[fmt])
     out = np.zeros((x.shape[0], rows), np.float32)
     bounds = np.linspace(0, r_end, nthreads + 1).astype(int)
-    list(ex.map(lambda i: oracle.gemv(fmt, Wh, rows, K, codes, m, e, int(bounds[i]), int(bounds[i + 1]), out),
+    prod = oracle.gemv_sub32 if sub32 else oracle.gemv
+    list(ex.map(lambda i: prod(fmt, Wh, rows, K, codes, m, e, int(bounds[i]), int(bounds[i + 1]), out),
                 range(nthreads)))
     return r_end
 
 
-def cpu_baseline(fmt, rows, K, ncols, Wh, x, wbytes, budget_s=10.0):
+def cpu_baseline(fmt, rows, K, ncols, Wh, x, wbytes, budget_s=10.0, sub32=False):
     n = _oracle_threads()
-    oracle_pass(fmt, rows, K, Wh, x, n)          # warm (also builds the oracle if needed)
+    oracle_pass(fmt, rows, K, Wh, x, n, sub32=sub32)          # warm (also builds the oracle if needed)
     reps, t0 = 0, time.perf_counter()
     while True:
-        oracle_pass(fmt, rows, K, Wh, x, n)
+        oracle_pass(fmt, rows, K, Wh, x, n, sub32=sub32)
         reps += 1
         el = time.perf_counter() - t0
         if el >= budget_s:
@@ -546,6 +575,7 @@ def cpu_baseline(fmt, rows, K, ncols, Wh, x, wbytes, budget_s=10.0):
 
 def run_reference(args):
     fmt, rows, K, ncols, seed, outl, desc = WORKLOADS[args.workload]
+    sub32 = args.workload in SUB32
     rng = np.random.default_rng(seed)
     lg = synth.draw(fmt, rng, rows, K)
     Wh = synth.pack(fmt, lg)
@@ -553,15 +583,15 @@ def run_reference(args):
     n = _oracle_threads()
     # size each step's row sample so the whole run stays within ~2 minutes
     t0 = time.perf_counter()
-    oracle_pass(fmt, rows, K, Wh, x, n)
+    oracle_pass(fmt, rows, K, Wh, x, n, sub32=sub32)
     full = time.perf_counter() - t0
     budget = 100.0 / max(1, args.steps + args.warmup)
     rows_s = int(max(1, min(rows, rows * budget / max(full, 1e-6))))
     for _ in range(args.warmup):
-        oracle_pass(fmt, rows, K, Wh, x, n, rows_s)
+        oracle_pass(fmt, rows, K, Wh, x, n, rows_s, sub32=sub32)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        oracle_pass(fmt, rows, K, Wh, x, n, rows_s)
+        oracle_pass(fmt, rows, K, Wh, x, n, rows_s, sub32=sub32)
     el = time.perf_counter() - t0
     rec = synth.record_bytes(fmt, K)
     value = rec * rows_s * args.steps / el / 1e9
