@@ -78,6 +78,13 @@ def lib():
         L.or_gemv_sub32_rows.argtypes = [i32, P, i64, i64, i64, i64, P, P, P, i32, P]
         L.or_gemv_sub32_rows.restype = i32
         L.or_group_values.argtypes, L.or_group_values.restype = [i32, P, i64, i64, P, P, P, i32, P], i32
+        L.or_int8_code.argtypes, L.or_int8_code.restype = [ctypes.c_float, ctypes.c_float], i32
+        L.or_cache_rows.argtypes, L.or_cache_rows.restype = [P, i64, i32, P, P], None
+        L.or_quantize_heads.argtypes, L.or_quantize_heads.restype = [i32, P, i32, i32, P, P, P], i32
+        L.or_int8_score.argtypes = [P, P, P, i32, i32, i32, P, ctypes.c_uint16]
+        L.or_int8_score.restype = ctypes.c_float
+        L.or_kv_scores.argtypes = [i32, P, P, P, i32, i32, P, P, i64, i64, i32, ctypes.c_float, P]
+        L.or_kv_scores.restype = i32
     return _lib
 
 
@@ -306,3 +313,63 @@ def group_values(fmt: int, W: np.ndarray, rows: int, K: int, codes, m, e) -> np.
     rc = lib().or_group_values(fmt, _p(W), rows, K, _p(codes), _p(m), _p(e), ncols, _p(v))
     assert rc == 0
     return v
+
+
+# ---------------------------------------------------------------- the int8 cache's score path
+
+def int8_code(x: float, inv: float) -> int:
+    """int8_codes (numerics page) of one element under the inverse scale inv."""
+    return int(lib().or_int8_code(np.float32(x), np.float32(inv)))
+
+
+def cache_rows(x: np.ndarray):
+    """cache_row (numerics page) of every row of x f32 [n][d]: codes int8 [n][d], f16 scale bits uint16 [n]."""
+    x = np.ascontiguousarray(np.atleast_2d(x), np.float32)
+    n, d = x.shape
+    codes = np.zeros((n, d), np.int8)
+    scales = np.zeros(n, np.uint16)
+    lib().or_cache_rows(_p(x), n, d, _p(codes), _p(scales))
+    return codes, scales
+
+
+def head_width(scaling: int, d: int) -> int:
+    """Codes a quantized head holds: d rounded up to whole groups under Sub32 (1), d under PerBlock (0)."""
+    return (d + 255) // 256 * 256 if scaling == 1 else d
+
+
+def quantize_heads(scaling: int, q: np.ndarray):
+    """quantize_head (numerics page) of q f32 [nh][d]: codes [nh][dp], m, e [nh][dp/32] (Sub32) or [nh][1]."""
+    q = np.ascontiguousarray(np.atleast_2d(q), np.float32)
+    nh, d = q.shape
+    dp = head_width(scaling, d)
+    nb = dp // 32 if scaling == 1 else 1
+    codes = np.zeros((nh, dp), np.int8)
+    m = np.zeros((nh, nb), np.uint8)
+    e = np.zeros((nh, nb), np.int16)
+    assert lib().or_quantize_heads(scaling, _p(q), nh, d, _p(codes), _p(m), _p(e)) == 0
+    return codes, m, e
+
+
+def int8_score(qc, m, e, blk: int, d: int, kc, ks: int) -> np.float32:
+    """int8_score (numerics page) of one quantized query head against one cached key row."""
+    qc = np.ascontiguousarray(qc, np.int8)
+    m = np.ascontiguousarray(m, np.uint8)
+    e = np.ascontiguousarray(e, np.int16)
+    kc = np.ascontiguousarray(kc, np.int8)
+    return np.float32(lib().or_int8_score(_p(qc), _p(m), _p(e), blk, len(m), d, _p(kc), int(ks)))
+
+
+def kv_scores(scaling: int, qc, qm, qe, d: int, kc, ks, L: int, nkv: int, scale: float) -> np.ndarray:
+    """Scores of every query head against L cached key rows: out f32 [nh][L].
+    kc int8 [nkv][lcap][d], ks uint16 [nkv][lcap]."""
+    qc = np.ascontiguousarray(qc, np.int8)
+    qm = np.ascontiguousarray(qm, np.uint8)
+    qe = np.ascontiguousarray(qe, np.int16)
+    kc = np.ascontiguousarray(kc, np.int8)
+    ks = np.ascontiguousarray(ks, np.uint16)
+    nh = qc.shape[0]
+    lcap = kc.shape[1]
+    out = np.zeros((nh, L), np.float32)
+    assert lib().or_kv_scores(scaling, _p(qc), _p(qm), _p(qe), nh, d, _p(kc), _p(ks), L, lcap, nkv,
+                              np.float32(scale), _p(out)) == 0
+    return out

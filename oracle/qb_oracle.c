@@ -16,7 +16,9 @@
  *                     the excess-form identity of the unit sums; group and
  *                     deliver32 for ActScaling::Sub32 (block_scale,
  *                     quantize, ACT_BLOCK = 32, GROUP = 256 on the
- *                     numerics page).
+ *                     numerics page).  The int8 cache's score path:
+ *                     cache_row, int8_codes, INV_127, quantize_head and
+ *                     int8_score on the numerics page.
  *
  * Readings taken where the pages are silent (each restated where used):
  *   R1  an activation block whose largest magnitude is 0 gets the scale
@@ -37,6 +39,15 @@
  *   R14 (Sub32) SUM_WINDOW never binds here either: a group's terms are
  *       summed exactly, whatever the spread of their exponents (a 384-bit
  *       integer holds every case), then rounded once as in R5.
+ *   R15 (Sub32) a group whose nonzero terms lie 318 or more places above
+ *       the least exponent of its terms is NAN (never for block_scale
+ *       scales with f16 weight scales; only a caller's out-of-range e).
+ *   R17 (int8 cache) the reciprocal under which a cache row's codes are
+ *       taken is the f32 quotient 1/s, correctly rounded (the page's recip
+ *       seeds Newton steps from a table it does not print).
+ *   R18 (int8 cache) a score against a key row whose f16 scale is infinite
+ *       or NaN (a row whose amax*INV_127 overflows binary16) is NAN, as an
+ *       unreadable weight scale is (R7); a query block without a scale too.
  *
  * Build: gcc -O2 -std=c11 -ffp-contract=off -fno-fast-math -shared -fPIC.
  * Contraction must stay off: the f32 rule multiplies and adds separately.
@@ -848,5 +859,138 @@ int or_group_values(int fmt, const uint8_t *W, int64_t rows, int64_t K, const in
                     group_value(&w, g, codes + (int64_t)c * K, am + (int64_t)c * (K / 32), ae + (int64_t)c * (K / 32));
     }
     row_free(&w);
+    return 0;
+}
+
+
+/* =====================================================================
+ * The int8 cache's score path (numerics page: cache_row, int8_codes,
+ * INV_127, quantize_head, int8_score).
+ * ===================================================================== */
+
+/* INV_127 (numerics page): 1/127 as an f32, to nearest (0x3C010204). */
+#define OR_INV_127 (1.0f / 127.0f)
+
+/* ---------------------------------------------------------------------
+ * int8_codes for one element (numerics page, int8_codes): x*inv as an f32
+ * product (operands and result flushed), to the nearest integer with ties to
+ * even, kept within +-127; a NaN product gives 0; an infinite inv (the
+ * reciprocal of a scale that rounded to zero) gives 0.
+ * ------------------------------------------------------------------- */
+int or_int8_code(float x, float inv) {
+    if (isinf(inv)) return 0;
+    float p = or_ftz(or_ftz(x) * inv);
+    if (isnan(p)) return 0;
+    if (p >= 127.0f) return 127;
+    if (p <= -127.0f) return -127;
+    return (int)rintf(p);                /* default rounding: to nearest, ties to even */
+}
+
+/* ---------------------------------------------------------------------
+ * cache_row (numerics page): n rows of d elements, each stored as int8 codes
+ * under one f16 scale.  amax = absmax(row); the scale is
+ * f32_to_f16(amax * INV_127) (an f32 product, flushed); the codes are
+ * int8_codes of the row under the reciprocal of that scale (reading R17);
+ * a scale that rounds to zero gives an infinite reciprocal and all-zero
+ * codes.  codes [n][d], scales (binary16 bits) [n].
+ * ------------------------------------------------------------------- */
+void or_cache_rows(const float *x, int64_t n, int d, int8_t *codes, uint16_t *scales) {
+    for (int64_t r = 0; r < n; r++) {
+        const float *xr = x + r * d;
+        float amax = or_absmax(xr, d);
+        uint16_t h = or_f32_to_f16(or_ftz(amax * OR_INV_127));
+        float s = or_f16_to_f32(h);
+        float inv = 1.0f / s;
+        for (int i = 0; i < d; i++) codes[r * d + i] = (int8_t)or_int8_code(xr[i], inv);
+        scales[r] = h;
+    }
+}
+
+/* ---------------------------------------------------------------------
+ * quantize_head (numerics page): nh query heads of d elements as the array
+ * reads them.  scaling 1 (ActScaling::Sub32): each head padded with zeros to
+ * a whole number of groups, dp = 256*ceil(d/256) elements, quantized per 32
+ * (quantize); codes [nh][dp], scales [nh][dp/32].  scaling 0
+ * (ActScaling::PerBlock): the whole head one block (quantize_blocks with
+ * block = d, wide_scale); codes [nh][d], scales [nh][1].
+ * ------------------------------------------------------------------- */
+int or_quantize_heads(int scaling, const float *q, int nh, int d, int8_t *codes, uint8_t *m, int16_t *e) {
+    if (d <= 0 || d % 16) return -1;
+    if (scaling == 1) {
+        int dp = (d + 255) / 256 * 256;
+        float *buf = (float *)calloc((size_t)dp, sizeof(float));
+        int16_t *s16 = (int16_t *)malloc((size_t)dp / 16 * sizeof(int16_t));
+        if (!buf || !s16) { free(buf); free(s16); return -1; }
+        for (int h = 0; h < nh; h++) {
+            memcpy(buf, q + (int64_t)h * d, (size_t)d * sizeof(float));
+            or_quantize_sub32(buf, dp, 1, codes + (int64_t)h * dp, m + (int64_t)h * (dp / 32),
+                              e + (int64_t)h * (dp / 32), s16);
+        }
+        free(buf);
+        free(s16);
+        return 0;
+    }
+    int16_t *s16 = (int16_t *)malloc((size_t)d / 16 * sizeof(int16_t));
+    if (!s16) return -1;
+    for (int h = 0; h < nh; h++)
+        or_quantize_blocks(q + (int64_t)h * d, d, 1, d, codes + (int64_t)h * d, m + h, e + h, s16);
+    free(s16);
+    return 0;
+}
+
+/* ---------------------------------------------------------------------
+ * int8_score (numerics page): a query head (nb blocks of blk codes with
+ * scales m*2^e; codes past d are padding) against a cached key row (d int8
+ * codes, f16 scale ks): per block, D_b = sum of q_i*k_i; the term
+ * sig(ks) * m_b * D_b at exponent exp(ks) + e_b; the terms summed exactly
+ * and rounded once (exact_sum, reading R5).  NaN for a query block without a
+ * scale or an unreadable key scale (R18).
+ * ------------------------------------------------------------------- */
+float or_int8_score(const int8_t *qc, const uint8_t *m, const int16_t *e, int blk, int nb, int d, const int8_t *kc,
+                    uint16_t ks) {
+    int64_t sg;
+    int ex;
+    if (or_f16_scale(ks, &sg, &ex)) return engine_nan();
+    int64_t *sig = (int64_t *)malloc((size_t)nb * sizeof(int64_t));
+    int *E = (int *)malloc((size_t)nb * sizeof(int));
+    if (!sig || !E) { free(sig); free(E); return engine_nan(); }
+    float r;
+    int bad = 0;
+    for (int b = 0; b < nb; b++) {
+        if (m[b] == 0) { bad = 1; break; }
+        int64_t D = 0;
+        for (int i = b * blk; i < (b + 1) * blk && i < d; i++) D += (int64_t)qc[i] * kc[i];
+        sig[b] = sg * m[b] * D;
+        E[b] = ex + e[b];
+    }
+    r = bad ? engine_nan() : or_exact_sum_f32(sig, E, nb);
+    free(sig);
+    free(E);
+    return r;
+}
+
+/* ---------------------------------------------------------------------
+ * The scores of nh query heads against L cached key rows of nkv key heads
+ * (query head h reads key head h / (nh / nkv)): out[h*L + p] = the f32
+ * product of int8_score and `scale` (flushed), NaN as the engine's.  Query
+ * as or_quantize_heads writes it; key codes [nkv][lcap][d], key scales
+ * [nkv][lcap] (positions 0..L-1 of each head used).
+ * ------------------------------------------------------------------- */
+int or_kv_scores(int scaling, const int8_t *qc, const uint8_t *qm, const int16_t *qe, int nh, int d,
+                 const int8_t *kc, const uint16_t *ks, int64_t L, int64_t lcap, int nkv, float scale, float *out) {
+    if (nkv <= 0 || nh % nkv || d <= 0 || d % 16 || L > lcap) return -1;
+    int dp = scaling == 1 ? (d + 255) / 256 * 256 : d;
+    int blk = scaling == 1 ? 32 : d, nb = dp / blk;
+    for (int h = 0; h < nh; h++) {
+        int kvh = h / (nh / nkv);
+        for (int64_t p = 0; p < L; p++) {
+            int64_t row = (int64_t)kvh * lcap + p;
+            float v = or_int8_score(qc + (int64_t)h * dp, qm + (int64_t)h * nb, qe + (int64_t)h * nb, blk, nb, d,
+                                    kc + row * d, ks[row]);
+            v = or_ftz(v * scale);
+            if (isnan(v)) v = engine_nan();
+            out[(int64_t)h * L + p] = v;
+        }
+    }
     return 0;
 }
