@@ -33,7 +33,9 @@ LIB_PATH = os.path.join(_HERE, "libqgemv.so")
 EXPORTS = ("quantize_act", "q_gemv", "quantize_act_f16", "q_gemv_f16", "q_check_weights", "q_weight_bytes",
            "q_block_values", "q_device_status", "q_strerror", "q_matvec", "q_matvec_workspace_bytes",
            "q_matvec_static", "q_gemv_many", "q_gemv_f16_many", "q_matvec_many", "quantize_act_sub32",
-           "q_gemv_sub32", "q_matvec_sub32_workspace_bytes", "q_matvec_sub32")
+           "q_gemv_sub32", "q_matvec_sub32_workspace_bytes", "q_matvec_sub32", "kv_head_codes", "kv_cache_rows",
+           "kv_quantize_heads", "kv_scores")
+PERBLOCK, SUB32 = 0, 1  # QB_PERBLOCK, QB_SUB32: how a query head is scaled
 
 
 class QbError(RuntimeError):
@@ -83,6 +85,11 @@ def lib() -> ctypes.CDLL:
         L.q_matvec_sub32_workspace_bytes.argtypes, L.q_matvec_sub32_workspace_bytes.restype = [i64, i32], i64
         L.q_matvec_sub32.argtypes = [i32, P, i64, i64, P, i32, P, P, ctypes.c_size_t, P]
         L.q_matvec_sub32.restype = i32
+        L.kv_head_codes.argtypes, L.kv_head_codes.restype = [i32, i32], i32
+        L.kv_cache_rows.argtypes, L.kv_cache_rows.restype = [P, i64, i32, P, P, P], i32
+        L.kv_quantize_heads.argtypes, L.kv_quantize_heads.restype = [i32, P, i32, i32, P, P, P], i32
+        L.kv_scores.argtypes = [i32, P, P, i32, i32, P, P, i64, i64, i32, ctypes.c_float, P, P]
+        L.kv_scores.restype = i32
         _lib = L
     return _lib
 
@@ -159,6 +166,37 @@ def q_matvec_sub32(fmt: int, W, rows: int, K: int, x, out, workspace=None, strea
         workspace = torch.empty(q_matvec_sub32_workspace_bytes(K, ncols), dtype=torch.uint8, device=x.device)
     _check(lib().q_matvec_sub32(fmt, _ptr(W), rows, K, _ptr(x), ncols, _ptr(out), _ptr(workspace),
                                 workspace.numel() * workspace.element_size(), _stream(stream)), "q_matvec_sub32")
+
+
+def kv_head_codes(scaling: int, d: int) -> int:
+    """Codes a quantized query head holds (d rounded up to whole groups under SUB32)."""
+    n = lib().kv_head_codes(scaling, d)
+    if n < 0:
+        raise QbError(n, "kv_head_codes")
+    return n
+
+
+def kv_cache_rows(x, codes, scales, stream=None) -> None:
+    """cache_row of every row of x f32 [n, d] -> codes int8 [n, d], scales (f16 bits) int16/uint16 [n]."""
+    n, d = x.shape
+    _check(lib().kv_cache_rows(_ptr(x), n, d, _ptr(codes), _ptr(scales), _stream(stream)), "kv_cache_rows")
+
+
+def kv_quantize_heads(scaling: int, q, codes, scales, stream=None) -> None:
+    """quantize_head of q f32 [nh, d] -> codes int8 [nh, dp], scales int32 [nh, dp/32] (SUB32) or [nh, 1]."""
+    nh, d = q.shape
+    _check(lib().kv_quantize_heads(scaling, _ptr(q), nh, d, _ptr(codes), _ptr(scales), _stream(stream)),
+           "kv_quantize_heads")
+
+
+def kv_scores(scaling: int, qcodes, qscales, d: int, kcodes, kscales, L: int, scale: float, out,
+              stream=None) -> None:
+    """int8_score of every query head against key rows 0..L-1 of its key head, times scale:
+    out f32 [nh, L].  kcodes int8 [nkv, lcap, d], kscales [nkv, lcap]."""
+    nh = qcodes.shape[0]
+    nkv, lcap = kcodes.shape[0], kcodes.shape[1]
+    _check(lib().kv_scores(scaling, _ptr(qcodes), _ptr(qscales), nh, d, _ptr(kcodes), _ptr(kscales), L, lcap, nkv,
+                           ctypes.c_float(scale), _ptr(out), _stream(stream)), "kv_scores")
 
 
 def _act(block, codes, scales, sums16):

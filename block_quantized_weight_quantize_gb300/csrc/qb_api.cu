@@ -478,6 +478,40 @@ int q_matvec_sub32(qb_fmt fmt, const void *W, int64_t rows, int64_t K, const flo
     return q_gemv_sub32(fmt, W, rows, K, &act, ncols, out, stream);
 }
 
+// ---------------------------------------------------------------- the int8 cache's score path
+
+int kv_head_codes(int scaling, int d) {
+    if ((scaling != QB_PERBLOCK && scaling != QB_SUB32) || d < 16 || d > 1024 || d % 16 != 0) return QB_E_ARG;
+    return scaling == QB_SUB32 ? (d + 255) / 256 * 256 : d;
+}
+
+int kv_cache_rows(const float *x, int64_t n, int d, int8_t *codes, uint16_t *scales, void *stream) {
+    if (!x || !codes || !scales) return QB_E_ARG;
+    if (n < 0 || d < 16 || d > 1024 || d % 16 != 0) return QB_E_ARG;
+    if (misaligned(x) || misaligned(codes) || (reinterpret_cast<uintptr_t>(scales) & 1u)) return QB_E_ARG;
+    if (n == 0) return QB_OK;
+    return launch_kv_cache_rows(x, n, d, codes, scales, static_cast<cudaStream_t>(stream));
+}
+
+int kv_quantize_heads(int scaling, const float *q, int nh, int d, int8_t *codes, qb_scale *scales, void *stream) {
+    if (kv_head_codes(scaling, d) < 0 || !q || !codes || !scales || nh < 1 || nh > 4096) return QB_E_ARG;
+    if (misaligned(q) || misaligned(codes) || (reinterpret_cast<uintptr_t>(scales) & 3u)) return QB_E_ARG;
+    return launch_kv_quantize_heads(scaling, q, nh, d, codes, scales, static_cast<cudaStream_t>(stream));
+}
+
+int kv_scores(int scaling, const int8_t *qcodes, const qb_scale *qscales, int nh, int d, const int8_t *kcodes,
+              const uint16_t *kscales, int64_t L, int64_t lcap, int nkv, float scale, float *out, void *stream) {
+    if (kv_head_codes(scaling, d) < 0) return QB_E_ARG;
+    if (!qcodes || !qscales || !kcodes || !kscales || !out) return QB_E_ARG;
+    if (nh < 1 || nh > 4096 || nkv < 1 || nh % nkv != 0 || L < 0 || lcap < L) return QB_E_ARG;
+    if (misaligned(qcodes) || misaligned(kcodes) || (reinterpret_cast<uintptr_t>(qscales) & 3u) ||
+        (reinterpret_cast<uintptr_t>(kscales) & 1u) || (reinterpret_cast<uintptr_t>(out) & 3u))
+        return QB_E_ARG;
+    if (L == 0) return QB_OK;
+    return launch_kv_scores(scaling, qcodes, qscales, nh, d, kcodes, kscales, L, lcap, nkv, scale, out,
+                            static_cast<cudaStream_t>(stream));
+}
+
 const char *q_strerror(int status) {
     switch (status) {
     case QB_OK: return "ok";

@@ -273,6 +273,51 @@ QB_API int64_t q_matvec_sub32_workspace_bytes(int64_t K, int ncols);
 QB_API int q_matvec_sub32(qb_fmt fmt, const void *W, int64_t rows, int64_t K, const float *x, int ncols,
                           float *out, void *workspace, size_t workspace_bytes, void *stream);
 
+/* ---- The int8 cache's score path (numerics page: cache_row, int8_codes,
+ * INV_127, quantize_head, int8_score). */
+
+/* How a query head is scaled (numerics page, ActScaling): per block of 32
+ * with a 4-bit significand, or the whole head one block with an 8-bit one. */
+#define QB_PERBLOCK 0
+#define QB_SUB32 1
+
+/* Codes a quantized query head holds: d rounded up to a whole number of
+ * 256-element groups under QB_SUB32, d under QB_PERBLOCK (scales: dp/32 a
+ * head, or one); QB_E_ARG unless d % 16 == 0 and 16 <= d <= 1024. */
+QB_API int kv_head_codes(int scaling, int d);
+
+/* cache_row (numerics page) for n rows of d f32 elements x [n][d]: each row's
+ * f16 scale f32_to_f16(amax * INV_127) (amax = absmax, INV_127 = 1/127
+ * rounded to f32, the product an f32 multiply with subnormals flushed),
+ * written as binary16 bits to scales[n], and its codes int8_codes under the
+ * reciprocal of that scale (the correctly rounded f32 1/s): x*inv to the
+ * nearest integer, ties to even, within +-127, NaN products 0, every code 0
+ * when the scale rounded to zero.  codes int8 [n][d].  d % 16 == 0,
+ * 16 <= d <= 1024; x and codes 16-byte aligned. */
+QB_API int kv_cache_rows(const float *x, int64_t n, int d, int8_t *codes, uint16_t *scales, void *stream);
+
+/* quantize_head (numerics page) for nh query heads q f32 [nh][d]:
+ * QB_SUB32 -- each head padded with zeros to dp = kv_head_codes(QB_SUB32, d)
+ * elements and quantized per 32 as quantize_act_sub32 does (codes [nh][dp],
+ * scales [nh][dp/32]); QB_PERBLOCK -- the whole head one block under
+ * wide_scale as quantize_act does (codes [nh][d], scales [nh][1]). */
+QB_API int kv_quantize_heads(int scaling, const float *q, int nh, int d, int8_t *codes, qb_scale *scales,
+                             void *stream);
+
+/* int8_score (numerics page) of nh quantized query heads (as
+ * kv_quantize_heads writes them) against L cached key rows of nkv key heads:
+ * query head h reads key head h / (nh / nkv); key codes int8 [nkv][lcap][d]
+ * and key scales (binary16 bits) [nkv][lcap] as kv_cache_rows writes them,
+ * positions 0..L-1 used.  Per query block b, D_b = sum of q_i*k_i; the terms
+ * sig(ks)*m_b*D_b at exponent exp(ks)+e_b are summed exactly and rounded once
+ * to f32 (as the products above); the score is then multiplied by `scale`
+ * (f32, subnormal results flushed).  out f32 [nh][L].  A key row whose scale
+ * is infinite or NaN, or a query block without a scale, gives the engine's
+ * NaN.  nh % nkv == 0, lcap >= L; codes 16-byte aligned. */
+QB_API int kv_scores(int scaling, const int8_t *qcodes, const qb_scale *qscales, int nh, int d,
+                     const int8_t *kcodes, const uint16_t *kscales, int64_t L, int64_t lcap, int nkv, float scale,
+                     float *out, void *stream);
+
 /* A static string for a status code. */
 QB_API const char *q_strerror(int status);
 
