@@ -68,6 +68,19 @@ GROUPED = {
 }
 
 
+# The int8 cache's score path: query heads quantized, then scored against the
+# cached key rows (kv_quantize_heads + kv_scores a step):
+# name: (scaling, query heads, key heads, head size, cached positions, seed, description)
+KV = {
+    "kv_scores_32k_sub32": (1, 32, 8, 128, 32768, 6,
+                            "int8 key cache scores: 32 query heads on 8 key heads of 128, 32768 positions, "
+                            "query scaled per 32 (Sub32)"),
+    "kv_scores_32k_perblock": (0, 32, 8, 128, 32768, 6,
+                               "int8 key cache scores: 32 query heads on 8 key heads of 128, 32768 positions, "
+                               "query one block a head (PerBlock)"),
+}
+
+
 def kernel_sources_sha() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "block_quantized_weight_quantize_gb300", "csrc")
@@ -179,6 +192,141 @@ def roofline(fmt, ncols, single, achieved, peak, peak_kind, traffic, roof_bytes,
 
 
 # ---------------------------------------------------------------- our arm
+
+def _kv_inputs(scaling, nh, nkv, d, L, seed):
+    rng = np.random.default_rng(seed)
+    q = rng.standard_normal((nh, d)).astype(np.float32)
+    k = rng.standard_normal((nkv * L, d)).astype(np.float32)
+    return q, k
+
+
+def run_kv(args, rank, world):
+    """A step is kv_quantize_heads + kv_scores over the whole key cache; the
+    cache (int8 codes + f16 scales, built by kv_cache_rows) is the streamed input."""
+    import torch
+    import block_quantized_weight_quantize_gb300 as qb
+
+    scaling, nh, nkv, d, L, seed, desc = KV[args.workload]
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    q, k = _kv_inputs(scaling, nh, nkv, d, L, seed + 1000 * rank)
+    kbytes = nkv * L * (d + 2)
+    ncopy = max(2, -(-4 * L2_BYTES // kbytes))
+    kc = torch.empty((ncopy, nkv, L, d), dtype=torch.int8, device=dev)
+    ks = torch.empty((ncopy, nkv, L), dtype=torch.int16, device=dev)
+    kd = torch.from_numpy(k).to(dev)
+    qb.kv_cache_rows(kd, kc[0].view(nkv * L, d), ks[0].view(-1))
+    for i in range(1, ncopy):
+        kc[i].copy_(kc[0])
+        ks[i].copy_(ks[0])
+    del kd
+    qd = torch.from_numpy(q).to(dev)
+    dp = qb.kv_head_codes(scaling, d)
+    nbq = dp // 32 if scaling == qb.SUB32 else 1
+    qc = torch.empty((nh, dp), dtype=torch.int8, device=dev)
+    qs = torch.empty((nh, nbq), dtype=torch.int32, device=dev)
+    out = torch.empty((nh, L), dtype=torch.float32, device=dev)
+    scale = float(1.0 / np.sqrt(d))
+    stream = torch.cuda.Stream(dev)
+
+    def step(i, s):
+        qb.kv_quantize_heads(scaling, qd, qc, qs, stream=s)
+        qb.kv_scores(scaling, qc, qs, d, kc[i % ncopy], ks[i % ncopy], L, scale, out, stream=s)
+
+    def scores_only(i, s):
+        qb.kv_scores(scaling, qc, qs, d, kc[i % ncopy], ks[i % ncopy], L, scale, out, stream=s)
+
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            step(i, stream)
+    stream.synchronize()
+    G = min(args.steps, 200)
+
+    def capture(fn, n):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            g.capture_begin()
+            for i in range(n):
+                fn(i, stream)
+            g.capture_end()
+        return g
+
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    g_main = capture(step, G)
+    g_w = capture(step, max(1, min(args.warmup, G)))
+    with torch.cuda.stream(stream):
+        for _ in range(max(1, args.warmup // max(1, min(args.warmup, G)))):
+            g_w.replay()
+    stream.synchronize()
+    nrep = max(1, args.steps // G)
+    with ClockSampler(dev.index) as clk:
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(nrep):
+                g_main.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / (nrep * G)
+    clocks = clk.summary()
+    g_roof = capture(scores_only, G)
+    with torch.cuda.stream(stream):
+        g_roof.replay()
+        e0.record(stream)
+        for _ in range(3):
+            g_roof.replay()
+        e1.record(stream)
+    stream.synchronize()
+    sc_s = e0.elapsed_time(e1) / 1e3 / (3 * G)
+    roof_bytes = kbytes + nh * (dp + 4 * nbq) + 4 * nh * L
+    peak, peak_kind = measured_peaks()
+    # e2e: the query from pinned host memory, the scores back to pinned host memory
+    qh = torch.from_numpy(q).pin_memory()
+    oh = torch.empty((nh, L), dtype=torch.float32).pin_memory()
+    n_e2e = min(args.steps, 2000)
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for i in range(n_e2e):
+            qd.copy_(qh, non_blocking=True)
+            step(i, stream)
+            oh.copy_(out, non_blocking=True)
+    stream.synchronize()
+    e2e_s = time.perf_counter() - t0
+    assert qb.q_device_status() == qb.QB_OK
+    step_s = ms / 1e3
+    value = world * kbytes / step_s / 1e9
+    res = {
+        "metric": f"key-cache GB/s ({desc})",
+        "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": nrep * G, "warmup": args.warmup,
+        "ms_per_step": round(ms, 6), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "int8 codes x int8 codes (tensor-core s8 MMA), exact int64, f32 rounding",
+        "data": "synthetic (seeded PCG64; N(0,1) keys and queries); no trained weights",
+        "config": {"workload": desc, "query_heads": nh, "key_heads": nkv, "head": d, "positions": L,
+                   "scaling": "Sub32" if scaling == 1 else "PerBlock", "key_bytes_per_step": kbytes,
+                   "l2": f"each step reads a different one of {ncopy} key caches ({ncopy * kbytes / 2**20:.0f} MiB "
+                         f"> 4x L2); no flush",
+                   "timing": f"CUDA graphs of {G} steps (kv_quantize_heads + kv_scores, 2 launches a step); "
+                             f"CUDA events on the launching stream",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "scores_per_s": round(world * nh * L / step_s, 1),
+        "frac_of_8tbs": round(value / 8000.0, 4), "frac_of_measured_copy": round(value / peak, 4),
+        "gpu_launches": 2 * nrep * G, "clocks": clocks,
+        "roofline": {"bound": "hbm", "kernel": f"kv_scores_kernel<{'Sub32' if scaling else 'PerBlock'}, {d // 32} blocks>",
+                     "achieved": round(roof_bytes / sc_s / 1e9, 1), "peak": peak,
+                     "peak_kind": f"{peak_kind} (HBM copy, burst)", "unit": "GB/s",
+                     "frac": round(roof_bytes / sc_s / 1e9 / peak, 4), "traffic": None,
+                     "algorithmic_bytes_per_launch": roof_bytes, "avg_launch_us": round(sc_s * 1e6, 4),
+                     "launches_timed": 3 * G},
+        "e2e": {"value": round(world * kbytes * n_e2e / e2e_s / 1e9, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": int(q.nbytes), "d2h_bytes_per_step": int(4 * nh * L), "steps": n_e2e,
+                "how": "per step: pinned query -> device, kv_quantize_heads + kv_scores through the binding, "
+                       "scores -> pinned host; host wall clock"},
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = kv_cpu_baseline(scaling, nh, nkv, d, L, q, k, kbytes, args.cpu_seconds)
+    return res
+
 
 def run_grouped(args, rank, world):
     """A step is one grouped call over the matrices of GROUPED[workload]; the
@@ -573,6 +721,70 @@ def cpu_baseline(fmt, rows, K, ncols, Wh, x, wbytes, budget_s=10.0, sub32=False)
                       f"threads of the scalar C oracle"}
 
 
+def kv_oracle_pass(scaling, nh, nkv, d, L, q, k, nthreads, pos_limit=None):
+    """cache rows + query heads + scores of (a sample of) positions with the oracle, key heads over threads."""
+    import oracle
+    P = L if pos_limit is None else min(L, pos_limit)
+    qc, m, e = oracle.quantize_heads(scaling, q)
+    G = nh // nkv
+    ex = _pool(nthreads)
+
+    def one(h):
+        kc, ks = oracle.cache_rows(k[h * L:h * L + P])
+        oracle.kv_scores(scaling, qc[h * G:(h + 1) * G], m[h * G:(h + 1) * G], e[h * G:(h + 1) * G], d,
+                         kc.reshape(1, P, d), ks.reshape(1, P), P, 1, 0.125)
+    list(ex.map(one, range(nkv)))
+    return P
+
+
+def kv_cpu_baseline(scaling, nh, nkv, d, L, q, k, kbytes, budget_s=10.0):
+    n = _oracle_threads()
+    t0 = time.perf_counter()
+    kv_oracle_pass(scaling, nh, nkv, d, L, q, k, n, 512)
+    per = (time.perf_counter() - t0) / 512
+    P = int(max(256, min(L, budget_s / 3 / max(per, 1e-9))))
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        kv_oracle_pass(scaling, nh, nkv, d, L, q, k, n, P)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    value = kbytes * (P / L) * reps / el / 1e9
+    return {"value": round(value, 4), "unit": "GB/s", "cores": n, "kind": "oracle",
+            "sample": f"{reps} passes over {P} of {L} positions of every key head (cache rows, query heads, "
+                      f"scores) in {el:.1f} s, key heads over {n} threads of the scalar C oracle"}
+
+
+def run_kv_reference(args):
+    scaling, nh, nkv, d, L, seed, desc = KV[args.workload]
+    q, k = _kv_inputs(scaling, nh, nkv, d, L, seed)
+    n = _oracle_threads()
+    kbytes = nkv * L * (d + 2)
+    t0 = time.perf_counter()
+    kv_oracle_pass(scaling, nh, nkv, d, L, q, k, n, 1024)
+    per = (time.perf_counter() - t0) / 1024
+    budget = 100.0 / max(1, args.steps + args.warmup)
+    P = int(max(64, min(L, budget / max(per, 1e-9))))
+    for _ in range(args.warmup):
+        kv_oracle_pass(scaling, nh, nkv, d, L, q, k, n, P)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        kv_oracle_pass(scaling, nh, nkv, d, L, q, k, n, P)
+    el = time.perf_counter() - t0
+    value = kbytes * (P / L) * args.steps / el / 1e9
+    sample = f"each step: cache rows, query heads and scores of {P} of {L} positions, key heads over {n} threads"
+    return {
+        "impl": "reference", "metric": f"key-cache GB/s ({desc})", "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": 0, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el * 1e3 / args.steps, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "int64 exact, f32 rounding (scalar C)", "data": "synthetic (seeded PCG64)",
+        "config": {"workload": desc, "query_heads": nh, "key_heads": nkv, "head": d, "positions": L},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": n, "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
 def run_reference(args):
     fmt, rows, K, ncols, seed, outl, desc = WORKLOADS[args.workload]
     sub32 = args.workload in SUB32
@@ -615,7 +827,7 @@ def main():
     ap.add_argument("--steps", type=int, default=100000)
     ap.add_argument("--warmup", type=int, default=1000)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="q4k_4096x4096", choices=sorted(WORKLOADS) + sorted(GROUPED))
+    ap.add_argument("--workload", default="q4k_4096x4096", choices=sorted(WORKLOADS) + sorted(GROUPED) + sorted(KV))
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--roof-launches", type=int, default=2000,
@@ -629,6 +841,8 @@ def main():
             if args.workload in GROUPED:
                 print(json.dumps({"impl": "reference", "unavailable": "the reference arm times single-matrix "
                                   "workloads; the grouped workload has no oracle timing"}), flush=True)
+            elif args.workload in KV:
+                print(json.dumps(run_kv_reference(args)), flush=True)
             else:
                 print(json.dumps(run_reference(args)), flush=True)
         return
@@ -637,7 +851,8 @@ def main():
         import torch.distributed as tdist
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
         tdist.init_process_group("nccl")
-    res = run_grouped(args, rank, world) if args.workload in GROUPED else run_ours(args, rank, world)
+    res = (run_grouped(args, rank, world) if args.workload in GROUPED else
+           run_kv(args, rank, world) if args.workload in KV else run_ours(args, rank, world))
     if rank == 0:
         print(json.dumps(res), flush=True)
     if world > 1:

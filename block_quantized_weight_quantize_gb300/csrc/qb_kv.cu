@@ -199,13 +199,35 @@ __device__ __forceinline__ float finish_score(float v, float scale) {
     return (v != v) ? __uint_as_float(kEngineNaN) : v;
 }
 
+__device__ __forceinline__ void cp_async16(void *dst, const void *src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+template <int NB>
+constexpr int kv_ring_depth() { return NB >= 8 ? 2 : 4; }
+// Shared memory of a score CTA: the head table, then each warp's ring of
+// tiles (16 rows at a pitch of d + 32 bytes, so that the fragment reads of a
+// half warp -- 4 rows x 4 eight-byte slots -- fall in 16 distinct bank pairs).
+template <int NB>
+__host__ __device__ inline int kv_smem_bytes(int nh) {
+    return ((nh * (2 + NB) * 4 + 15) & ~15) + 8 * kv_ring_depth<NB>() * 16 * (32 * NB + 32);
+}
+
 // Per query head, in shared memory: [mode, emin, M_0 .. M_{NB-1}] (mode 0
-// fast, 1 exact routine, 2 NaN).  Warps take tiles of 16 key rows x 8 query
-// heads (of one key head); NB = d / 32 blocks a key row.
+// fast, 1 exact routine, 2 NaN).  Tiles are 16 key rows x 8 query heads (of
+// one key head), ordered key head, head chunk, row tile; each warp takes a
+// contiguous range of them (consecutive tiles are consecutive 16*d bytes of
+// the cache) and streams them through its own ring of asynchronous copies,
+// several tiles ahead; the query fragments and multipliers stay in registers
+// while the key head and chunk are the same.  NB = d / 32 blocks a key row.
 template <bool S32, int NB>
-__global__ void __launch_bounds__(256) kv_scores_kernel(const KvK p) {
-    extern __shared__ int hsm[];
-    constexpr int kW = 2 + NB;
+__global__ void __launch_bounds__(256, 2) kv_scores_kernel(const KvK p) {
+    extern __shared__ __align__(16) int hsm[];
+    constexpr int kW = 2 + NB, kD = kv_ring_depth<NB>(), kPitch = 32 * NB + 32, kTile = 16 * kPitch;
     pdl_launch_dependents();
     pdl_wait();
     for (int h = threadIdx.x; h < p.nh; h += blockDim.x) {
@@ -241,77 +263,177 @@ __global__ void __launch_bounds__(256) kv_scores_kernel(const KvK p) {
     }
     __syncthreads();
 
-    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-    const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
-    for (int64_t tile = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); tile < p.ntiles;
-         tile += nwarps) {
-        const int chunk = (int)(tile % p.nchunk);
-        const int64_t rest = tile / p.nchunk;
-        const int64_t rt = rest % p.ntr;
-        const int kvh = (int)(rest / p.ntr);
-        const int64_t p0 = rt * 16 + g, p1 = p0 + 8;
-        const int8_t *k0 = p.kc + ((int64_t)kvh * p.lcap + p0) * p.d;
-        const int8_t *k1 = k0 + (int64_t)8 * p.d;
-        // A: rows p0 and p1, bytes [32b + 8t, 32b + 8t + 8) of every block
-        uint2 A0[NB], A1[NB];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    uint8_t *ring = reinterpret_cast<uint8_t *>(hsm) + ((p.nh * kW * 4 + 15) & ~15) + warp * kD * kTile;
+    const int64_t nw = (int64_t)gridDim.x * (blockDim.x >> 5);
+    const int64_t wid = (int64_t)blockIdx.x * (blockDim.x >> 5) + warp;
+    const int64_t t_begin = wid * p.ntiles / nw, t_end = (wid + 1) * p.ntiles / nw;
+    if (t_begin >= t_end) return;
+    const int ntr = (int)p.ntr;
+
+    // this lane's copies within a tile: chunk ci = lane + 32q is row ci / (2NB),
+    // 16-byte column ci % (2NB)
+    int crow[NB], csrc[NB], cdst[NB];
 #pragma unroll
-        for (int b = 0; b < NB; ++b) {
-            A0[b] = p0 < p.L ? __ldg(reinterpret_cast<const uint2 *>(k0 + 32 * b + 8 * t)) : make_uint2(0, 0);
-            A1[b] = p1 < p.L ? __ldg(reinterpret_cast<const uint2 *>(k1 + 32 * b + 8 * t)) : make_uint2(0, 0);
+    for (int q = 0; q < NB; ++q) {
+        const int ci = lane + 32 * q, r = ci / (2 * NB), c = ci % (2 * NB);
+        crow[q] = r;
+        csrc[q] = r * p.d + 16 * c;
+        cdst[q] = r * kPitch + 16 * c;
+    }
+    // tile coordinates, advanced without division: key head, head chunk, row tile
+    struct Pos { int kvh, chunk, rt; };
+    auto advance = [&](Pos &x) {
+        if (++x.rt == ntr) {
+            x.rt = 0;
+            if (++x.chunk == p.nchunk) { x.chunk = 0; ++x.kvh; }
         }
-        // B: query head hb = column g of this chunk, the same bytes
-        const int jb = chunk * 8 + g;
-        const bool bin = jb < p.G;
-        const int8_t *qb = p.qc + (int64_t)(kvh * p.G + (bin ? jb : 0)) * p.dp;
-        // this thread's output heads: columns 2t, 2t+1 of the chunk
-        const int j0 = chunk * 8 + 2 * t, j1 = j0 + 1;
-        const int h0 = kvh * p.G + j0, h1 = h0 + 1;
-        const int *w0 = hsm + (j0 < p.G ? h0 : 0) * kW, *w1 = hsm + (j1 < p.G ? h1 : 0) * kW;
+    };
+    Pos cur;
+    {
+        const int64_t kc0 = t_begin / ntr;
+        cur.rt = (int)(t_begin - kc0 * ntr);
+        cur.kvh = (int)(kc0 / p.nchunk);
+        cur.chunk = (int)(kc0 - (int64_t)cur.kvh * p.nchunk);
+    }
+    // the copies kD tiles ahead: one commit group per call, empty past the range
+    Pos ip = cur;
+    int64_t itile = t_begin;
+    int islot = 0;
+    auto issue = [&]() {
+        if (itile < t_end) {
+            uint8_t *dst = ring + islot * kTile;
+            const int64_t left = p.L - (int64_t)ip.rt * 16;
+            const int rows_left = left < 16 ? (int)left : 16;
+            const int8_t *src = p.kc + ((int64_t)ip.kvh * p.lcap + (int64_t)ip.rt * 16) * p.d;
+#pragma unroll
+            for (int q = 0; q < NB; ++q) {
+                const bool ok = crow[q] < rows_left;
+                cp_async16(dst + cdst[q], ok ? src + csrc[q] : src, ok ? 16u : 0u);
+            }
+            advance(ip);
+        }
+        cp_async_commit();
+        ++itile;
+        islot = (islot + 1 == kD) ? 0 : islot + 1;
+    };
+#pragma unroll
+    for (int i = 0; i < kD; ++i) issue();
+
+    // key scales of a tile's rows g and g + 8 (0 past L; never read there)
+    auto ks_load = [&](const Pos &x, uint32_t &a, uint32_t &b) {
+        const int64_t r = (int64_t)x.rt * 16 + g;
+        const uint16_t *base = p.ks + (int64_t)x.kvh * p.lcap + r;
+        a = r < p.L ? __ldg(base) : 0u;
+        b = r + 8 < p.L ? __ldg(base + 8) : 0u;
+    };
+    uint32_t ks0, ks1;
+    ks_load(cur, ks0, ks1);
+
+    int held = -1;  // key head * nchunk + chunk of the fragments held
+    uint2 B[NB];
+    int M0[NB], M1[NB];
+    int mode0 = 0, mode1 = 0, emin0 = 0, emin1 = 0, h0 = 0;
+    bool hv0 = false, hv1 = false;
+    float *out0 = p.out, *out1 = p.out;
+    int slot = 0;
+    for (int64_t tile = t_begin; tile < t_end; ++tile) {
+        Pos nxt = cur;
+        advance(nxt);
+        uint32_t kn0 = 0, kn1 = 0;
+        if (tile + 1 < t_end) ks_load(nxt, kn0, kn1);  // early: used one tile later
+        const int kc_ = cur.kvh * p.nchunk + cur.chunk;
+        if (kc_ != held) {
+            held = kc_;
+            const int jb = cur.chunk * 8 + g;
+            const bool bin = jb < p.G;
+            const int8_t *qb = p.qc + (int64_t)(cur.kvh * p.G + (bin ? jb : 0)) * p.dp + 8 * t;
+#pragma unroll
+            for (int b = 0; b < NB; ++b)
+                B[b] = bin ? __ldg(reinterpret_cast<const uint2 *>(qb + 32 * b)) : make_uint2(0, 0);
+            const int j0 = cur.chunk * 8 + 2 * t;
+            hv0 = j0 < p.G;
+            hv1 = j0 + 1 < p.G;
+            h0 = cur.kvh * p.G + j0;
+            const int *w0 = hsm + (hv0 ? h0 : 0) * kW, *w1 = hsm + (hv1 ? h0 + 1 : 0) * kW;
+            mode0 = w0[0]; emin0 = w0[1];
+            mode1 = w1[0]; emin1 = w1[1];
+#pragma unroll
+            for (int b = 0; b < NB; ++b) { M0[b] = w0[2 + b]; M1[b] = w1[2 + b]; }
+            out0 = p.out + (int64_t)h0 * p.L;
+            out1 = out0 + p.L;
+        }
+        cp_async_wait<kD - 1>();  // this tile's group has landed (this lane's copies)
+        __syncwarp();             // ... and every lane's
+        const uint8_t *sl = ring + slot * kTile;
         long long acc[4] = {0, 0, 0, 0};
         int c[4] = {0, 0, 0, 0};
 #pragma unroll
         for (int b = 0; b < NB; ++b) {
-            const uint2 B = bin ? __ldg(reinterpret_cast<const uint2 *>(qb + 32 * b + 8 * t)) : make_uint2(0, 0);
+            const uint2 a0 = *reinterpret_cast<const uint2 *>(sl + g * kPitch + 32 * b + 8 * t);
+            const uint2 a1 = *reinterpret_cast<const uint2 *>(sl + (g + 8) * kPitch + 32 * b + 8 * t);
             if (S32) { c[0] = c[1] = c[2] = c[3] = 0; }
-            mma_s8_16832(c, A0[b].x, A1[b].x, A0[b].y, A1[b].y, B.x, B.y);
+            mma_s8_16832(c, a0.x, a1.x, a0.y, a1.y, B[b].x, B[b].y);
             if (S32) {
-                const long long M0 = w0[2 + b], M1 = w1[2 + b];
-                acc[0] += M0 * c[0];
-                acc[1] += M1 * c[1];
-                acc[2] += M0 * c[2];
-                acc[3] += M1 * c[3];
+                acc[0] += (long long)M0[b] * c[0];
+                acc[1] += (long long)M1[b] * c[1];
+                acc[2] += (long long)M0[b] * c[2];
+                acc[3] += (long long)M1[b] * c[3];
             }
         }
+        __syncwarp();  // every lane has read the slot
+        issue();       // refill it kD tiles ahead
+        slot = (slot + 1 == kD) ? 0 : slot + 1;
         if (!S32) {
-            acc[0] = (long long)w0[2] * c[0];
-            acc[1] = (long long)w1[2] * c[1];
-            acc[2] = (long long)w0[2] * c[2];
-            acc[3] = (long long)w1[2] * c[3];
+            acc[0] = (long long)M0[0] * c[0];
+            acc[1] = (long long)M1[0] * c[1];
+            acc[2] = (long long)M0[0] * c[2];
+            acc[3] = (long long)M1[0] * c[3];
         }
-        // epilogue: (row, head) pairs (p0, h0) (p0, h1) (p1, h0) (p1, h1)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int64_t pr = (i < 2) ? p0 : p1;
-            const int j = (i & 1) ? j1 : j0;
-            if (pr >= p.L || j >= p.G) continue;
-            const int h = kvh * p.G + j;
-            const int *w = (i & 1) ? w1 : w0;
-            const int64_t krow = (int64_t)kvh * p.lcap + pr;
-            const uint32_t ksb = __ldg(p.ks + krow);
-            float v;
-            if (w[0] == 2) {
-                v = __uint_as_float(kEngineNaN);
-            } else if (w[0] == 1) {
-                v = kv_score_exact(p.qc + (int64_t)h * p.dp, p.qs + (int64_t)h * p.nbq, p.nbq, S32 ? 32 : p.d, p.d,
-                                   p.kc + krow * p.d, ksb);
-            } else {
-                int sg, ex;
-                v = f16_scale(ksb, sg, ex) ? round_fast((long long)sg * acc[i], ex + w[1])
-                                           : __uint_as_float(kEngineNaN);
+        // epilogue: (row, head) pairs (pA, h0) (pA, h0+1) (pB, h0) (pB, h0+1)
+        const int64_t pA = (int64_t)cur.rt * 16 + g, pB = pA + 8;
+        const bool rA = pA < p.L, rB = pB < p.L;
+        int sgA, exA, sgB, exB;
+        const bool okA = f16_scale(ks0, sgA, exA), okB = f16_scale(ks1, sgB, exB);
+        if ((mode0 | mode1) == 0 && okA && okB) {
+            if (rA) {
+                if (hv0) out0[pA] = finish_score(round_fast((long long)sgA * acc[0], exA + emin0), p.scale);
+                if (hv1) out1[pA] = finish_score(round_fast((long long)sgA * acc[1], exA + emin1), p.scale);
             }
-            p.out[(int64_t)h * p.L + pr] = finish_score(v, p.scale);
+            if (rB) {
+                if (hv0) out0[pB] = finish_score(round_fast((long long)sgB * acc[2], exB + emin0), p.scale);
+                if (hv1) out1[pB] = finish_score(round_fast((long long)sgB * acc[3], exB + emin1), p.scale);
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const bool rowok = (i < 2) ? rA : rB;
+                const bool hok = (i & 1) ? hv1 : hv0;
+                if (!rowok || !hok) continue;
+                const int64_t pr = (i < 2) ? pA : pB;
+                const int h = h0 + (i & 1);
+                const int mode = (i & 1) ? mode1 : mode0;
+                const uint32_t ksb = (i < 2) ? ks0 : ks1;
+                float v;
+                if (mode == 2) {
+                    v = __uint_as_float(kEngineNaN);
+                } else if (mode == 1) {
+                    v = kv_score_exact(p.qc + (int64_t)h * p.dp, p.qs + (int64_t)h * p.nbq, p.nbq, S32 ? 32 : p.d,
+                                       p.d, p.kc + ((int64_t)cur.kvh * p.lcap + pr) * p.d, ksb);
+                } else {
+                    const bool ok = (i < 2) ? okA : okB;
+                    v = ok ? round_fast((long long)((i < 2) ? sgA : sgB) * acc[i],
+                                        ((i < 2) ? exA : exB) + ((i & 1) ? emin1 : emin0))
+                           : __uint_as_float(kEngineNaN);
+                }
+                ((i & 1) ? out1 : out0)[pr] = finish_score(v, p.scale);
+            }
         }
+        cur = nxt;
+        ks0 = kn0;
+        ks1 = kn1;
     }
+    cp_async_wait<0>();  // no copy outlives the warp
 }
 
 // Any d (% 16 == 0, <= 1024): one thread per score through the exact routine.
@@ -349,11 +471,19 @@ int launch_kv_quantize_heads(int scaling, const float *q, int nh, int d, int8_t 
 
 template <bool S32, int NB>
 static int launch_scores_nb(const KvK &k, cudaStream_t stream) {
-    const size_t smem = (size_t)k.nh * (2 + NB) * sizeof(int);
-    if (smem > 48 * 1024) return QB_E_ARG;
+    const int smem = kv_smem_bytes<NB>(k.nh);
+    if (smem > 113 * 1024) return QB_E_ARG;
+    static bool attr_set = false;
+    if (!attr_set) {
+        if (cudaFuncSetAttribute(kv_scores_kernel<S32, NB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 113 * 1024) != cudaSuccess)
+            return QB_E_CUDA;
+        attr_set = true;
+    }
+    // persistent: two CTAs of 8 warps a SM, each warp a contiguous range of tiles
     const int64_t blocks = (k.ntiles + 7) / 8;
-    const unsigned grid = (unsigned)std::max<int64_t>(1, std::min<int64_t>(blocks, (int64_t)num_sms() * 8));
-    return launch_pdl(kv_scores_kernel<S32, NB>, dim3(grid), dim3(256), smem, stream, k);
+    const unsigned grid = (unsigned)std::max<int64_t>(1, std::min<int64_t>(blocks, (int64_t)num_sms() * 2));
+    return launch_pdl(kv_scores_kernel<S32, NB>, dim3(grid), dim3(256), (size_t)smem, stream, k);
 }
 
 int launch_kv_scores(int scaling, const int8_t *qc, const qb_scale *qs, int nh, int d, const int8_t *kc,
