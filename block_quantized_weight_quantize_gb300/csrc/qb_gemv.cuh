@@ -373,6 +373,10 @@ int dispatch_hi(int nc, const GemvK &k, int threads, int smem, unsigned grid, cu
 // qb_skinny_*.cu); QB_E_ARG when it does not apply to the shape.
 template <int F>
 int launch_skinny(const GemvArgs &a, cudaStream_t stream);
+// One column through the multi-column kernel's organisation where it is the
+// faster one (qb_gemv3.cuh, launch_gemv3_one); QB_E_ARG where it does not apply.
+template <int F>
+int launch_one_col3(const GemvArgs &a, cudaStream_t stream, const float *x);
 
 inline int gcd_int(int a, int b) { while (b) { int t = a % b; a = b; b = t; } return a; }
 
@@ -382,8 +386,10 @@ inline int gcd_int(int a, int b) { while (b) { int t = a % b; a = b; b = t; } re
 template <int F>
 int launch_gemv_fmt(const GemvArgs &a, cudaStream_t stream) {
     constexpr int blk = fmt_block(F);
-    if (a.mode == 0 && a.ncols == 1) {  // the streaming kernel, where it applies
-        const int rc = launch_gemv2<F>(a, stream);
+    if (a.mode == 0 && a.ncols == 1) {  // the streaming kernels, where they apply
+        int rc = launch_one_col3<F>(a, stream, nullptr);
+        if (rc != QB_E_ARG) return rc;
+        rc = launch_gemv2<F>(a, stream);
         if (rc != QB_E_ARG) return rc;
     }
     if (a.mode == 0 && a.ncols >= 2) {

@@ -48,6 +48,7 @@ struct Gemv3K {
     const int8_t *codes;  // column 0 of this launch
     const qb_scale *scales;
     const int16_t *sums16;
+    const float *x;  // one-column single-launch form: the f32 activation, quantized in the kernel
     int *fault;
 };
 // A launch over several matrices sharing the activation: the table, outputs
@@ -57,17 +58,20 @@ struct Gemv3KM : Gemv3K {
 };
 
 struct Gemv3Smem {
-    int bars, act, val, ring, total;
+    int bars, act, sums, scl, val, ring, total;
 };
 
-// act: the launch's activation codes (ncols * K bytes); val: the block values
-// of H iterations; ring: D slots of 2*nt weight rows.
+// act: the launch's activation codes (ncols * K bytes); sums, scl: the unit
+// sums and scales the single-launch form quantizes into (fused only); val:
+// the block values of H iterations; ring: D slots of 2*nt weight rows.
 __host__ __device__ inline Gemv3Smem gemv3_smem(int K, int ncols, int rec, int nt, int ncp, int D, int H,
-                                                int vstride) {
+                                                int vstride, bool fused = false) {
     Gemv3Smem s;
     s.bars = 0;
     s.act = 128;
-    s.val = s.act + ((ncols * K + 127) & ~127);
+    s.sums = s.act + ((ncols * K + 127) & ~127);
+    s.scl = s.sums + (fused ? ((K / 16 * 2 + 127) & ~127) : 0);
+    s.val = s.scl + (fused ? ((K / 32 * 4 + 127) & ~127) : 0);
     s.ring = s.val + ((H * nt * 2 * ncp * vstride * 4 + 127) & ~127);
     s.total = s.ring + D * nt * 2 * rec;
     return s;
@@ -187,14 +191,20 @@ __device__ __forceinline__ void half_q8_0_cg(const uint8_t *q, const uint8_t *dp
 template <int CG>
 constexpr int gemv3_threads() { return CG >= 4 ? 256 : 512; }
 
-template <int F, int CG, bool MULTI>
+// FUSED (one column, CG = 1): the f32 activation p.x is quantized in the
+// prologue (quantize_blocks, as the one-column kernel's single-launch form
+// does) while the first weight fills are in flight.
+template <int F, int CG, bool MULTI, bool FUSED = false>
 __global__ void __launch_bounds__(gemv3_threads<CG>(), 1)
     gemv3_kernel(const typename std::conditional<MULTI, Gemv3KM, Gemv3K>::type p) {
+    static_assert(!FUSED || CG == 1, "the single-launch form takes one column");
     extern __shared__ __align__(128) uint8_t smem[];
     const int ncp = p.ncg * CG;  // padded columns
-    const Gemv3Smem L = gemv3_smem(p.K, p.ncols, p.rec, p.nt, ncp, p.D, p.H, p.vstride);
+    const Gemv3Smem L = gemv3_smem(p.K, p.ncols, p.rec, p.nt, ncp, p.D, p.H, p.vstride, FUSED);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L.bars);
     uint8_t *act = smem + L.act;
+    int16_t *asum = reinterpret_cast<int16_t *>(smem + L.sums);
+    uint32_t *ascl = reinterpret_cast<uint32_t *>(smem + L.scl);
     float *val = reinterpret_cast<float *>(smem + L.val);
     uint8_t *ring = smem + L.ring;
 
@@ -233,8 +243,43 @@ __global__ void __launch_bounds__(gemv3_threads<CG>(), 1)
     // ---- the activation codes of every column, once per CTA: coalesced
     // loads, stored in shared memory with 16-B unit u of the launch's codes at
     // (u & ~7) | ((u & 7) ^ ((u >> 3) & 7)) (Q8_0: at u), so that the register
-    // loads below hit eight banks per phase
-    {
+    // loads below hit eight banks per phase.  The single-launch form quantizes
+    // x here instead: a thread takes 8 consecutive elements, a block of B
+    // elements is B/8 consecutive lanes; all loads first, then the quantizer.
+    if constexpr (FUSED) {
+        constexpr int kB = fmt_block(F), kL = kB / 8, kMaxG = 4;  // groups per thread: K/8 <= 4 * blockDim
+        const int G = p.K / 8;
+        float4 xv[2 * kMaxG];
+#pragma unroll
+        for (int r = 0; r < kMaxG; ++r) {
+            const int g8 = tid + r * (int)blockDim.x;
+            const bool in = g8 < G;
+            xv[2 * r] = in ? ldg_f4_ordered(reinterpret_cast<const float4 *>(p.x) + 2 * g8) : make_float4(0, 0, 0, 0);
+            xv[2 * r + 1] = in ? ldg_f4_ordered(reinterpret_cast<const float4 *>(p.x) + 2 * g8 + 1)
+                               : make_float4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int r = 0; r < kMaxG; ++r) {
+            if (r * (int)blockDim.x >= G) break;  // uniform: whole warps are in or out (G % 32 == 0)
+            const int g8 = tid + r * (int)blockDim.x;
+            const uint32_t xb[8] = {__float_as_uint(xv[2 * r].x), __float_as_uint(xv[2 * r].y),
+                                    __float_as_uint(xv[2 * r].z), __float_as_uint(xv[2 * r].w),
+                                    __float_as_uint(xv[2 * r + 1].x), __float_as_uint(xv[2 * r + 1].y),
+                                    __float_as_uint(xv[2 * r + 1].z), __float_as_uint(xv[2 * r + 1].w)};
+            uint2 c;
+            int usum;
+            uint32_t scale;
+            quantize8<kL>(xb, c, usum, scale);
+            if (g8 < G) {
+                const int u = g8 >> 1;
+                const int pos = (F == kQ8_0) ? u : ((u & ~7) | ((u & 7) ^ ((u >> 3) & 7)));
+                *reinterpret_cast<uint2 *>(act + 16 * pos + 8 * (g8 & 1)) = c;
+                if ((g8 & 1) == 0) asum[u] = (int16_t)usum;
+                if ((g8 & (kL - 1)) == 0) ascl[g8 / kL] = scale;
+            }
+        }
+        __syncthreads();
+    } else {
         const int nu = p.ncols * (p.K / 16);
         const uint4 *src = reinterpret_cast<const uint4 *>(p.codes);
         constexpr int kU = 4;
@@ -253,7 +298,8 @@ __global__ void __launch_bounds__(gemv3_threads<CG>(), 1)
             }
         }
     }
-    // my columns' unit sums and scales (global memory; small)
+    // my columns' unit sums and scales (global memory, small; the single-launch
+    // form's own, in shared memory)
     uint4 a[CG][8];
     uint32_t S[CG][4];
     uint4 scl[CG];  // Q8_0: the scales of blocks 4j..4j+3
@@ -267,9 +313,11 @@ __global__ void __launch_bounds__(gemv3_threads<CG>(), 1)
         m0[c] = 128;
         e0[c] = 0;
         if (in && F == kQ8_0) {
-            scl[c] = __ldg(reinterpret_cast<const uint4 *>(p.scales + (int64_t)col * (p.K / 32)) + j);
+            scl[c] = FUSED ? *reinterpret_cast<const uint4 *>(ascl + 4 * j)
+                           : __ldg(reinterpret_cast<const uint4 *>(p.scales + (int64_t)col * (p.K / 32)) + j);
         } else if (in) {
-            const uint4 sw = __ldg(reinterpret_cast<const uint4 *>(p.sums16 + (int64_t)col * (p.K / 16)) + j);
+            const uint4 sw = FUSED ? *reinterpret_cast<const uint4 *>(asum + 8 * j)
+                                   : __ldg(reinterpret_cast<const uint4 *>(p.sums16 + (int64_t)col * (p.K / 16)) + j);
             const uint32_t pw[4] = {sw.x, sw.y, sw.z, sw.w};
             if (F == kQ4K) {  // per-32 sums of my four sub-blocks from the per-16 ones
 #pragma unroll
@@ -280,7 +328,8 @@ __global__ void __launch_bounds__(gemv3_threads<CG>(), 1)
             } else {
                 S[c][0] = pw[0]; S[c][1] = pw[1]; S[c][2] = pw[2]; S[c][3] = pw[3];
             }
-            const uint32_t sv = __ldg(reinterpret_cast<const uint32_t *>(p.scales) + (int64_t)col * (p.K / 256) + sb);
+            const uint32_t sv = FUSED ? ascl[sb]
+                                      : __ldg(reinterpret_cast<const uint32_t *>(p.scales) + (int64_t)col * (p.K / 256) + sb);
             m0[c] = (int)(sv & 0xFFu);
             e0[c] = (int)(int16_t)(sv >> 16);
         }
@@ -380,8 +429,11 @@ __global__ void __launch_bounds__(gemv3_threads<CG>(), 1)
 }
 
 // The shape of one launch over `ncols` columns; false when it does not fit.
+// fused: the one-column single-launch form (its quantizer holds at most four
+// 8-element groups a thread, so at least K/32 threads).
 template <int F, int CG>
-bool gemv3_shape(int64_t rows, int64_t K, int ncols, Gemv3K &k, int &grid, int &threads, int &smem) {
+bool gemv3_shape(int64_t rows, int64_t K, int ncols, Gemv3K &k, int &grid, int &threads, int &smem,
+                 bool fused = false) {
     constexpr int kThreads = gemv3_threads<CG>();
     const int ts = (int)(K / 128);
     const int ncg = (ncols + CG - 1) / CG, ncp = ncg * CG;
@@ -399,19 +451,71 @@ bool gemv3_shape(int64_t rows, int64_t K, int ncols, Gemv3K &k, int &grid, int &
     const int64_t rpc = (rows + grid - 1) / grid;  // most rows any CTA owns
     const int budget = 225 * 1024;
     k.nt = (int)std::min<int64_t>(kThreads / tpt, std::max<int64_t>(1, (rpc + 1) / 2));
+    if (fused) k.nt = std::max(k.nt, std::min(4, kThreads / tpt));
+    auto L = [&](int D, int H) { return gemv3_smem(k.K, ncols, k.rec, k.nt, ncp, D, H, k.vstride, fused).total; };
     // room for two ring slots and one history step
-    while (k.nt > 1 && gemv3_smem(k.K, ncols, k.rec, k.nt, ncp, 2, 1, k.vstride).total > budget) --k.nt;
-    if (gemv3_smem(k.K, ncols, k.rec, k.nt, ncp, 1, 1, k.vstride).total > budget) return false;
+    while (k.nt > 1 && L(2, 1) > budget) --k.nt;
+    if (L(1, 1) > budget) return false;
     k.n_iter = (int)((rpc + 2LL * k.nt - 1) / (2LL * k.nt));
     k.base = rows / grid;
     k.rem = rows % grid;
     threads = (k.nt * tpt + 31) / 32 * 32;
+    if (fused && K / 8 > 4 * threads) return false;
     k.H = std::max(1, std::min({k.n_iter, 8, threads / (k.nt * 2 * ncp)}));  // about one fold line a thread
-    const int hist = gemv3_smem(k.K, ncols, k.rec, k.nt, ncp, 0, k.H, k.vstride).total;
+    const int hist = L(0, k.H);
     k.D = std::max(1, std::min({k.n_iter, 4, (budget - hist) / (2 * k.nt * k.rec)}));
-    while (gemv3_smem(k.K, ncols, k.rec, k.nt, ncp, k.D, k.H, k.vstride).total > budget && k.H > 1) --k.H;
-    smem = gemv3_smem(k.K, ncols, k.rec, k.nt, ncp, k.D, k.H, k.vstride).total;
+    while (L(k.D, k.H) > budget && k.H > 1) --k.H;
+    smem = L(k.D, k.H);
     return smem <= 227 * 1024;
+}
+
+// One column in groups of one (CG = 1), the activation quantized beforehand
+// or, with x, in the prologue (one launch).  Taken for the 256-element
+// formats where the one-column kernel (qb_gemv2.cuh) would need more than one
+// ring iteration per CTA -- there this organisation measured faster (Q6_K-like
+// 14336x4096: 9.46 against 11.5 us; Q4_K-like 14336x4096: 8.0 against 8.3);
+// QB_E_ARG otherwise, or when the shape does not fit.
+template <int F>
+int launch_gemv3_one(const GemvArgs &a, cudaStream_t stream, const float *x) {
+    if (F == kQ8_0 || a.ncols != 1 || a.mode != 0 || a.K % 256 != 0) return QB_E_ARG;
+    const MatTable mt = a.mats ? *a.mats : single_table(a.W, a.rows, a.out);
+    const int64_t rows = mt.start[mt.n];
+    const int ts = (int)(a.K / 128);
+    if (rows < 1 || ts > 512) return QB_E_ARG;
+    const int64_t g1 = std::max<int64_t>(1, std::min<int64_t>(num_sms(), rows));
+    if (((rows + g1 - 1) / g1 + 1) / 2 <= 512 / ts) return QB_E_ARG;  // one iteration: the one-column kernel
+    Gemv3KM k;
+    int grid, threads, smem;
+    const bool fused = x != nullptr;
+    if (!gemv3_shape<F, 1>(rows, a.K, 1, k, grid, threads, smem, fused)) return QB_E_ARG;
+    int *fault = fault_word();
+    if (!fault) return QB_E_CUDA;
+    k.mt = mt;
+    k.W = mt.W[0];
+    k.out = mt.out[0];
+    k.codes = a.codes;
+    k.scales = a.scales;
+    k.sums16 = a.sums16;
+    k.x = x;
+    k.fault = fault;
+    const bool multi = mt.n > 1;
+    static bool attr_set[4] = {false, false, false, false};
+    const int ai = (multi ? 1 : 0) + (fused ? 2 : 0);
+    const void *f = multi ? (fused ? reinterpret_cast<const void *>(gemv3_kernel<F, 1, true, true>)
+                                   : reinterpret_cast<const void *>(gemv3_kernel<F, 1, true, false>))
+                          : (fused ? reinterpret_cast<const void *>(gemv3_kernel<F, 1, false, true>)
+                                   : reinterpret_cast<const void *>(gemv3_kernel<F, 1, false, false>));
+    if (!attr_set[ai]) {
+        if (cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) != cudaSuccess)
+            return QB_E_CUDA;
+        attr_set[ai] = true;
+    }
+    const Gemv3K &k1 = k;
+    if (multi)
+        return fused ? launch_pdl(gemv3_kernel<F, 1, true, true>, dim3(grid), dim3(threads), (size_t)smem, stream, k)
+                     : launch_pdl(gemv3_kernel<F, 1, true, false>, dim3(grid), dim3(threads), (size_t)smem, stream, k);
+    return fused ? launch_pdl(gemv3_kernel<F, 1, false, true>, dim3(grid), dim3(threads), (size_t)smem, stream, k1)
+                 : launch_pdl(gemv3_kernel<F, 1, false, false>, dim3(grid), dim3(threads), (size_t)smem, stream, k1);
 }
 
 // The product for 2..16 columns: as many columns a launch as one CTA holds,
@@ -452,6 +556,7 @@ int launch_gemv3_cg(const GemvArgs &a, cudaStream_t stream) {
         k.codes = a.codes + (int64_t)c0 * a.K;
         k.scales = a.scales + (int64_t)c0 * (a.K / blk);
         k.sums16 = a.sums16 ? a.sums16 + (int64_t)c0 * (a.K / 16) : nullptr;
+        k.x = nullptr;
         k.fault = fault;
         const Gemv3K &k1 = k;
         const int rc = multi ? launch_pdl(gemv3_kernel<F, CG, true>, dim3(grid), dim3(threads), (size_t)smem, stream, k)

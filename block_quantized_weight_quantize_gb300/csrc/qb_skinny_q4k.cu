@@ -11,4 +11,8 @@ int launch_skinny<kQ4K>(const GemvArgs &a, cudaStream_t stream) {
     const int rc = launch_gemv5<kQ4K>(a, stream);
     return rc == QB_E_ARG ? launch_gemv3<kQ4K>(a, stream) : rc;
 }
+template <>
+int launch_one_col3<kQ4K>(const GemvArgs &a, cudaStream_t stream, const float *x) {
+    return launch_gemv3_one<kQ4K>(a, stream, x);
+}
 }  // namespace qb

@@ -8,4 +8,8 @@ template <>
 int launch_skinny<kQ6K>(const GemvArgs &a, cudaStream_t stream) {
     return launch_gemv3<kQ6K>(a, stream);
 }
+template <>
+int launch_one_col3<kQ6K>(const GemvArgs &a, cudaStream_t stream, const float *x) {
+    return launch_gemv3_one<kQ6K>(a, stream, x);
+}
 }  // namespace qb

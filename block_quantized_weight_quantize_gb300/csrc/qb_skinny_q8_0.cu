@@ -8,4 +8,8 @@ template <>
 int launch_skinny<kQ8_0>(const GemvArgs &a, cudaStream_t stream) {
     return launch_gemv3<kQ8_0>(a, stream);
 }
+template <>
+int launch_one_col3<kQ8_0>(const GemvArgs &a, cudaStream_t stream, const float *x) {
+    return launch_gemv3_one<kQ8_0>(a, stream, x);
+}
 }  // namespace qb

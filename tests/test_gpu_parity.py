@@ -404,12 +404,15 @@ def test_f16_sixteen_columns_and_nonfinite():
 
 @pytest.mark.parametrize("fmt", FMTS)
 @pytest.mark.parametrize("ncols", [1, 3])
-@pytest.mark.parametrize("rows,K", [(261, 4096), (1000, 1024), (7, 256), (152 * 3 + 5, 2048)])
+@pytest.mark.parametrize("rows,K", [(261, 4096), (1000, 1024), (7, 256), (152 * 3 + 5, 2048), (5021, 4096),
+                                    (1200, 14336)])
 def test_matvec_bit_exact(fmt, ncols, rows, K):
     """q_matvec -- in one launch for one column (the activation quantized inside
     the product kernel), through a workspace otherwise -- equals the oracle's
     quantize_blocks + dot, including activation blocks that are zero, hold a
-    NaN, a denormal or an infinity."""
+    NaN, a denormal or an infinity.  The last two shapes take several ring
+    iterations a CTA: the 256-element formats' one-column launch then runs in
+    the multi-column kernel's organisation."""
     import torch
     blk = synth.BLOCK[fmt]
     x = _edge_activation(ncols, K, blk, seed=rows + K + ncols + fmt)
