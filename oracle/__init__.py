@@ -85,6 +85,8 @@ def lib():
         L.or_int8_score.restype = ctypes.c_float
         L.or_kv_scores.argtypes = [i32, P, P, P, i32, i32, P, P, i64, i64, i32, ctypes.c_float, P]
         L.or_kv_scores.restype = i32
+        L.or_e4m3_to_f32.argtypes, L.or_e4m3_to_f32.restype = [ctypes.c_uint8], ctypes.c_float
+        L.or_gemv_fp8.argtypes, L.or_gemv_fp8.restype = [P, P, i64, i64, P, i32, P, P], i32
     return _lib
 
 
@@ -373,3 +375,23 @@ def kv_scores(scaling: int, qc, qm, qe, d: int, kc, ks, L: int, nkv: int, scale:
     assert lib().or_kv_scores(scaling, _p(qc), _p(qm), _p(qe), nh, d, _p(kc), _p(ks), L, lcap, nkv,
                               np.float32(scale), _p(out)) == 0
     return out
+
+
+# ---------------------------------------------------------------- FP8 E4M3 with 128x128 block scales
+
+def e4m3_to_f32(b: int) -> np.float32:
+    """e4m3ToF32 (colizig OPS page, FP8) of one byte."""
+    return np.float32(lib().or_e4m3_to_f32(int(b) & 0xFF))
+
+
+def gemv_fp8(W: np.ndarray, scales: np.ndarray, rows: int, K: int, x: np.ndarray):
+    """matmulFp8 as dequantize-then-dot (exact dot, one rounding): out f32 [ncols][rows] and
+    absdot f64 [ncols][rows] = sum |x_i * w_i| (the scale of a summation-error bound)."""
+    W = np.ascontiguousarray(W, np.uint8)
+    scales = np.ascontiguousarray(scales, np.float32)
+    x = np.ascontiguousarray(np.atleast_2d(x), np.float32)
+    ncols = x.shape[0]
+    out = np.zeros((ncols, rows), np.float32)
+    ab = np.zeros((ncols, rows), np.float64)
+    assert lib().or_gemv_fp8(_p(W), _p(scales), rows, K, _p(x), ncols, _p(out), _p(ab)) == 0
+    return out, ab

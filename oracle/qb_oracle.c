@@ -19,6 +19,9 @@
  *                     numerics page).  The int8 cache's score path:
  *                     cache_row, int8_codes, INV_127, quantize_head and
  *                     int8_score on the numerics page.
+ *   colizig OPS page -- FP8: e4m3ToF32, dequantRow, matmulFp8 (E4M3 weights
+ *                     with 128x128 block scales; a float path checked there
+ *                     against "dequantize then f32 matmul").
  *
  * Readings taken where the pages are silent (each restated where used):
  *   R1  an activation block whose largest magnitude is 0 gets the scale
@@ -45,6 +48,10 @@
  *   R17 (int8 cache) the reciprocal under which a cache row's codes are
  *       taken is the f32 quotient 1/s, correctly rounded (the page's recip
  *       seeds Newton steps from a table it does not print).
+ *   R19 (FP8) matmulFp8 is read as the page's own check: each weight the f32
+ *       product of its decoded byte and its block scale, the dot exact (in
+ *       double), rounded once; a GPU result is held to the f32 summation
+ *       bound (K + 4) * 2^-24 * sum |x_i * w_i| around it.
  *   R18 (int8 cache) a score against a key row whose f16 scale is infinite
  *       or NaN (a row whose amax*INV_127 overflows binary16) is NAN, as an
  *       unreadable weight scale is (R7); a query block without a scale too.
@@ -992,5 +999,59 @@ int or_kv_scores(int scaling, const int8_t *qc, const uint8_t *qm, const int16_t
             out[(int64_t)h * L + p] = v;
         }
     }
+    return 0;
+}
+
+
+/* =====================================================================
+ * FP8 E4M3 weights with 128x128 block scales (colizig OPS page, FP8:
+ * e4m3ToF32, dequantRow, matmulFp8).
+ * ===================================================================== */
+
+/* ---------------------------------------------------------------------
+ * e4m3ToF32: an OCP E4M3 byte [s:1][e:4][m:3], exponent bias 7, as a number:
+ * e = 0 -> (m/8) * 2^-6 (subnormal; m = 0 is a zero of the sign), otherwise
+ * (1 + m/8) * 2^(e-7); e = 15 with m = 7 is NaN (the format has no
+ * infinity).  Written from the format's definition with ldexp.
+ * ------------------------------------------------------------------- */
+float or_e4m3_to_f32(uint8_t b) {
+    int s = b >> 7, e = (b >> 3) & 15, m = b & 7;
+    if (e == 15 && m == 7) return engine_nan();
+    double v = (e == 0) ? ldexp((double)m, -9) : ldexp(8.0 + m, e - 10);
+    return (float)(s ? -v : v);
+}
+
+/* ---------------------------------------------------------------------
+ * matmulFp8 read as "dequantize then f32 matmul" (the page's own check): the
+ * weight W[r][i] is the f32 product of its decoded byte and its 128x128 block
+ * scale (dequantRow folds the scale), rounded to nearest; the row's dot with
+ * each activation column x[c][:] is then taken in double and rounded once to
+ * f32.  Scales [ceil(rows/128)][ceil(K/128)].  Also the sum of |x_i * w_i| in
+ * double (absdot), against which a GPU's f32 summation error is bounded.
+ * A NaN result is the engine's NaN.
+ * ------------------------------------------------------------------- */
+int or_gemv_fp8(const uint8_t *W, const float *scales, int64_t rows, int64_t K, const float *x, int ncols,
+                float *out, double *absdot) {
+    int64_t kb = (K + 127) / 128;
+    float *w = (float *)malloc((size_t)K * sizeof(float));
+    if (!w) return -1;
+    for (int64_t r = 0; r < rows; r++) {
+        for (int64_t i = 0; i < K; i++) {
+            float s = scales[(r / 128) * kb + i / 128];
+            w[i] = or_e4m3_to_f32(W[r * K + i]) * s;   /* one f32 product, to nearest */
+        }
+        for (int c = 0; c < ncols; c++) {
+            double acc = 0.0, ab = 0.0;
+            for (int64_t i = 0; i < K; i++) {
+                double t = (double)x[(int64_t)c * K + i] * (double)w[i];
+                acc += t;
+                ab += fabs(t);
+            }
+            float v = (float)acc;
+            out[(int64_t)c * rows + r] = isnan(v) ? engine_nan() : v;
+            if (absdot) absdot[(int64_t)c * rows + r] = ab;
+        }
+    }
+    free(w);
     return 0;
 }
