@@ -81,6 +81,14 @@ KV = {
 }
 
 
+# FP8 E4M3 weights with 128x128 block scales (q_gemv_fp8, one launch a step):
+# name: (rows, K, columns, seed, description)
+FP8 = {
+    "fp8_4096x4096": (4096, 4096, 1, 7, "FP8 E4M3 GEMV 4096x4096, 128x128 block scales, batch 1"),
+    "fp8_4096x4096_b16": (4096, 4096, 16, 7, "FP8 E4M3 GEMV 4096x4096, 128x128 block scales, 16 columns"),
+}
+
+
 def kernel_sources_sha() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "block_quantized_weight_quantize_gb300", "csrc")
@@ -721,6 +729,155 @@ def cpu_baseline(fmt, rows, K, ncols, Wh, x, wbytes, budget_s=10.0, sub32=False)
                       f"threads of the scalar C oracle"}
 
 
+def _fp8_inputs(rows, K, ncols, seed):
+    rng = np.random.default_rng(seed)
+    W = rng.integers(0, 256, size=(rows, K), dtype=np.uint8)
+    W[(W & 0x7F) == 0x7F] = 0x3C  # no NaN codes
+    scales = (2.0 ** rng.uniform(-12, -4, size=((rows + 127) // 128, (K + 127) // 128))).astype(np.float32)
+    x = rng.standard_normal((ncols, K)).astype(np.float32)
+    return W, scales, x
+
+
+def run_fp8(args, rank, world):
+    """A step is one q_gemv_fp8 over the matrix (weights streamed from HBM)."""
+    import torch
+    import block_quantized_weight_quantize_gb300 as qb
+
+    rows, K, ncols, seed, desc = FP8[args.workload]
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    Wh, sh, x = _fp8_inputs(rows, K, ncols, seed + 1000 * rank)
+    wbytes = rows * K + sh.nbytes
+    ncopy = max(2, -(-4 * L2_BYTES // wbytes))
+    W = torch.empty((ncopy, rows, K), dtype=torch.uint8, device=dev)
+    W[0].copy_(torch.from_numpy(Wh))
+    for i in range(1, ncopy):
+        W[i].copy_(W[0])
+    sd = torch.from_numpy(sh).to(dev)
+    xd = torch.from_numpy(x).to(dev)
+    out = torch.empty((ncols, rows), dtype=torch.float32, device=dev)
+    stream = torch.cuda.Stream(dev)
+
+    def step(i, s):
+        qb.q_gemv_fp8(W[i % ncopy], sd, rows, K, xd, out, stream=s)
+
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            step(i, stream)
+    stream.synchronize()
+    G = min(args.steps, 1000)
+
+    def capture(fn, n):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            g.capture_begin()
+            for i in range(n):
+                fn(i, stream)
+            g.capture_end()
+        return g
+
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    g_main = capture(step, G)
+    g_w = capture(step, max(1, min(args.warmup, G)))
+    with torch.cuda.stream(stream):
+        for _ in range(max(1, args.warmup // max(1, min(args.warmup, G)))):
+            g_w.replay()
+    stream.synchronize()
+    nrep = max(1, args.steps // G)
+    with ClockSampler(dev.index) as clk:
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(nrep):
+                g_main.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / (nrep * G)
+    clocks = clk.summary()
+    # e2e: x from pinned host memory, the outputs back
+    xh = torch.from_numpy(x).pin_memory()
+    oh = torch.empty((ncols, rows), dtype=torch.float32).pin_memory()
+    n_e2e = min(args.steps, 3000)
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for i in range(n_e2e):
+            xd.copy_(xh, non_blocking=True)
+            step(i, stream)
+            oh.copy_(out, non_blocking=True)
+    stream.synchronize()
+    e2e_s = time.perf_counter() - t0
+    assert qb.q_device_status() == qb.QB_OK
+    step_s = ms / 1e3
+    value = world * wbytes / step_s / 1e9
+    peak, peak_kind = measured_peaks()
+    roof_bytes = wbytes + 4 * K * ncols + 4 * rows * ncols
+    ops = 2 * rows * K * ncols
+    cmax = 16  # columns a launch: the staged activation stays within 200 KB (as the library splits them)
+    while cmax > 1 and cmax * ((K // 16 + 31) // 32) * 2048 > 200 * 1024:
+        cmax //= 2
+    launches = -(-ncols // cmax)
+    res = {
+        "metric": f"weight GB/s ({desc})", "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": nrep * G, "warmup": args.warmup, "ms_per_step": round(ms, 6), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 weights decoded to f32, f32 x, f32 FMA",
+        "data": "synthetic (seeded PCG64: uniform E4M3 codes without NaN, log-uniform 2^-12..2^-4 block scales, "
+                "N(0,1) activations)",
+        "config": {"workload": desc, "rows": rows, "K": K, "ncols": ncols, "weight_bytes_per_step": wbytes,
+                   "l2": f"each step reads a different one of {ncopy} weight copies "
+                         f"({ncopy * wbytes / 2**20:.0f} MiB > 4x L2); no flush",
+                   "timing": f"CUDA graphs of {G} steps, one q_gemv_fp8 launch a step; CUDA events",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "rows_per_s": round(world * rows / step_s, 1), "tops": round(world * ops / step_s / 1e12, 3),
+        "frac_of_8tbs": round(value / 8000.0, 4), "frac_of_measured_copy": round(value / peak, 4),
+        "gpu_launches": nrep * G * launches, "clocks": clocks,
+        "roofline": {"bound": "hbm", "kernel": f"gemv_fp8_kernel ({ncols} columns in {launches} launch(es))",
+                     "achieved": round(roof_bytes / step_s / 1e9, 1), "peak": peak,
+                     "peak_kind": f"{peak_kind} (HBM copy, burst)", "unit": "GB/s",
+                     "frac": round(roof_bytes / step_s / 1e9 / peak, 4), "traffic": None,
+                     "algorithmic_bytes_per_launch": roof_bytes, "avg_launch_us": round(ms * 1e3, 4)},
+        "e2e": {"value": round(world * wbytes * n_e2e / e2e_s / 1e9, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": int(x.nbytes), "d2h_bytes_per_step": int(4 * rows * ncols), "steps": n_e2e,
+                "how": "per step: pinned x -> device, q_gemv_fp8 through the binding, out -> pinned host"},
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = fp8_cpu_baseline(rows, K, Wh, sh, x, wbytes, args.cpu_seconds)
+    return res
+
+
+def fp8_oracle_pass(rows, K, Wh, sh, x, nthreads, row_limit=None):
+    import oracle
+    r_end = rows if row_limit is None else min(rows, row_limit)
+    ex = _pool(nthreads)
+    bounds = np.linspace(0, r_end, nthreads + 1).astype(int)
+
+    def one(i):
+        a, b = int(bounds[i]), int(bounds[i + 1])
+        a0 = a // 128 * 128  # whole scale blocks: the oracle indexes scales from the first row it gets
+        if b > a:
+            oracle.gemv_fp8(Wh[a0:b], sh[a0 // 128:], b - a0, K, x)
+    list(ex.map(one, range(nthreads)))
+    return r_end
+
+
+def fp8_cpu_baseline(rows, K, Wh, sh, x, wbytes, budget_s=10.0):
+    n = _oracle_threads()
+    t0 = time.perf_counter()
+    fp8_oracle_pass(rows, K, Wh, sh, x, n, 256)
+    per = (time.perf_counter() - t0) / 256
+    R = int(max(128, min(rows, budget_s / 3 / max(per, 1e-9))))
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        fp8_oracle_pass(rows, K, Wh, sh, x, n, R)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    return {"value": round(wbytes * (R / rows) * reps / el / 1e9, 4), "unit": "GB/s", "cores": n, "kind": "oracle",
+            "sample": f"{reps} passes over {R} of {rows} rows in {el:.1f} s, rows over {n} threads of the scalar C "
+                      f"oracle (decode, dequantize, dot in double)"}
+
+
 def kv_oracle_pass(scaling, nh, nkv, d, L, q, k, nthreads, pos_limit=None):
     """cache rows + query heads + scores of (a sample of) positions with the oracle, key heads over threads."""
     import oracle
@@ -785,6 +942,34 @@ def run_kv_reference(args):
     }
 
 
+def run_fp8_reference(args):
+    rows, K, ncols, seed, desc = FP8[args.workload]
+    Wh, sh, x = _fp8_inputs(rows, K, ncols, seed)
+    n = _oracle_threads()
+    wbytes = rows * K + sh.nbytes
+    t0 = time.perf_counter()
+    fp8_oracle_pass(rows, K, Wh, sh, x, n, 256)
+    per = (time.perf_counter() - t0) / 256
+    budget = 100.0 / max(1, args.steps + args.warmup)
+    R = int(max(128, min(rows, budget / max(per, 1e-9))))
+    for _ in range(args.warmup):
+        fp8_oracle_pass(rows, K, Wh, sh, x, n, R)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        fp8_oracle_pass(rows, K, Wh, sh, x, n, R)
+    el = time.perf_counter() - t0
+    value = wbytes * (R / rows) * args.steps / el / 1e9
+    sample = f"each step: {R} of {rows} rows, over {n} threads of the scalar C oracle"
+    return {
+        "impl": "reference", "metric": f"weight GB/s ({desc})", "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": 0, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el * 1e3 / args.steps, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 dot (scalar C)",
+        "data": "synthetic (seeded PCG64)", "config": {"workload": desc, "rows": rows, "K": K, "ncols": ncols},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": n, "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
 def run_reference(args):
     fmt, rows, K, ncols, seed, outl, desc = WORKLOADS[args.workload]
     sub32 = args.workload in SUB32
@@ -827,7 +1012,7 @@ def main():
     ap.add_argument("--steps", type=int, default=100000)
     ap.add_argument("--warmup", type=int, default=1000)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="q4k_4096x4096", choices=sorted(WORKLOADS) + sorted(GROUPED) + sorted(KV))
+    ap.add_argument("--workload", default="q4k_4096x4096", choices=sorted(WORKLOADS) + sorted(GROUPED) + sorted(KV) + sorted(FP8))
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--roof-launches", type=int, default=2000,
@@ -843,6 +1028,8 @@ def main():
                                   "workloads; the grouped workload has no oracle timing"}), flush=True)
             elif args.workload in KV:
                 print(json.dumps(run_kv_reference(args)), flush=True)
+            elif args.workload in FP8:
+                print(json.dumps(run_fp8_reference(args)), flush=True)
             else:
                 print(json.dumps(run_reference(args)), flush=True)
         return
@@ -852,7 +1039,8 @@ def main():
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
         tdist.init_process_group("nccl")
     res = (run_grouped(args, rank, world) if args.workload in GROUPED else
-           run_kv(args, rank, world) if args.workload in KV else run_ours(args, rank, world))
+           run_kv(args, rank, world) if args.workload in KV else
+           run_fp8(args, rank, world) if args.workload in FP8 else run_ours(args, rank, world))
     if rank == 0:
         print(json.dumps(res), flush=True)
     if world > 1:

@@ -34,7 +34,7 @@ EXPORTS = ("quantize_act", "q_gemv", "quantize_act_f16", "q_gemv_f16", "q_check_
            "q_block_values", "q_device_status", "q_strerror", "q_matvec", "q_matvec_workspace_bytes",
            "q_matvec_static", "q_gemv_many", "q_gemv_f16_many", "q_matvec_many", "quantize_act_sub32",
            "q_gemv_sub32", "q_matvec_sub32_workspace_bytes", "q_matvec_sub32", "kv_head_codes", "kv_cache_rows",
-           "kv_quantize_heads", "kv_scores")
+           "kv_quantize_heads", "kv_scores", "q_gemv_fp8")
 PERBLOCK, SUB32 = 0, 1  # QB_PERBLOCK, QB_SUB32: how a query head is scaled
 
 
@@ -90,6 +90,7 @@ def lib() -> ctypes.CDLL:
         L.kv_quantize_heads.argtypes, L.kv_quantize_heads.restype = [i32, P, i32, i32, P, P, P], i32
         L.kv_scores.argtypes = [i32, P, P, i32, i32, P, P, i64, i64, i32, ctypes.c_float, P, P]
         L.kv_scores.restype = i32
+        L.q_gemv_fp8.argtypes, L.q_gemv_fp8.restype = [P, P, i64, i64, P, i32, P, P], i32
         _lib = L
     return _lib
 
@@ -197,6 +198,14 @@ def kv_scores(scaling: int, qcodes, qscales, d: int, kcodes, kscales, L: int, sc
     nkv, lcap = kcodes.shape[0], kcodes.shape[1]
     _check(lib().kv_scores(scaling, _ptr(qcodes), _ptr(qscales), nh, d, _ptr(kcodes), _ptr(kscales), L, lcap, nkv,
                            ctypes.c_float(scale), _ptr(out), _stream(stream)), "kv_scores")
+
+
+def q_gemv_fp8(W, scales, rows: int, K: int, x, out, stream=None) -> None:
+    """FP8 E4M3 weights (uint8 [rows, K]) with 128x128 block scales (f32
+    [ceil(rows/128), ceil(K/128)]) times x f32 [ncols, K]: out f32 [ncols, rows]."""
+    ncols = x.shape[0]
+    _check(lib().q_gemv_fp8(_ptr(W), _ptr(scales), rows, K, _ptr(x), ncols, _ptr(out), _stream(stream)),
+           "q_gemv_fp8")
 
 
 def _act(block, codes, scales, sums16):

@@ -478,6 +478,20 @@ int q_matvec_sub32(qb_fmt fmt, const void *W, int64_t rows, int64_t K, const flo
     return q_gemv_sub32(fmt, W, rows, K, &act, ncols, out, stream);
 }
 
+// ---------------------------------------------------------------- FP8 E4M3, 128x128 block scales
+
+int q_gemv_fp8(const uint8_t *W, const float *scales, int64_t rows, int64_t K, const float *x, int ncols, float *out,
+               void *stream) {
+    if (!W || !scales || !x || !out) return QB_E_ARG;
+    if (rows < 0 || rows > (int64_t(1) << 31) || K < 16 || K > 32768 || K % 16 != 0 || ncols < 1 || ncols > 16)
+        return QB_E_ARG;
+    if (misaligned(W) || misaligned(x) || (reinterpret_cast<uintptr_t>(scales) & 3u) ||
+        (reinterpret_cast<uintptr_t>(out) & 3u))
+        return QB_E_ARG;
+    if (rows == 0) return QB_OK;
+    return launch_gemv_fp8(W, scales, rows, K, x, ncols, out, static_cast<cudaStream_t>(stream));
+}
+
 // ---------------------------------------------------------------- the int8 cache's score path
 
 int kv_head_codes(int scaling, int d) {

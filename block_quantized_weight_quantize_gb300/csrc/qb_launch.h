@@ -92,6 +92,9 @@ int launch_gemv_f16(const uint16_t *W, int64_t rows, int64_t K, const uint16_t *
 // Several F16 matrices in one launch; QB_E_ARG when the streaming kernel does not take the shape.
 int launch_gemv_f16_many(const MatTable &t, int64_t K, const uint16_t *x16, int ncols, cudaStream_t stream);
 int launch_check_weights(int fmt, const void *W, int64_t rows, int64_t K, int *flag, cudaStream_t stream);
+// FP8 E4M3 weights with 128x128 block scales (qb_fp8.cu).
+int launch_gemv_fp8(const uint8_t *W, const float *scales, int64_t rows, int64_t K, const float *x, int ncols,
+                    float *out, cudaStream_t stream);
 // The int8 cache's score path (qb_kv.cu).
 int launch_kv_cache_rows(const float *x, int64_t n, int d, int8_t *codes, uint16_t *scales, cudaStream_t stream);
 int launch_kv_quantize_heads(int scaling, const float *q, int nh, int d, int8_t *codes, qb_scale *scales,

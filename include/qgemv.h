@@ -273,6 +273,21 @@ QB_API int64_t q_matvec_sub32_workspace_bytes(int64_t K, int ncols);
 QB_API int q_matvec_sub32(qb_fmt fmt, const void *W, int64_t rows, int64_t K, const float *x, int ncols,
                           float *out, void *workspace, size_t workspace_bytes, void *stream);
 
+/* ---- FP8 E4M3 weights with 128x128 block scales (colizig OPS page, FP8:
+ * e4m3ToF32, dequantRow, matmulFp8).
+ *
+ * W: rows x K bytes, row-major, each an OCP E4M3 number ([s:1][e:4][m:3],
+ * bias 7, subnormals m*2^-9, S.1111.111 NaN, no infinity); scales: f32
+ * [ceil(rows/128)][ceil(K/128)], one per 128x128 block; a weight is its
+ * decoded byte times its block's scale.  x: f32 [ncols][K]; out[c*rows + r]
+ * = the row's dot with column c in f32 arithmetic (a float path, as on the
+ * page: the order of the additions is this library's, and the result lies
+ * within (K + 4) * 2^-24 * sum |x_i * w_i| of the exact dot of the weights
+ * dequantized to f32).  A NaN result is written as 0x7FC00000.
+ * K % 16 == 0, 16 <= K <= 32768, ncols in 1..16; W and x 16-byte aligned. */
+QB_API int q_gemv_fp8(const uint8_t *W, const float *scales, int64_t rows, int64_t K, const float *x, int ncols,
+                      float *out, void *stream);
+
 /* ---- The int8 cache's score path (numerics page: cache_row, int8_codes,
  * INV_127, quantize_head, int8_score). */
 
