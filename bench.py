@@ -174,10 +174,24 @@ def algorithmic_bytes(fmt, rows, K, ncols, sub32=False):
 DP4A_PEAK_TOPS = 64 * 8 * 152 * 2.07e9 / 1e12
 
 
+def one_col_gemv3(fmt, rows, K):
+    """The library's rule for one column: the 256-element formats take the
+    multi-column kernel's organisation when the one-column kernel would need
+    more than one ring iteration per CTA (more than 2 * (512 // (K/128)) rows a
+    CTA over min(152, rows) CTAs)."""
+    if fmt == synth.FMT_Q8_0 or K % 256:
+        return False
+    g = max(1, min(152, rows))
+    return ((rows + g - 1) // g + 1) // 2 > 512 // (K // 128)
+
+
 def roofline(fmt, ncols, single, achieved, peak, peak_kind, traffic, roof_bytes, per_launch_s, prod_s, abytes,
-             ops_per_step, roof_launches, sub32=False):
+             ops_per_step, roof_launches, sub32=False, rows=0, K=0):
+    g3 = ncols == 1 and not sub32 and fmt != synth.FMT_F16 and one_col_gemv3(fmt, rows, K)
     name = ("gemv_f16_kernel" if fmt == synth.FMT_F16 else
             f"s32_kernel<{synth.FORMAT_NAMES[fmt]}, {min(ncols, 2)} column(s) a thread group>" if sub32 else
+            f"gemv3_kernel<{synth.FORMAT_NAMES[fmt]}, one column, single launch> (quantize + product)"
+            if single and g3 else
             f"gemv2_kernel<{synth.FORMAT_NAMES[fmt]}, single launch> (quantize + product)" if single else
             f"gemv3_kernel<{synth.FORMAT_NAMES[fmt]}, {ncols} columns>")
     prod = {"avg_launch_us": round(prod_s * 1e6, 4),
@@ -657,7 +671,7 @@ def run_ours(args, rank, world):
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
         "roofline": roofline(fmt, ncols, single, achieved, peak, peak_kind, traffic, roof_bytes, per_launch_s,
-                             prod_s, abytes, ops_per_step, args.roof_launches, sub32),
+                             prod_s, abytes, ops_per_step, args.roof_launches, sub32, rows, K),
         "e2e": {
             "value": round(world * wbytes * n_e2e / e2e_s / 1e9, 2),
             "unit": "GB/s",
