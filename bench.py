@@ -97,6 +97,26 @@ def kernel_sources_sha() -> str:
     return h.hexdigest()[:16]
 
 
+def barrier():
+    """All ranks meet (nothing to do for one process)."""
+    import torch.distributed as tdist
+    if tdist.is_available() and tdist.is_initialized() and tdist.get_world_size() > 1:
+        tdist.barrier()
+
+
+def max_over_ranks(v, device=None) -> float:
+    """The largest v over the ranks (v itself for one process): a timed region
+    lasts until its slowest rank ends."""
+    import torch
+    import torch.distributed as tdist
+    if not (tdist.is_available() and tdist.is_initialized()) or tdist.get_world_size() == 1:
+        return float(v)
+    dev = device if tdist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(v)], dtype=torch.float64, device=dev)
+    tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def traffic_for(workload):
     """DRAM bytes per launch of the workload's dominant kernel from the committed
     ncu summary, or None when the kernels changed since that capture."""
@@ -295,6 +315,7 @@ def run_kv(args, rank, world):
     stream.synchronize()
     nrep = max(1, args.steps // G)
     with ClockSampler(dev.index) as clk:
+        barrier()
         torch.cuda.synchronize()
         with torch.cuda.stream(stream):
             e0.record(stream)
@@ -302,7 +323,8 @@ def run_kv(args, rank, world):
                 g_main.replay()
             e1.record(stream)
         torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / (nrep * G)
+        barrier()
+    ms = max_over_ranks(e0.elapsed_time(e1), dev) / (nrep * G)
     clocks = clk.summary()
     g_roof = capture(scores_only, G)
     with torch.cuda.stream(stream):
@@ -319,6 +341,7 @@ def run_kv(args, rank, world):
     qh = torch.from_numpy(q).pin_memory()
     oh = torch.empty((nh, L), dtype=torch.float32).pin_memory()
     n_e2e = min(args.steps, 2000)
+    barrier()
     t0 = time.perf_counter()
     with torch.cuda.stream(stream):
         for i in range(n_e2e):
@@ -326,7 +349,7 @@ def run_kv(args, rank, world):
             step(i, stream)
             oh.copy_(out, non_blocking=True)
     stream.synchronize()
-    e2e_s = time.perf_counter() - t0
+    e2e_s = max_over_ranks(time.perf_counter() - t0, dev)
     assert qb.q_device_status() == qb.QB_OK
     step_s = ms / 1e3
     value = world * kbytes / step_s / 1e9
@@ -425,6 +448,7 @@ def run_grouped(args, rank, world):
         sampler = ClockSampler(dev.index) if clocks else None
         if sampler:
             sampler.__enter__()
+        barrier()
         torch.cuda.synchronize()
         with torch.cuda.stream(stream):
             e0.record(stream)
@@ -432,9 +456,11 @@ def run_grouped(args, rank, world):
                 g.replay()
             e1.record(stream)
         torch.cuda.synchronize()
+        barrier()
         if sampler:
             sampler.__exit__(None, None, None)
-        return e0.elapsed_time(e1) / (max(1, steps // G) * G), (sampler.summary() if sampler else None)
+        ms_ = max_over_ranks(e0.elapsed_time(e1), dev)
+        return ms_ / (max(1, steps // G) * G), (sampler.summary() if sampler else None)
 
     ms, clocks = time_graph(grouped, args.steps, clocks=True)
     ms_sep, _ = time_graph(separate, min(args.steps, 20000))
@@ -446,6 +472,7 @@ def run_grouped(args, rank, world):
     xh = torch.from_numpy(x).pin_memory()
     ohs = [torch.empty((ncols, r), dtype=torch.float32).pin_memory() for r in rows_list]
     n_e2e = min(args.steps, 3000)
+    barrier()
     t0 = time.perf_counter()
     with torch.cuda.stream(stream):
         for i in range(n_e2e):
@@ -454,7 +481,7 @@ def run_grouped(args, rank, world):
             for oh, o in zip(ohs, outs):
                 oh.copy_(o, non_blocking=True)
     stream.synchronize()
-    e2e_s = time.perf_counter() - t0
+    e2e_s = max_over_ranks(time.perf_counter() - t0, dev)
     assert qb.q_device_status() == qb.QB_OK
     return {
         "metric": f"weight GB/s ({desc})",
@@ -570,27 +597,18 @@ def run_ours(args, rank, world):
             g_w.replay()
     stream.synchronize()
 
-    dist = world > 1
-    if dist:
-        import torch.distributed as tdist
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     with ClockSampler(dev.index) as clk:
-        if dist:
-            tdist.barrier()
+        barrier()
         torch.cuda.synchronize()
         with torch.cuda.stream(stream):
             e0.record(stream)
             replay_steps(args.steps // G, g_rem)
             e1.record(stream)
         torch.cuda.synchronize()
-        if dist:
-            tdist.barrier()
-    ms = e0.elapsed_time(e1)
-    if dist:
-        t = torch.tensor([ms], device=dev)
-        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
-        ms = float(t.item())
+        barrier()
+    ms = max_over_ranks(e0.elapsed_time(e1), dev)
     clocks = clk.summary()
 
     # ---- roofline: the step's dominant kernel, live, over rotating copies.  For a
@@ -627,8 +645,7 @@ def run_ours(args, rank, world):
             step(i, stream)
             oh.copy_(out, non_blocking=True)
     stream.synchronize()
-    if dist:
-        tdist.barrier()
+    barrier()
     t0 = time.perf_counter()
     with torch.cuda.stream(stream):
         for i in range(n_e2e):
@@ -636,11 +653,7 @@ def run_ours(args, rank, world):
             step(i, stream)
             oh.copy_(out, non_blocking=True)
     stream.synchronize()
-    e2e_s = time.perf_counter() - t0
-    if dist:
-        t = torch.tensor([e2e_s], device=dev)
-        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
-        e2e_s = float(t.item())
+    e2e_s = max_over_ranks(time.perf_counter() - t0, dev)
 
     assert qb.q_device_status() == qb.QB_OK
     step_s = ms / 1e3 / args.steps
@@ -808,6 +821,7 @@ def run_fp8(args, rank, world):
     stream.synchronize()
     nrep = max(1, args.steps // G)
     with ClockSampler(dev.index) as clk:
+        barrier()
         torch.cuda.synchronize()
         with torch.cuda.stream(stream):
             e0.record(stream)
@@ -815,12 +829,14 @@ def run_fp8(args, rank, world):
                 g_main.replay()
             e1.record(stream)
         torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / (nrep * G)
+        barrier()
+    ms = max_over_ranks(e0.elapsed_time(e1), dev) / (nrep * G)
     clocks = clk.summary()
     # e2e: x from pinned host memory, the outputs back
     xh = torch.from_numpy(x).pin_memory()
     oh = torch.empty((ncols, rows), dtype=torch.float32).pin_memory()
     n_e2e = min(args.steps, 3000)
+    barrier()
     t0 = time.perf_counter()
     with torch.cuda.stream(stream):
         for i in range(n_e2e):
@@ -828,7 +844,7 @@ def run_fp8(args, rank, world):
             step(i, stream)
             oh.copy_(out, non_blocking=True)
     stream.synchronize()
-    e2e_s = time.perf_counter() - t0
+    e2e_s = max_over_ranks(time.perf_counter() - t0, dev)
     assert qb.q_device_status() == qb.QB_OK
     step_s = ms / 1e3
     value = world * wbytes / step_s / 1e9
