@@ -34,8 +34,8 @@ EXPORTS = ("quantize_act", "q_gemv", "quantize_act_f16", "q_gemv_f16", "q_check_
            "q_block_values", "q_device_status", "q_strerror", "q_matvec", "q_matvec_workspace_bytes",
            "q_matvec_static", "q_gemv_many", "q_gemv_f16_many", "q_matvec_many", "quantize_act_sub32",
            "q_gemv_sub32", "q_matvec_sub32_workspace_bytes", "q_matvec_sub32", "kv_head_codes", "kv_cache_rows",
-           "kv_quantize_heads", "kv_scores", "q_gemv_fp8")
-PERBLOCK, SUB32 = 0, 1  # QB_PERBLOCK, QB_SUB32: how a query head is scaled
+           "kv_quantize_heads", "kv_scores", "q_gemv_fp8", "q_matvec_host_workspace_bytes", "q_matvec_host")
+PERBLOCK, SUB32 = 0, 1  # QB_PERBLOCK, QB_SUB32: how an activation (or a query head) is scaled
 
 
 class QbError(RuntimeError):
@@ -91,6 +91,10 @@ def lib() -> ctypes.CDLL:
         L.kv_scores.argtypes = [i32, P, P, i32, i32, P, P, i64, i64, i32, ctypes.c_float, P, P]
         L.kv_scores.restype = i32
         L.q_gemv_fp8.argtypes, L.q_gemv_fp8.restype = [P, P, i64, i64, P, i32, P, P], i32
+        L.q_matvec_host_workspace_bytes.argtypes = [i32, i32, i64, i64, i32]
+        L.q_matvec_host_workspace_bytes.restype = i64
+        L.q_matvec_host.argtypes = [i32, i32, P, i64, i64, P, i32, P, P, ctypes.c_size_t, P]
+        L.q_matvec_host.restype = i32
         _lib = L
     return _lib
 
@@ -206,6 +210,24 @@ def q_gemv_fp8(W, scales, rows: int, K: int, x, out, stream=None) -> None:
     ncols = x.shape[0]
     _check(lib().q_gemv_fp8(_ptr(W), _ptr(scales), rows, K, _ptr(x), ncols, _ptr(out), _stream(stream)),
            "q_gemv_fp8")
+
+
+def q_matvec_host_workspace_bytes(scaling: int, fmt: int, rows: int, K: int, ncols: int) -> int:
+    n = lib().q_matvec_host_workspace_bytes(scaling, fmt, rows, K, ncols)
+    if n < 0:
+        raise QbError(int(n), "q_matvec_host_workspace_bytes")
+    return int(n)
+
+
+def q_matvec_host(fmt: int, W, rows: int, K: int, x_host, out_host, workspace, scaling: int = PERBLOCK,
+                  stream=None) -> None:
+    """One call from host to host: x_host f32 [ncols, K] (a pinned CPU tensor for
+    an asynchronous call) is copied to the device, multiplied (q_matvec, or
+    q_matvec_sub32 with scaling=SUB32) and the result copied into out_host f32
+    [ncols, rows] (CPU); synchronize the stream before reading it."""
+    ncols = x_host.shape[0]
+    _check(lib().q_matvec_host(scaling, fmt, _ptr(W), rows, K, _ptr(x_host), ncols, _ptr(out_host), _ptr(workspace),
+                               workspace.numel() * workspace.element_size(), _stream(stream)), "q_matvec_host")
 
 
 def _act(block, codes, scales, sums16):

@@ -478,6 +478,41 @@ int q_matvec_sub32(qb_fmt fmt, const void *W, int64_t rows, int64_t K, const flo
     return q_gemv_sub32(fmt, W, rows, K, &act, ncols, out, stream);
 }
 
+// ---------------------------------------------------------------- host buffers in, host buffers out
+
+int64_t q_matvec_host_workspace_bytes(int scaling, qb_fmt fmt, int64_t rows, int64_t K, int ncols) {
+    if ((scaling != QB_PERBLOCK && scaling != QB_SUB32) || rows < 0 || K < 0 || ncols < 1 || ncols > 16)
+        return QB_E_ARG;
+    if (scaling == QB_SUB32 && fmt == QB_F16) return QB_E_FORMAT;
+    const int64_t inner =
+        scaling == QB_SUB32 ? q_matvec_sub32_workspace_bytes(K, ncols) : q_matvec_workspace_bytes(fmt, K, ncols);
+    if (inner < 0) return inner;
+    return align16(4 * K * ncols) + align16(4 * rows * ncols) + inner;
+}
+
+int q_matvec_host(int scaling, qb_fmt fmt, const void *W, int64_t rows, int64_t K, const float *x_host, int ncols,
+                  float *out_host, void *workspace, size_t workspace_bytes, void *stream) {
+    if (!x_host || !out_host || !W || !workspace || misaligned(workspace)) return QB_E_ARG;
+    const int64_t need = q_matvec_host_workspace_bytes(scaling, fmt, rows, K, ncols);
+    if (need < 0) return (int)need;
+    if ((int64_t)workspace_bytes < need) return QB_E_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    float *xd = reinterpret_cast<float *>(ws);
+    float *od = reinterpret_cast<float *>(ws + align16(4 * K * ncols));
+    uint8_t *inner = ws + align16(4 * K * ncols) + align16(4 * rows * ncols);
+    const size_t inner_bytes = (size_t)(need - (inner - ws));
+    if (rows == 0) return QB_OK;
+    if (K > 0 && cudaMemcpyAsync(xd, x_host, (size_t)(4 * K * ncols), cudaMemcpyHostToDevice, s) != cudaSuccess)
+        return QB_E_CUDA;
+    const int rc = scaling == QB_SUB32 ? q_matvec_sub32(fmt, W, rows, K, xd, ncols, od, inner, inner_bytes, stream)
+                                       : q_matvec(fmt, W, rows, K, xd, ncols, od, inner, inner_bytes, stream);
+    if (rc) return rc;
+    if (cudaMemcpyAsync(out_host, od, (size_t)(4 * rows * ncols), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return QB_E_CUDA;
+    return QB_OK;
+}
+
 // ---------------------------------------------------------------- FP8 E4M3, 128x128 block scales
 
 int q_gemv_fp8(const uint8_t *W, const float *scales, int64_t rows, int64_t K, const float *x, int ncols, float *out,

@@ -333,6 +333,25 @@ QB_API int kv_scores(int scaling, const int8_t *qcodes, const qb_scale *qscales,
                      const int8_t *kcodes, const uint16_t *kscales, int64_t L, int64_t lcap, int nkv, float scale,
                      float *out, void *stream);
 
+/* ---- One call from host memory to host memory. */
+
+/* Device workspace q_matvec_host needs: the activation and the outputs on the
+ * device plus q_matvec's (QB_PERBLOCK) or q_matvec_sub32's (QB_SUB32) own
+ * workspace; a negative QB_E_* code for a bad request. */
+QB_API int64_t q_matvec_host_workspace_bytes(int scaling, qb_fmt fmt, int64_t rows, int64_t K, int ncols);
+
+/* q_matvec (scaling QB_PERBLOCK; every format) or q_matvec_sub32 (QB_SUB32)
+ * with the activation x_host f32 [ncols][K] and the result out_host f32
+ * [ncols][rows] in HOST memory: one call enqueues on `stream` the copy of x
+ * to the device workspace, the product and the copy of the result back
+ * (cudaMemcpyAsync each way; asynchronous when the host buffers are pinned,
+ * so synchronize the stream before reading out_host).  W is device memory as
+ * for q_matvec; workspace is device memory of at least
+ * q_matvec_host_workspace_bytes(...) bytes, 16-byte aligned.  Results and
+ * errors are those of q_matvec / q_matvec_sub32. */
+QB_API int q_matvec_host(int scaling, qb_fmt fmt, const void *W, int64_t rows, int64_t K, const float *x_host,
+                         int ncols, float *out_host, void *workspace, size_t workspace_bytes, void *stream);
+
 /* A static string for a status code. */
 QB_API const char *q_strerror(int status);
 

@@ -71,3 +71,17 @@ def test_binding_fails_loudly_without_library(monkeypatch):
     monkeypatch.setattr(qb, "LIB_PATH", "/nonexistent/libqgemv.so")
     with pytest.raises(RuntimeError):
         qb.lib()
+
+
+def test_matvec_host_argument_checks():
+    L = qb.lib()
+    P = ctypes.c_void_p
+    assert L.q_matvec_host_workspace_bytes(2, qb.Q4K, 4, 256, 1) == qb.QB_E_ARG
+    assert L.q_matvec_host_workspace_bytes(qb.SUB32, qb.F16, 4, 256, 1) == qb.QB_E_FORMAT
+    assert L.q_matvec_host_workspace_bytes(qb.PERBLOCK, qb.Q4K, 4, 256, 17) == qb.QB_E_ARG
+    n = L.q_matvec_host_workspace_bytes(qb.PERBLOCK, qb.Q4K, 4, 256, 1)
+    assert n >= 4 * 256 + 4 * 4
+    # null host buffers and a short workspace are refused before any CUDA call
+    assert L.q_matvec_host(qb.PERBLOCK, qb.Q4K, P(4096), 4, 256, None, 1, P(4096), P(4096), n, None) == qb.QB_E_ARG
+    assert L.q_matvec_host(qb.PERBLOCK, qb.Q4K, P(4096), 4, 256, P(4096), 1, P(4096), P(4096), n - 16,
+                           None) == qb.QB_E_ARG

@@ -475,3 +475,37 @@ def test_matvec_f16():
     qb.q_matvec(qb.F16, dev(W), rows, K, dev(x), out, workspace=ws)
     torch.cuda.synchronize()
     assert np.array_equal(bits(host(out)), bits(want))
+
+
+# ---------------------------------------------------------------- host to host in one call
+
+@pytest.mark.parametrize("scaling,fmt,ncols", [(qb.PERBLOCK, synth.FMT_Q4K, 1), (qb.PERBLOCK, synth.FMT_Q6K, 3),
+                                               (qb.PERBLOCK, synth.FMT_Q8_0, 1), (qb.SUB32, synth.FMT_Q4K, 2),
+                                               (qb.PERBLOCK, synth.FMT_F16, 2)])
+def test_matvec_host_matches_device_call(scaling, fmt, ncols):
+    """q_matvec_host (pinned x in, pinned out back, one call) gives the bits of
+    the device-buffer call on the same stream."""
+    import torch
+    rows, K = 1000, 1024
+    rng = np.random.default_rng(31 + fmt + ncols + scaling)
+    if fmt == synth.FMT_F16:
+        W = synth.draw_f16(rng, rows, K)
+        Wd = dev(W.view(np.int16))
+    else:
+        W = synth.pack(fmt, synth.draw(fmt, rng, rows, K))
+        Wd = dev(W)
+    x = synth.draw_act(rng, ncols, K, outlier_frac=0.001)
+    xh = torch.from_numpy(x).pin_memory()
+    oh = torch.full((ncols, rows), float("nan"), dtype=torch.float32).pin_memory()
+    ws = torch.empty(qb.q_matvec_host_workspace_bytes(scaling, fmt, rows, K, ncols), dtype=torch.uint8, device="cuda")
+    s = torch.cuda.Stream()
+    qb.q_matvec_host(fmt, Wd, rows, K, xh, oh, ws, scaling=scaling, stream=s)
+    s.synchronize()
+    od = torch.full((ncols, rows), float("nan"), dtype=torch.float32, device="cuda")
+    if scaling == qb.SUB32:
+        qb.q_matvec_sub32(fmt, Wd, rows, K, dev(x), od)
+    else:
+        ws2 = torch.empty(qb.q_matvec_workspace_bytes(fmt, K, ncols), dtype=torch.uint8, device="cuda")
+        qb.q_matvec(fmt, Wd, rows, K, dev(x), od, workspace=ws2)
+    torch.cuda.synchronize()
+    assert np.array_equal(bits(oh.numpy()), bits(host(od)))
