@@ -220,7 +220,8 @@ def one_col_gemv3(fmt, rows, K):
 def roofline(fmt, ncols, single, achieved, peak, peak_kind, traffic, roof_bytes, per_launch_s, prod_s, abytes,
              ops_per_step, roof_launches, sub32=False, rows=0, K=0):
     g3 = ncols == 1 and not sub32 and fmt != synth.FMT_F16 and one_col_gemv3(fmt, rows, K)
-    name = ("gemv_f16_kernel" if fmt == synth.FMT_F16 else
+    name = (f"gemv_f16w_kernel<{ncols}{', single launch (f16 rounding in the prologue)' if single else ''}>"
+            if fmt == synth.FMT_F16 else
             f"s32_kernel<{synth.FORMAT_NAMES[fmt]}, {min(ncols, 2)} column(s) a thread group>" if sub32 else
             f"gemv3_kernel<{synth.FORMAT_NAMES[fmt]}, one column, single launch> (quantize + product)"
             if single and g3 else
@@ -546,7 +547,8 @@ def run_ours(args, rank, world):
     ws = torch.empty(qb.q_matvec_sub32_workspace_bytes(K, ncols) if sub32 else
                      qb.q_matvec_workspace_bytes(fmt, K, ncols), dtype=torch.uint8, device=dev)
     # one launch per step where the single-launch product applies, else two
-    single = fmt != synth.FMT_F16 and ncols == 1 and K % 256 == 0 and not sub32
+    single = ((fmt != synth.FMT_F16 and ncols == 1 and K % 256 == 0 and not sub32) or
+              (fmt == synth.FMT_F16 and ncols * K * 4 <= 227 * 1024))
     launches_per_step = 1 if single else 2
     stream = torch.cuda.Stream(dev)
 

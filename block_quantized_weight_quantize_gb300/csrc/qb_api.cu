@@ -264,6 +264,18 @@ int q_matvec(qb_fmt fmt, const void *W, int64_t rows, int64_t K, const float *x,
             if (r != QB_E_ARG) return r;  // QB_E_ARG: the single-launch kernel does not take this shape
         }
     }
+    if (fmt == QB_F16) {  // one launch where the warp-ring kernel takes the shape (f16 rounding in its prologue)
+        if (rows < 0 || K < 0 || K % 8 != 0 || ncols < 1 || ncols > 16 || rows > (int64_t(1) << 31) ||
+            misaligned(W) || (reinterpret_cast<uintptr_t>(out) & 3u))
+            return QB_E_ARG;
+        if (rows == 0) return QB_OK;
+        if (K == 0)
+            return cudaMemsetAsync(out, 0, (size_t)ncols * rows * sizeof(float), s) == cudaSuccess ? QB_OK : QB_E_CUDA;
+        if ((int64_t)ncols * K * 4 <= 227 * 1024) {
+            const int r = launch_matvec_f16(single_table(W, rows, out), K, x, ncols, s);
+            if (r != QB_E_ARG) return r;
+        }
+    }
     if (!workspace || (int64_t)workspace_bytes < need || misaligned(workspace)) return QB_E_ARG;
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     if (fmt == QB_F16) {
@@ -378,6 +390,17 @@ int q_matvec_many(qb_fmt fmt, int nmat, const void *const *W, const int64_t *row
             cudaStream_t s = static_cast<cudaStream_t>(stream);
             rc = f == kQ8_0 ? launch_matvec_q8_0(a, x, s) : f == kQ4K ? launch_matvec_q4k(a, x, s)
                                                                       : launch_matvec_q6k(a, x, s);
+            if (rc != QB_E_ARG) return rc;
+        }
+    }
+    if (fmt == QB_F16 && t.start[nmat] > 0 && K > 0 && K % 8 == 0 && ncols >= 1 && ncols <= 16 &&
+        (int64_t)ncols * K * 4 <= 227 * 1024) {  // one launch for the group
+        bool okp = true;
+        for (int i = 0; i < nmat; ++i)
+            okp = okp && W[i] && out[i] && rows[i] >= 0 && !misaligned(W[i]) &&
+                  !(reinterpret_cast<uintptr_t>(out[i]) & 3u);
+        if (okp) {
+            rc = launch_matvec_f16(t, K, x, ncols, static_cast<cudaStream_t>(stream));
             if (rc != QB_E_ARG) return rc;
         }
     }

@@ -126,6 +126,167 @@ __global__ void __launch_bounds__(256) gemv_f16_kernel(const F16K p) {
     }
 }
 
+// ------------------------------------------------------------------ warp rings
+// The same arithmetic with every warp streaming its own groups of 8 rows
+// through D slots of its own: a slot is refilled as soon as its warp has used
+// it (a bulk copy per row into the padded pitch, completing on the warp's
+// slot mbarrier), so no warp waits at a CTA-wide barrier for a refill.  The
+// CTA's rows are contiguous; warp w takes its 8-row groups w, w + nw, ...
+// FUSED: the activation is rounded to f16 here (f32_to_f16, as
+// quantize_act_f16 does) and widened to f32 in shared memory.
+struct F16WK {
+    MatTable mt;
+    int64_t rows;
+    int K;
+    int pitch;  // bytes per row in a slot (2K padded to an odd number of 16-B units)
+    int D;      // slots a warp
+    int nw;     // warps a CTA
+    int64_t base;
+    int64_t rem;
+    const uint16_t *x16;
+    const float *x32;  // FUSED: the f32 activation
+    int *fault;
+};
+
+__host__ __device__ inline int f16w_smem(int K, int nc, int pitch, int D, int nw) {
+    return 256 + f16_xs_bytes(K, nc) + nw * D * 8 * pitch;
+}
+
+template <int NC, bool FUSED>
+__global__ void __launch_bounds__(256) gemv_f16w_kernel(const F16WK p) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    const int rr = lane >> 2, pp = lane & 3;  // row of the group, lane pair
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem) + w * p.D;
+    float *xs = reinterpret_cast<float *>(smem + 256);
+    uint8_t *ring = smem + 256 + f16_xs_bytes(p.K, NC) + (int64_t)w * p.D * 8 * p.pitch;
+    const int64_t c = blockIdx.x;
+    const int64_t row0 = c * p.base + (c < p.rem ? c : p.rem);
+    const int64_t count = p.base + (c < p.rem ? 1 : 0);
+    const int64_t ngroups = (count + 7) / 8;
+    const uint32_t rowb = (uint32_t)(2 * p.K);
+
+    if (lane == 0) {
+        for (int s = 0; s < p.D; ++s) mbar_init(bars + s, 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+    // the fill of this warp's j-th group into slot j % D
+    auto fill = [&](int j) {
+        const int64_t gi = w + (int64_t)j * p.nw;
+        if (gi >= ngroups) return;
+        const int slot = j % p.D;
+        const int n = (int)(count - 8 * gi < 8 ? count - 8 * gi : 8);
+        if (lane == 0) mbar_arrive_expect_tx(bars + slot, (uint32_t)n * rowb);
+        __syncwarp();
+        if (lane < n)
+            bulk_g2s(ring + ((int64_t)slot * 8 + lane) * p.pitch, row_ptr(p.mt, row0 + 8 * gi + lane, rowb), rowb,
+                     bars + slot);
+    };
+    for (int j = 0; j < p.D; ++j) fill(j);  // weights depend on no earlier kernel
+    pdl_wait();
+    if (FUSED) {
+        for (int i = tid; i < NC * p.K; i += blockDim.x) xs[i] = __half2float(__float2half_rn(__ldg(p.x32 + i)));
+    } else {
+        for (int i = tid; i < NC * p.K; i += blockDim.x) xs[i] = __half2float(__ushort_as_half(p.x16[i]));
+    }
+    __syncthreads();
+    pdl_launch_dependents();
+
+    const int n8 = p.K / 8;
+    for (int j = 0;; ++j) {
+        const int64_t gi = w + (int64_t)j * p.nw;
+        if (gi >= ngroups) break;
+        const int slot = j % p.D;
+        const bool ok = mbar_wait_bounded(bars + slot, (uint32_t)((j / p.D) & 1), p.fault);
+        if (!__all_sync(0xFFFFFFFFu, ok)) return;  // a fill never completed: fault word raised
+        const int64_t l = 8 * gi + rr;              // row within the CTA's range
+        const bool have = l < count;
+        float acc0[NC], acc1[NC];
+#pragma unroll
+        for (int q = 0; q < NC; ++q) { acc0[q] = 0.0f; acc1[q] = 0.0f; }
+        if (have) {
+            const uint32_t *wr = reinterpret_cast<const uint32_t *>(ring + ((int64_t)slot * 8 + rr) * p.pitch) + pp;
+#pragma unroll 4
+            for (int k = 0; k < n8; ++k) {
+                const uint32_t w2 = wr[4 * k];  // elements 8k+2pp, 8k+2pp+1: lanes 2pp, 2pp+1
+                const float2 wf = __half22float2(*reinterpret_cast<const __half2 *>(&w2));
+#pragma unroll
+                for (int q = 0; q < NC; ++q) {
+                    const float2 xv = *reinterpret_cast<const float2 *>(xs + q * p.K + 8 * k + 2 * pp);
+                    acc0[q] = fmaf(wf.x, xv.x, acc0[q]);
+                    acc1[q] = fmaf(wf.y, xv.y, acc1[q]);
+                }
+            }
+        }
+#pragma unroll
+        for (int q = 0; q < NC; ++q) {
+            const float pair = __fadd_rn(acc0[q], acc1[q]);                             // (l0+l1) .. (l6+l7)
+            const float quad = __fadd_rn(pair, __shfl_xor_sync(0xFFFFFFFFu, pair, 1));  // on even pp
+            const float all = __fadd_rn(quad, __shfl_xor_sync(0xFFFFFFFFu, quad, 2));   // on pp == 0
+            if (have && pp == 0) {
+                float r = all;
+                if (r != r) r = __uint_as_float(kEngineNaN);
+                *out_ptr(p.mt, q, row0 + l) = r;
+            }
+        }
+        __syncwarp();  // every lane has read the slot
+        if (lane == 0) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        fill(j + p.D);
+    }
+}
+
+template <int NC>
+static int launch_f16w_nc(const F16WK &k, int smem, unsigned grid, bool fused, cudaStream_t stream) {
+    static bool attr_set[2] = {false, false};
+    const void *f = fused ? reinterpret_cast<const void *>(gemv_f16w_kernel<NC, true>)
+                          : reinterpret_cast<const void *>(gemv_f16w_kernel<NC, false>);
+    if (!attr_set[fused]) {
+        if (cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) != cudaSuccess)
+            return QB_E_CUDA;
+        attr_set[fused] = true;
+    }
+    return fused ? launch_pdl(gemv_f16w_kernel<NC, true>, dim3(grid), dim3(32 * k.nw), (size_t)smem, stream, k)
+                 : launch_pdl(gemv_f16w_kernel<NC, false>, dim3(grid), dim3(32 * k.nw), (size_t)smem, stream, k);
+}
+
+// The warp-ring kernel over a table of matrices: 8 warps a CTA (or as many
+// as fit with two slots each, at least 4), up to 3 slots a warp; QB_E_ARG
+// when fewer than 4 warps fit.
+static int launch_f16w_table(const MatTable &t, int64_t K, const uint16_t *x16, const float *x32, int ncols,
+                             cudaStream_t stream) {
+    F16WK k;
+    k.mt = t;
+    k.rows = t.start[t.n];
+    k.K = (int)K;
+    const int units = (int)(K / 8);
+    k.pitch = 16 * (units + ((units & 1) ? 2 : 1));  // odd number of 16-B units
+    const int budget = 227 * 1024 - 1024;
+    k.nw = 8;
+    while (k.nw > 4 && f16w_smem(k.K, ncols, k.pitch, 2, k.nw) > budget) --k.nw;
+    if (f16w_smem(k.K, ncols, k.pitch, 2, k.nw) > budget) return QB_E_ARG;
+    k.D = 2;
+    while (k.D < 3 && f16w_smem(k.K, ncols, k.pitch, k.D + 1, k.nw) <= budget) ++k.D;
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(num_sms(), (k.rows + 8 * k.nw - 1) / (8 * k.nw)));
+    k.base = k.rows / grid;
+    k.rem = k.rows % grid;
+    k.x16 = x16;
+    k.x32 = x32;
+    k.fault = fault_word();
+    if (!k.fault) return QB_E_CUDA;
+    const int smem = f16w_smem(k.K, ncols, k.pitch, k.D, k.nw);
+    const bool fused = x32 != nullptr;
+    switch (ncols) {
+#define QB_CASE(N) \
+    case N: return launch_f16w_nc<N>(k, smem, (unsigned)grid, fused, stream);
+        QB_CASE(1) QB_CASE(2) QB_CASE(3) QB_CASE(4) QB_CASE(5) QB_CASE(6) QB_CASE(7) QB_CASE(8)
+        QB_CASE(9) QB_CASE(10) QB_CASE(11) QB_CASE(12) QB_CASE(13) QB_CASE(14) QB_CASE(15) QB_CASE(16)
+#undef QB_CASE
+    }
+    return QB_E_ARG;
+}
+
 // Rows longer than the streaming kernel's shared-memory ring allows: one
 // thread per row, the row read straight from global memory in 16-byte chunks.
 __device__ __forceinline__ uint4 ldg_nc16(const void *p) {
@@ -263,7 +424,9 @@ static int launch_f16_table(const MatTable &t, int64_t K, const uint16_t *x16, i
 
 int launch_gemv_f16(const uint16_t *W, int64_t rows, int64_t K, const uint16_t *x16, int ncols, float *out,
                     cudaStream_t stream) {
-    const int rc = launch_f16_table(single_table(W, rows, out), K, x16, ncols, stream);
+    int rc = launch_f16w_table(single_table(W, rows, out), K, x16, nullptr, ncols, stream);
+    if (rc != QB_E_ARG) return rc;
+    rc = launch_f16_table(single_table(W, rows, out), K, x16, ncols, stream);
     if (rc != QB_E_ARG) return rc;
     switch (ncols) {  // a slot of 8 rows does not fit: the row-per-thread kernel
 #define QB_CASE(N) \
@@ -276,7 +439,12 @@ int launch_gemv_f16(const uint16_t *W, int64_t rows, int64_t K, const uint16_t *
 }
 
 int launch_gemv_f16_many(const MatTable &t, int64_t K, const uint16_t *x16, int ncols, cudaStream_t stream) {
-    return launch_f16_table(t, K, x16, ncols, stream);
+    const int rc = launch_f16w_table(t, K, x16, nullptr, ncols, stream);
+    return rc != QB_E_ARG ? rc : launch_f16_table(t, K, x16, ncols, stream);
+}
+
+int launch_matvec_f16(const MatTable &t, int64_t K, const float *x, int ncols, cudaStream_t stream) {
+    return launch_f16w_table(t, K, nullptr, x, ncols, stream);
 }
 
 }  // namespace qb

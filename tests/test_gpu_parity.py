@@ -463,18 +463,32 @@ def test_matvec_repeated_launches_graph():
         assert np.array_equal(bits(host(outs[i])), bits(want)), i
 
 
-def test_matvec_f16():
+@pytest.mark.parametrize("rows,K,ncols", [(1536, 576, 2), (49152, 576, 1), (777, 576, 6), (300, 2048, 3),
+                                         (9, 8, 1), (64, 16384, 1)])
+def test_matvec_f16(rows, K, ncols):
+    """q_matvec for F16 -- one launch that rounds x to f16 in the prologue where
+    the warp-ring kernel takes the shape (no workspace), else quantize_act_f16
+    + q_gemv_f16 -- equals the oracle's f32_to_f16 + fdot, including elements
+    that round to f16 infinities, subnormals and NaN."""
     import torch
-    rng = np.random.default_rng(4)
-    rows, K = 1536, 576
+    rng = np.random.default_rng(4 + rows + K)
     W = synth.draw_f16(rng, rows, K)
-    x = synth.draw_act(rng, 2, K)
+    x = synth.draw_act(rng, ncols, K)
+    x[0, 0] = np.float32(70000.0)          # past the f16 top: +inf
+    x[0, min(1, K - 1)] = np.float32(3e-6)  # an f16 subnormal
+    if K > 2:
+        x[-1, 2] = np.nan
     want = oracle.gemv_f16(W, rows, K, oracle.quantize_f16(x))
-    out = torch.empty((2, rows), dtype=torch.float32, device="cuda")
-    ws = torch.empty(qb.q_matvec_workspace_bytes(qb.F16, K, 2), dtype=torch.uint8, device="cuda")
+    out = torch.full((ncols, rows), float("nan"), dtype=torch.float32, device="cuda")
+    ws = torch.empty(qb.q_matvec_workspace_bytes(qb.F16, K, ncols), dtype=torch.uint8, device="cuda")
     qb.q_matvec(qb.F16, dev(W), rows, K, dev(x), out, workspace=ws)
     torch.cuda.synchronize()
     assert np.array_equal(bits(host(out)), bits(want))
+    if ncols * K * 4 <= 16 * 1024:  # the one-launch form needs no workspace
+        out2 = torch.full((ncols, rows), float("nan"), dtype=torch.float32, device="cuda")
+        qb.q_matvec(qb.F16, dev(W), rows, K, dev(x), out2, workspace=None)
+        torch.cuda.synchronize()
+        assert np.array_equal(bits(host(out2)), bits(want))
 
 
 # ---------------------------------------------------------------- host to host in one call
