@@ -217,15 +217,30 @@ def one_col_gemv3(fmt, rows, K):
     return ((rows + g - 1) // g + 1) // 2 > 512 // (K // 128)
 
 
+def one_col_gemv6(fmt, rows, K):
+    """The library's rule for the warp-ring one-column kernel: 256-element
+    formats, K = 4096, at most 32 rows a CTA over min(152, rows/2) CTAs."""
+    if fmt == synth.FMT_Q8_0 or K != 4096 or rows < 1:
+        return False
+    g = max(1, min(152, (rows + 1) // 2))
+    return (rows + g - 1) // g <= 32
+
+
 def roofline(fmt, ncols, single, achieved, peak, peak_kind, traffic, roof_bytes, per_launch_s, prod_s, abytes,
              ops_per_step, roof_launches, sub32=False, rows=0, K=0):
-    g3 = ncols == 1 and not sub32 and fmt != synth.FMT_F16 and one_col_gemv3(fmt, rows, K)
-    name = (f"gemv_f16w_kernel<{ncols}{', single launch (f16 rounding in the prologue)' if single else ''}>"
+    g6 = ncols == 1 and not sub32 and fmt != synth.FMT_F16 and one_col_gemv6(fmt, rows, K)
+    g3 = ncols == 1 and not sub32 and fmt != synth.FMT_F16 and not g6 and one_col_gemv3(fmt, rows, K)
+    g6name = (f"gemv6_kernel<{synth.FORMAT_NAMES[fmt]}, one column, warp rings" +
+              (", single launch> (quantize + product)" if single else ">"))
+    name = (g6name if g6 else
+            f"gemv_f16w_kernel<{ncols}{', single launch (f16 rounding in the prologue)' if single else ''}>"
             if fmt == synth.FMT_F16 else
             f"s32_kernel<{synth.FORMAT_NAMES[fmt]}, {min(ncols, 2)} column(s) a thread group>" if sub32 else
             f"gemv3_kernel<{synth.FORMAT_NAMES[fmt]}, one column, single launch> (quantize + product)"
             if single and g3 else
             f"gemv2_kernel<{synth.FORMAT_NAMES[fmt]}, single launch> (quantize + product)" if single else
+            f"gemv5_kernel<q4k, {ncols} columns> (f16 tensor-core sub-block sums)"
+            if fmt == synth.FMT_Q4K and 11 <= ncols <= 16 and K % 256 == 0 and K <= 4096 else
             f"gemv3_kernel<{synth.FORMAT_NAMES[fmt]}, {ncols} columns>")
     prod = {"avg_launch_us": round(prod_s * 1e6, 4),
             "achieved_gbs": round(abytes / prod_s / 1e9, 1),
@@ -502,7 +517,7 @@ def run_grouped(args, rank, world):
         "frac_of_8tbs": round(value / 8000.0, 4), "frac_of_measured_copy": round(value / peak, 4),
         "gpu_launches": max(1, args.steps // G) * G, "clocks": clocks,
         "roofline": {"bound": "hbm",
-                     "kernel": f"{'gemv3_kernel' if one_col_gemv3(fmt, sum(rows_list), K) else 'gemv2_kernel'}"
+                     "kernel": f"{'gemv6_kernel' if one_col_gemv6(fmt, sum(rows_list), K) else 'gemv3_kernel' if one_col_gemv3(fmt, sum(rows_list), K) else 'gemv2_kernel'}"
                                f"<{synth.FORMAT_NAMES[fmt]}, one column, single launch, grouped>",
                      "achieved": round(roof_bytes / step_s / 1e9, 1), "peak": peak,
                      "peak_kind": f"{peak_kind} (HBM copy, burst)", "unit": "GB/s",

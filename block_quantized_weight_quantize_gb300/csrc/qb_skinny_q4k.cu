@@ -1,8 +1,10 @@
 // qb_skinny_q4k.cu -- the 2..16-column kernels for the Q4_K-like format (a
 // translation unit of its own so the formats compile in parallel): the
-// tensor-core kernel from 11 columns, the dp4a streaming kernel otherwise.
+// tensor-core kernel from 11 columns, the dp4a streaming kernel otherwise;
+// and the one-column forms (qb_gemv6.cuh, qb_gemv3.cuh) where they apply.
 #include "qb_gemv.cuh"
 #include "qb_gemv3.cuh"
+#include "qb_gemv6.cuh"
 #include "qb_gemv5.cuh"
 
 namespace qb {
@@ -13,6 +15,8 @@ int launch_skinny<kQ4K>(const GemvArgs &a, cudaStream_t stream) {
 }
 template <>
 int launch_one_col3<kQ4K>(const GemvArgs &a, cudaStream_t stream, const float *x) {
+    const int r6 = launch_gemv6<kQ4K>(a, stream, x);  // K = 4096, up to one row pair a warp
+    if (r6 != QB_E_ARG) return r6;
     return launch_gemv3_one<kQ4K>(a, stream, x);
 }
 }  // namespace qb

@@ -2,6 +2,7 @@
 // (a translation unit of its own so the formats compile in parallel).
 #include "qb_gemv.cuh"
 #include "qb_gemv3.cuh"
+#include "qb_gemv6.cuh"
 
 namespace qb {
 template <>
@@ -10,6 +11,8 @@ int launch_skinny<kQ6K>(const GemvArgs &a, cudaStream_t stream) {
 }
 template <>
 int launch_one_col3<kQ6K>(const GemvArgs &a, cudaStream_t stream, const float *x) {
+    const int r6 = launch_gemv6<kQ6K>(a, stream, x);  // K = 4096, up to one row pair a warp
+    if (r6 != QB_E_ARG) return r6;
     return launch_gemv3_one<kQ6K>(a, stream, x);
 }
 }  // namespace qb

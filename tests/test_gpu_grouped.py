@@ -56,7 +56,8 @@ def _dev_w(Wh):
 
 @pytest.mark.parametrize("fmt", FMTS)
 @pytest.mark.parametrize("ncols", [1, 3, 16])
-@pytest.mark.parametrize("rows_list,K", [([300, 77, 0, 129], 2048), ([4096, 1024, 1024], 4096), ([5, 3], 256)])
+@pytest.mark.parametrize("rows_list,K", [([300, 77, 0, 129], 2048), ([4096, 1024, 1024], 4096), ([5, 3], 256),
+                                         ([1001, 2000, 513], 4096)])
 def test_gemv_many_bit_exact(fmt, ncols, rows_list, K):
     import torch
     Ws = _mats(fmt, rows_list, K, seed=sum(rows_list) + ncols + fmt)
@@ -78,10 +79,12 @@ def test_gemv_many_bit_exact(fmt, ncols, rows_list, K):
 
 @pytest.mark.parametrize("fmt", FMTS)
 @pytest.mark.parametrize("ncols", [1, 3])
-def test_matvec_many_matches_separate_calls(fmt, ncols):
-    """q_matvec_many (one launch for one column) against q_matvec per matrix."""
+@pytest.mark.parametrize("rows_list,K", [([700, 152 * 2 + 3, 64], 1024), ([1001, 2000, 513], 4096)])
+def test_matvec_many_matches_separate_calls(fmt, ncols, rows_list, K):
+    """q_matvec_many (one launch for one column) against q_matvec per matrix;
+    at K = 4096 the group is under 33 rows a CTA (the warp-ring one-column
+    kernel), with matrix boundaries inside row pairs."""
     import torch
-    rows_list, K = [700, 152 * 2 + 3, 64], 1024
     Ws = [dev(W) for W in _mats(fmt, rows_list, K, seed=11 + fmt)]
     x = dev(synth.draw_act(np.random.default_rng(3), ncols, K, outlier_frac=0.001))
     ws = torch.empty(qb.q_matvec_workspace_bytes(fmt, K, ncols) + 16, dtype=torch.uint8, device="cuda")
