@@ -89,6 +89,17 @@ FP8 = {
 }
 
 
+# The 8B-class decode stack: a step is every product of one decode step --
+# 32 layers of QKV 6144x4096, O 4096x4096, gate+up 28672x4096, down 4096x14336
+# (Q4_K-like) and the 128256x4096 Q6_K-like output -- each from its f32
+# activation in one q_matvec call (name: columns)
+STACK = {"stack_8b_b1": 1, "stack_8b_b4": 4, "stack_8b_b16": 16}
+STACK_LAYERS = 32
+STACK_MATS = [("qkv", synth.FMT_Q4K, 6144, 4096), ("o", synth.FMT_Q4K, 4096, 4096),
+              ("gate_up", synth.FMT_Q4K, 28672, 4096), ("down", synth.FMT_Q4K, 4096, 14336)]
+STACK_OUT = ("output", synth.FMT_Q6K, 128256, 4096)
+
+
 def kernel_sources_sha() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "block_quantized_weight_quantize_gb300", "csrc")
@@ -782,6 +793,152 @@ def cpu_baseline(fmt, rows, K, ncols, Wh, x, wbytes, budget_s=10.0, sub32=False)
                       f"threads of the scalar C oracle"}
 
 
+def run_stack(args, rank, world):
+    """One step = the 129 products of an 8B-class decode step (every layer's
+    weights its own copy in HBM, 4.36 GB in all), each a q_matvec call from
+    its f32 activation; the first and the last take host buffers
+    (q_matvec_host), so the step runs from a host activation to host logits."""
+    import torch
+    import block_quantized_weight_quantize_gb300 as qb
+
+    ncols = STACK[args.workload]
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    rng = np.random.default_rng(9 + 1000 * rank)
+    mats = []  # (name, fmt, rows, K, device weights per layer)
+    for name, fmt, rows, K in STACK_MATS:
+        Wh = synth.pack(fmt, synth.draw(fmt, rng, rows, K))
+        w0 = torch.from_numpy(Wh).to(dev)
+        layers = [w0] + [w0.clone() for _ in range(STACK_LAYERS - 1)]
+        mats.append((name, fmt, rows, K, layers))
+        del Wh
+    oname, ofmt, orows, oK = STACK_OUT
+    part = orows // 8  # drawn once, tiled 8 times on the device
+    Wo = synth.pack(ofmt, synth.draw(ofmt, rng, part, oK))
+    wo = torch.empty(orows * synth.record_bytes(ofmt, oK), dtype=torch.uint8, device=dev)
+    for i in range(8):
+        wo[i * Wo.size:(i + 1) * Wo.size].copy_(torch.from_numpy(Wo))
+    del Wo
+    wbytes = sum(synth.weight_bytes(f, r, k) for _, f, r, k in STACK_MATS) * STACK_LAYERS + \
+        synth.weight_bytes(ofmt, orows, oK)
+    xs = {k: torch.from_numpy(synth.draw_act(rng, ncols, k)).to(dev) for k in (4096, 14336)}
+    outs = {name: torch.empty((ncols, rows), dtype=torch.float32, device=dev) for name, _, rows, _, _ in mats}
+    logits = torch.empty((ncols, orows), dtype=torch.float32, device=dev)
+    wsb = max(qb.q_matvec_workspace_bytes(f, k, ncols) for _, f, _, k in STACK_MATS + [STACK_OUT])
+    ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(dev)
+    launches_per_call = 1 if ncols == 1 else 2
+
+    def step(i, s):
+        for layer in range(STACK_LAYERS):
+            for name, fmt, rows, K, layers in mats:
+                qb.q_matvec(fmt, layers[layer], rows, K, xs[K], outs[name], workspace=ws, stream=s)
+        qb.q_matvec(ofmt, wo, orows, oK, xs[oK], logits, workspace=ws, stream=s)
+
+    with torch.cuda.stream(stream):
+        step(0, stream)
+    stream.synchronize()
+    G = max(1, min(args.steps, 5))
+
+    def capture(fn, n):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            g.capture_begin()
+            for i in range(n):
+                fn(i, stream)
+            g.capture_end()
+        return g
+
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    g_main = capture(step, G)
+    with torch.cuda.stream(stream):
+        for _ in range(max(1, -(-args.warmup // G))):
+            g_main.replay()
+    stream.synchronize()
+    nrep = max(1, args.steps // G)
+    with ClockSampler(dev.index) as clk:
+        barrier()
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(nrep):
+                g_main.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+    ms = max_over_ranks(e0.elapsed_time(e1), dev) / (nrep * G)
+    clocks = clk.summary()
+    # e2e: host activation in (the first call), host logits out (the last)
+    xh = torch.from_numpy(synth.draw_act(np.random.default_rng(10), ncols, 4096)).pin_memory()
+    lh = torch.empty((ncols, orows), dtype=torch.float32).pin_memory()
+    f0, r0, k0 = mats[0][1], mats[0][2], mats[0][3]
+    wsh0 = torch.empty(qb.q_matvec_host_workspace_bytes(qb.PERBLOCK, f0, r0, k0, ncols), dtype=torch.uint8, device=dev)
+    wsh1 = torch.empty(qb.q_matvec_host_workspace_bytes(qb.PERBLOCK, ofmt, orows, oK, ncols), dtype=torch.uint8,
+                       device=dev)
+
+    qkv_host = torch.empty((ncols, mats[0][2]), dtype=torch.float32).pin_memory()
+
+    def host_step():
+        for layer in range(STACK_LAYERS):
+            for j, (name, fmt, rows, K, layers) in enumerate(mats):
+                if layer == 0 and j == 0:  # the step's input arrives from the host
+                    qb.q_matvec_host(fmt, layers[0], rows, K, xh, qkv_host, wsh0, stream=stream)
+                else:
+                    qb.q_matvec(fmt, layers[layer], rows, K, xs[K], outs[name], workspace=ws, stream=stream)
+        qb.q_matvec_host(ofmt, wo, orows, oK, xh, lh, wsh1, stream=stream)  # logits back to the host
+
+    host_step()
+    stream.synchronize()
+    n_e2e = max(3, min(args.steps, 20))
+    barrier()
+    t0 = time.perf_counter()
+    for _ in range(n_e2e):
+        host_step()
+    stream.synchronize()
+    e2e_s = max_over_ranks(time.perf_counter() - t0, dev)
+    assert qb.q_device_status() == qb.QB_OK
+    step_s = ms / 1e3
+    value = world * wbytes / step_s / 1e9
+    peak, peak_kind = measured_peaks()
+    nrows = sum(r for _, _, r, _ in STACK_MATS) * STACK_LAYERS + orows
+    ops = 2 * ncols * (sum(r * k for _, _, r, k in STACK_MATS) * STACK_LAYERS + orows * oK)
+    res = {
+        "metric": f"weight GB/s (8B-class decode stack, {ncols} column(s): 32 layers of Q4_K-like QKV 6144x4096, "
+                  f"O 4096x4096, gate+up 28672x4096, down 4096x14336 + Q6_K-like output 128256x4096)",
+        "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": nrep * G, "warmup": args.warmup,
+        "ms_per_step": round(ms, 6), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "int8 codes x int8 codes, exact int32/int64, f32 rounding",
+        "data": "synthetic (seeded PCG64; the formats' code/scale distributions; one drawn copy per matrix shape, "
+                "each layer its own device copy, the output matrix drawn as 1/8 and tiled); no trained weights",
+        "config": {"workload": f"8B-class decode stack, {ncols} column(s)", "layers": STACK_LAYERS,
+                   "matrices": [[n, synth.FORMAT_NAMES[f], r, k] for n, f, r, k in STACK_MATS + [STACK_OUT]],
+                   "ncols": ncols, "weight_bytes_per_step": wbytes,
+                   "l2": "every layer reads its own weights (4.36 GB a step, 34x L2); no flush",
+                   "timing": f"CUDA graphs of {G} steps ({(4 * STACK_LAYERS + 1) * launches_per_call} launches a step, "
+                             f"programmatic dependent launch); CUDA events",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "rows_per_s": round(world * nrows / step_s, 1), "tokens_per_s": round(world * ncols / step_s, 1),
+        "tops": round(world * ops / step_s / 1e12, 3),
+        "frac_of_8tbs": round(value / 8000.0, 4), "frac_of_measured_copy": round(value / peak, 4),
+        "gpu_launches": nrep * G * (4 * STACK_LAYERS + 1) * launches_per_call, "clocks": clocks,
+        "roofline": {"bound": "hbm" if ncols == 1 else "alu", "kernel": "the step's 129 products (one-column "
+                     "streaming kernels at 1 column; dp4a / f16 tensor-core kernels at 4 and 16)",
+                     "achieved": round(value, 1) if ncols == 1 else round(ops / step_s / 1e12, 2),
+                     "peak": peak if ncols == 1 else round(DP4A_PEAK_TOPS, 1),
+                     "peak_kind": f"{peak_kind} (HBM copy, burst)" if ncols == 1 else
+                                  "dp4a issue rate from unit counts and the maximum clock",
+                     "unit": "GB/s" if ncols == 1 else "TOPS",
+                     "frac": round(value / peak, 4) if ncols == 1 else round(ops / step_s / 1e12 / DP4A_PEAK_TOPS, 4),
+                     "traffic": None, "algorithmic_bytes_per_step": wbytes},
+        "e2e": {"value": round(world * wbytes * n_e2e / e2e_s / 1e9, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": int(xh.numel() * 4), "d2h_bytes_per_step": int(lh.numel() * 4),
+                "steps": n_e2e, "how": "per step the 129 calls through the binding, the first (QKV) and the last "
+                "(output) q_matvec_host with pinned host buffers; host wall clock"},
+    }
+    return res
+
+
 def _fp8_inputs(rows, K, ncols, seed):
     rng = np.random.default_rng(seed)
     W = rng.integers(0, 256, size=(rows, K), dtype=np.uint8)
@@ -1068,7 +1225,7 @@ def main():
     ap.add_argument("--steps", type=int, default=100000)
     ap.add_argument("--warmup", type=int, default=1000)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="q4k_4096x4096", choices=sorted(WORKLOADS) + sorted(GROUPED) + sorted(KV) + sorted(FP8))
+    ap.add_argument("--workload", default="q4k_4096x4096", choices=sorted(WORKLOADS) + sorted(GROUPED) + sorted(KV) + sorted(FP8) + sorted(STACK))
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--roof-launches", type=int, default=2000,
@@ -1086,6 +1243,10 @@ def main():
                 print(json.dumps(run_kv_reference(args)), flush=True)
             elif args.workload in FP8:
                 print(json.dumps(run_fp8_reference(args)), flush=True)
+            elif args.workload in STACK:
+                print(json.dumps({"impl": "reference", "unavailable": "the reference arm times single-matrix "
+                                  "workloads; the 8B-class stack (4.36 GB a step) has no oracle timing"}),
+                      flush=True)
             else:
                 print(json.dumps(run_reference(args)), flush=True)
         return
@@ -1095,6 +1256,7 @@ def main():
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
         tdist.init_process_group("nccl")
     res = (run_grouped(args, rank, world) if args.workload in GROUPED else
+           run_stack(args, rank, world) if args.workload in STACK else
            run_kv(args, rank, world) if args.workload in KV else
            run_fp8(args, rank, world) if args.workload in FP8 else run_ours(args, rank, world))
     if rank == 0:
