@@ -229,12 +229,12 @@ def one_col_gemv3(fmt, rows, K):
 
 
 def one_col_gemv6(fmt, rows, K):
-    """The library's rule for the warp-ring one-column kernel: 256-element
-    formats, K = 4096, at most 32 rows a CTA over min(152, rows/2) CTAs."""
-    if fmt == synth.FMT_Q8_0 or K != 4096 or rows < 1:
+    """The library's rule for the warp-ring one-column kernel: K = 4096, every
+    Q6_K-like shape, Q4_K-like ones up to 48 rows a CTA over min(152, rows/2) CTAs."""
+    if fmt not in (synth.FMT_Q4K, synth.FMT_Q6K) or K != 4096 or rows < 1:
         return False
     g = max(1, min(152, (rows + 1) // 2))
-    return (rows + g - 1) // g <= 32
+    return fmt == synth.FMT_Q6K or (rows + g - 1) // g <= 48
 
 
 def roofline(fmt, ncols, single, achieved, peak, peak_kind, traffic, roof_bytes, per_launch_s, prod_s, abytes,

@@ -190,12 +190,13 @@ __global__ void __launch_bounds__(512, 1) gemv6_kernel(const Gemv6K p) {
 }
 
 // The kernel for one column of a Q4_K-like or Q6_K-like matrix (or a table of
-// them) at K = 4096 where every warp has at most one row pair (up to 32 rows
-// a CTA: there it measured faster than the other streaming kernels -- 4096
-// rows, Q4_K-like 3.95 -> 3.84 us and Q6_K-like 4.70 -> 4.56 us for the
-// single launch, 3.59 -> 3.35 and 4.58 -> 3.77 us with the activation
-// quantized beforehand; with more rows a CTA they were as fast or faster);
-// x given: the single-launch form.  QB_E_ARG otherwise.
+// them) at K = 4096: every Q6_K-like shape, and Q4_K-like ones up to 48 rows a
+// CTA, where it measured faster than the other streaming kernels (single
+// launch: Q4_K-like 4096 rows 3.95 -> 3.84 us, 6144 rows 5.50 -> 5.23 us;
+// Q6_K-like 4096 rows 4.70 -> 4.56 us, 128256 rows 82.0 -> 65.7 us); the
+// one-column gemv3 form stayed faster for Q4_K-like at 14336 and 28672 rows
+// (7.9 against 8.6 us, 13.3 against 14.0 us).  x given: the single-launch
+// form.  QB_E_ARG otherwise.
 template <int F>
 int launch_gemv6(const GemvArgs &a, cudaStream_t stream, const float *x) {
     if ((F != kQ4K && F != kQ6K) || a.ncols != 1 || a.mode != 0 || a.K != kG6K) return QB_E_ARG;
@@ -205,13 +206,13 @@ int launch_gemv6(const GemvArgs &a, cudaStream_t stream, const float *x) {
     if (k.rows < 1) return QB_E_ARG;
     {
         const int64_t g = std::max<int64_t>(1, std::min<int64_t>(num_sms(), (k.rows + 1) / 2));
-        if ((k.rows + g - 1) / g > 2 * kG6Warps) return QB_E_ARG;  // more than one pair a warp
+        if (F == kQ4K && (k.rows + g - 1) / g > 3 * kG6Warps) return QB_E_ARG;  // more than 48 rows a CTA
     }
     k.rec = (int)record_bytes(F, kG6K);
     const int budget = 225 * 1024;
     k.D = 1;
     while (k.D < 4 && gemv6_smem(k.rec, k.D + 1) <= budget) ++k.D;
-    if (k.D < 2) return QB_E_ARG;
+    if (k.D < 2) return QB_E_ARG;  // two slots a warp at least (Q4_K-like: 3, Q6_K-like: 2)
     const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(num_sms(), (k.rows + 1) / 2));
     k.base = k.rows / grid;
     k.rem = k.rows % grid;

@@ -11,7 +11,7 @@ int launch_skinny<kQ6K>(const GemvArgs &a, cudaStream_t stream) {
 }
 template <>
 int launch_one_col3<kQ6K>(const GemvArgs &a, cudaStream_t stream, const float *x) {
-    const int r6 = launch_gemv6<kQ6K>(a, stream, x);  // K = 4096, up to one row pair a warp
+    const int r6 = launch_gemv6<kQ6K>(a, stream, x);  // K = 4096 (qb_gemv6.cuh: which shapes)
     if (r6 != QB_E_ARG) return r6;
     return launch_gemv3_one<kQ6K>(a, stream, x);
 }
