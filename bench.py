@@ -68,6 +68,15 @@ GROUPED = {
 }
 
 
+# A Q6_K-like FFN block at batch 1: gate and up (14336x4096) from one shared
+# activation in one grouped call, then down (4096x14336) from its own
+# activation (q_matvec_many + q_matvec a step):
+# name: (fmt, gate/up rows, K, down rows, seed, description)
+FFN = {
+    "q6k_ffn_14336x4096": (synth.FMT_Q6K, 14336, 4096, 4096, 2,
+                           "Q6_K-like FFN: gate + up 14336x4096 (one grouped call) and down 4096x14336, batch 1"),
+}
+
 # The int8 cache's score path: query heads quantized, then scored against the
 # cached key rows (kv_quantize_heads + kv_scores a step):
 # name: (scaling, query heads, key heads, head size, cached positions, seed, description)
@@ -793,6 +802,198 @@ def cpu_baseline(fmt, rows, K, ncols, Wh, x, wbytes, budget_s=10.0, sub32=False)
                       f"threads of the scalar C oracle"}
 
 
+def _ffn_host(rng_seed):
+    """The FFN workload's three matrices and two activations, drawn on the host."""
+    fmt, rows, K, drows, seed, desc = FFN["q6k_ffn_14336x4096"]
+    rng = np.random.default_rng(rng_seed)
+    Ws = [synth.pack(fmt, synth.draw(fmt, rng, r, k)) for r, k in ((rows, K), (rows, K), (drows, rows))]
+    x = synth.draw_act(rng, 1, K)
+    h = synth.draw_act(rng, 1, rows)
+    return fmt, rows, K, drows, desc, Ws, x, h
+
+
+def ffn_oracle_pass(fmt, rows, K, drows, Ws, x, h, n, frac=1.0):
+    """The oracle over the FFN step: gate and up from x, down from h (a
+    fraction of each matrix's rows when frac < 1)."""
+    for W, r, k, a in ((Ws[0], rows, K, x), (Ws[1], rows, K, x), (Ws[2], drows, rows, h)):
+        oracle_pass(fmt, r, k, W, a, n, row_limit=max(1, int(r * frac)))
+
+
+def run_ffn(args, rank, world):
+    """A step is the FFN block: q_matvec_many over gate and up (one launch),
+    then q_matvec of down (K = 14336); the two calls are also timed alone."""
+    import torch
+    import block_quantized_weight_quantize_gb300 as qb
+
+    fmt, rows, K, drows, desc, Ws, x, h = _ffn_host(2 + 1000 * rank)
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    sizes = [W.size for W in Ws]
+    wbytes = int(sum(sizes))
+    ncopy = max(2, -(-4 * L2_BYTES // wbytes))
+    bufs = [[torch.from_numpy(W).to(dev) for W in Ws]]
+    for _ in range(1, ncopy):
+        bufs.append([w.clone() for w in bufs[0]])
+    xd = torch.from_numpy(x).to(dev)
+    hd = torch.from_numpy(h).to(dev)
+    og = torch.empty((1, rows), dtype=torch.float32, device=dev)
+    ou = torch.empty((1, rows), dtype=torch.float32, device=dev)
+    od = torch.empty((1, drows), dtype=torch.float32, device=dev)
+    ws = torch.empty(max(qb.q_matvec_workspace_bytes(fmt, k, 1) for k in (K, rows)), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(dev)
+
+    def gate_up(i, s):
+        b = bufs[i % ncopy]
+        qb.q_matvec_many(fmt, [b[0], b[1]], [rows, rows], K, xd, [og, ou], workspace=ws, stream=s)
+
+    def down(i, s):
+        qb.q_matvec(fmt, bufs[i % ncopy][2], drows, rows, hd, od, workspace=ws, stream=s)
+
+    def step(i, s):
+        gate_up(i, s)
+        down(i, s)
+
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            step(i, stream)
+    stream.synchronize()
+    G = min(args.steps, 500)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+
+    def time_graph(fn, steps, clocks=False):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            g.capture_begin()
+            for i in range(G):
+                fn(i, stream)
+            g.capture_end()
+        with torch.cuda.stream(stream):
+            for _ in range(max(1, -(-args.warmup // G))):
+                g.replay()
+        stream.synchronize()
+        sampler = ClockSampler(dev.index) if clocks else None
+        if sampler:
+            sampler.__enter__()
+        barrier()
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(max(1, steps // G)):
+                g.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        if sampler:
+            sampler.__exit__(None, None, None)
+        return max_over_ranks(e0.elapsed_time(e1), dev) / (max(1, steps // G) * G), \
+            (sampler.summary() if sampler else None)
+
+    ms, clocks = time_graph(step, args.steps, clocks=True)
+    ms_gu, _ = time_graph(gate_up, min(args.steps, 20000))
+    ms_dn, _ = time_graph(down, min(args.steps, 20000))
+    # e2e: pinned x and h in, the three outputs back, a step's calls through the binding
+    xh = torch.from_numpy(x).pin_memory()
+    hh = torch.from_numpy(h).pin_memory()
+    ohs = [torch.empty((1, r), dtype=torch.float32).pin_memory() for r in (rows, rows, drows)]
+    n_e2e = min(args.steps, 2000)
+    barrier()
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for i in range(n_e2e):
+            xd.copy_(xh, non_blocking=True)
+            hd.copy_(hh, non_blocking=True)
+            step(i, stream)
+            for oh, o in zip(ohs, (og, ou, od)):
+                oh.copy_(o, non_blocking=True)
+    stream.synchronize()
+    e2e_s = max_over_ranks(time.perf_counter() - t0, dev)
+    assert qb.q_device_status() == qb.QB_OK
+    step_s = ms / 1e3
+    value = world * wbytes / step_s / 1e9
+    peak, peak_kind = measured_peaks()
+    gu_bytes = sizes[0] + sizes[1] + 4 * K + 8 * rows
+    two = False  # Q6_K-like down: the single-launch form (q_matvec's rule)
+    res = {
+        "metric": f"weight GB/s ({desc})",
+        "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": max(1, args.steps // G) * G,
+        "warmup": args.warmup, "ms_per_step": round(ms, 6), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "int8 codes x int8 codes, exact int32/int64, f32 rounding",
+        "data": "synthetic (seeded PCG64; the format's code/scale distributions); no trained weights",
+        "config": {"workload": desc, "gate_up_rows": [rows, rows], "K": K, "down": [drows, rows], "ncols": 1,
+                   "format": synth.FORMAT_NAMES[fmt], "weight_bytes_per_step": wbytes,
+                   "l2": f"each step reads a different one of {ncopy} copies of the three matrices "
+                         f"({ncopy * wbytes / 2**20:.0f} MiB > 4x L2); no flush",
+                   "timing": f"CUDA graphs of {G} steps (two launches a step, programmatic dependent launch); "
+                             f"CUDA events",
+                   "gate_up_ms": round(ms_gu, 6), "down_ms": round(ms_dn, 6),
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "rows_per_s": round(world * (2 * rows + drows) / step_s, 1),
+        "frac_of_8tbs": round(value / 8000.0, 4), "frac_of_measured_copy": round(value / peak, 4),
+        "gpu_launches": max(1, args.steps // G) * G * (3 if two else 2), "clocks": clocks,
+        "roofline": {"bound": "hbm",
+                     "kernel": "gemv6_kernel<q6k, one column, single launch, grouped> (gate + up, 28672 rows)",
+                     "achieved": round(gu_bytes / (ms_gu / 1e3) / 1e9, 1), "peak": peak,
+                     "peak_kind": f"{peak_kind} (HBM copy, burst)", "unit": "GB/s",
+                     "frac": round(gu_bytes / (ms_gu / 1e3) / 1e9 / peak, 4), "traffic": traffic_for(args.workload),
+                     "algorithmic_bytes_per_launch": gu_bytes, "avg_launch_us": round(ms_gu * 1e3, 4),
+                     "down_kernel": "gemv3_kernel<q6k, one column, single launch> (4096 x 14336)",
+                     "down_achieved": round((sizes[2] + 4 * rows + 4 * drows) / (ms_dn / 1e3) / 1e9, 1)},
+        "e2e": {"value": round(world * wbytes * n_e2e / e2e_s / 1e9, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": int(x.nbytes + h.nbytes), "d2h_bytes_per_step": int(4 * (2 * rows + drows)),
+                "steps": n_e2e,
+                "how": "per step: pinned x and h -> device, q_matvec_many + q_matvec through the Python binding, "
+                       "the three outputs -> pinned host; host wall clock over all steps"},
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        n = _oracle_threads()
+        ffn_oracle_pass(fmt, rows, K, drows, Ws, x, h, n)
+        reps, t0 = 0, time.perf_counter()
+        while True:
+            ffn_oracle_pass(fmt, rows, K, drows, Ws, x, h, n)
+            reps += 1
+            el = time.perf_counter() - t0
+            if el >= args.cpu_seconds:
+                break
+        res["cpu_baseline"] = {"value": round(wbytes * reps / el / 1e9, 4), "unit": "GB/s", "cores": n,
+                               "kind": "oracle",
+                               "sample": f"{reps} full FFN steps (quantize x and h, all rows of gate, up and down) "
+                                         f"in {el:.1f} s, rows split over {n} threads of the scalar C oracle"}
+    return res
+
+
+def run_ffn_reference(args):
+    """The reference arm on the FFN workload: the oracle over whole FFN steps."""
+    fmt, rows, K, drows, desc, Ws, x, h = _ffn_host(2)
+    wbytes = int(sum(W.size for W in Ws))
+    n = _oracle_threads()
+    t0 = time.perf_counter()
+    ffn_oracle_pass(fmt, rows, K, drows, Ws, x, h, n)
+    full = time.perf_counter() - t0
+    frac = max(1e-4, min(1.0, (100.0 / max(1, args.steps + args.warmup)) / max(full, 1e-6)))
+    for _ in range(args.warmup):
+        ffn_oracle_pass(fmt, rows, K, drows, Ws, x, h, n, frac)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        ffn_oracle_pass(fmt, rows, K, drows, Ws, x, h, n, frac)
+    el = time.perf_counter() - t0
+    done = sum(synth.record_bytes(fmt, k) * max(1, int(r * frac)) for r, k in ((rows, K), (rows, K), (drows, rows)))
+    value = done * args.steps / el / 1e9
+    sample = (f"each step: quantize x and h + {frac:.3g} of the rows of gate, up and down, split over {n} threads "
+              f"of the scalar C oracle")
+    return {
+        "impl": "reference", "metric": f"weight GB/s ({desc})",
+        "value": round(value, 4), "unit": "GB/s", "n_gpus": 0, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(el * 1e3 / args.steps, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "int64/int128 exact, f32 rounding (scalar C)",
+        "data": "synthetic (seeded PCG64)",
+        "config": {"workload": desc, "gate_up_rows": [rows, rows], "K": K, "down": [drows, rows], "ncols": 1,
+                   "weight_bytes_per_step": wbytes},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": n, "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
 def run_stack(args, rank, world):
     """One step = the 129 products of an 8B-class decode step (every layer's
     weights its own copy in HBM, 4.36 GB in all), each a q_matvec call from
@@ -827,7 +1028,10 @@ def run_stack(args, rank, world):
     wsb = max(qb.q_matvec_workspace_bytes(f, k, ncols) for _, f, _, k in STACK_MATS + [STACK_OUT])
     ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
     stream = torch.cuda.Stream(dev)
-    launches_per_call = 1 if ncols == 1 else 2
+    # q_matvec launches a call: one for a single column, except Q4_K-like at
+    # K >= 12288 given a workspace (quantize, then the product), two otherwise
+    calls = [(f, k) for _, f, _, k in STACK_MATS] * STACK_LAYERS + [(STACK_OUT[1], STACK_OUT[3])]
+    launches_step = sum(1 if ncols == 1 and not (f == synth.FMT_Q4K and k >= 12288) else 2 for f, k in calls)
 
     def step(i, s):
         for layer in range(STACK_LAYERS):
@@ -915,13 +1119,13 @@ def run_stack(args, rank, world):
                    "matrices": [[n, synth.FORMAT_NAMES[f], r, k] for n, f, r, k in STACK_MATS + [STACK_OUT]],
                    "ncols": ncols, "weight_bytes_per_step": wbytes,
                    "l2": "every layer reads its own weights (4.36 GB a step, 34x L2); no flush",
-                   "timing": f"CUDA graphs of {G} steps ({(4 * STACK_LAYERS + 1) * launches_per_call} launches a step, "
+                   "timing": f"CUDA graphs of {G} steps ({launches_step} launches a step, "
                              f"programmatic dependent launch); CUDA events",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "rows_per_s": round(world * nrows / step_s, 1), "tokens_per_s": round(world * ncols / step_s, 1),
         "tops": round(world * ops / step_s / 1e12, 3),
         "frac_of_8tbs": round(value / 8000.0, 4), "frac_of_measured_copy": round(value / peak, 4),
-        "gpu_launches": nrep * G * (4 * STACK_LAYERS + 1) * launches_per_call, "clocks": clocks,
+        "gpu_launches": nrep * G * launches_step, "clocks": clocks,
         "roofline": {"bound": "hbm" if ncols == 1 else "alu", "kernel": "the step's 129 products (one-column "
                      "streaming kernels at 1 column; dp4a / f16 tensor-core kernels at 4 and 16)",
                      "achieved": round(value, 1) if ncols == 1 else round(ops / step_s / 1e12, 2),
@@ -1225,7 +1429,8 @@ def main():
     ap.add_argument("--steps", type=int, default=100000)
     ap.add_argument("--warmup", type=int, default=1000)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="q4k_4096x4096", choices=sorted(WORKLOADS) + sorted(GROUPED) + sorted(KV) + sorted(FP8) + sorted(STACK))
+    ap.add_argument("--workload", default="q4k_4096x4096", choices=sorted(WORKLOADS) + sorted(GROUPED) + sorted(FFN) + sorted(KV) + sorted(FP8) +
+                    sorted(STACK))
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--roof-launches", type=int, default=2000,
@@ -1239,6 +1444,8 @@ def main():
             if args.workload in GROUPED:
                 print(json.dumps({"impl": "reference", "unavailable": "the reference arm times single-matrix "
                                   "workloads; the grouped workload has no oracle timing"}), flush=True)
+            elif args.workload in FFN:
+                print(json.dumps(run_ffn_reference(args)), flush=True)
             elif args.workload in KV:
                 print(json.dumps(run_kv_reference(args)), flush=True)
             elif args.workload in FP8:
@@ -1257,6 +1464,7 @@ def main():
         tdist.init_process_group("nccl")
     res = (run_grouped(args, rank, world) if args.workload in GROUPED else
            run_stack(args, rank, world) if args.workload in STACK else
+           run_ffn(args, rank, world) if args.workload in FFN else
            run_kv(args, rank, world) if args.workload in KV else
            run_fp8(args, rank, world) if args.workload in FP8 else run_ours(args, rank, world))
     if rank == 0:

@@ -255,7 +255,14 @@ int q_matvec(qb_fmt fmt, const void *W, int64_t rows, int64_t K, const float *x,
         if (rows == 0) return QB_OK;
         if (K == 0)
             return cudaMemsetAsync(out, 0, (size_t)ncols * rows * sizeof(float), s) == cudaSuccess ? QB_OK : QB_E_CUDA;
-        if (ncols == 1) {
+        // Q4_K-like rows of K >= 12288 with a workspace at hand: quantize_act and
+        // the product as two launches measured faster than quantizing the long
+        // activation inside every CTA of the single-launch kernel (4096 x 14336:
+        // 10.7 against 12.0 us; Q6_K-like there, and every K = 4096 shape, the
+        // other way round).
+        const bool two = f == kQ4K && K >= 12288 && workspace && (int64_t)workspace_bytes >= need &&
+                         !misaligned(workspace);
+        if (ncols == 1 && !two) {
             GemvArgs a = {};
             a.W = W; a.rows = rows; a.K = K; a.ncols = 1; a.out = out; a.mode = 0;
             const int r = f == kQ8_0 ? launch_matvec_q8_0(a, x, s)

@@ -136,7 +136,8 @@ QB_API int64_t q_matvec_workspace_bytes(qb_fmt fmt, int64_t K, int ncols);
  * K % 256 == 0, and for F16 with ncols * K * 4 <= 227 KB (rows short enough
  * for the F16 kernel's rings), it is a single launch that quantizes (or
  * rounds) the activation inside the product kernel and needs no workspace
- * (`workspace` may be NULL); otherwise
+ * (`workspace` may be NULL; a Q4_K matrix with K >= 12288 given a workspace
+ * takes the two launches, measured faster there); otherwise
  * `workspace` must be device memory of at least q_matvec_workspace_bytes()
  * bytes, 16-byte aligned, owned by the caller and not used by another call
  * while this one runs.  x must be 16-byte aligned. */

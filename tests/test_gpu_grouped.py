@@ -57,7 +57,7 @@ def _dev_w(Wh):
 @pytest.mark.parametrize("fmt", FMTS)
 @pytest.mark.parametrize("ncols", [1, 3, 16])
 @pytest.mark.parametrize("rows_list,K", [([300, 77, 0, 129], 2048), ([4096, 1024, 1024], 4096), ([5, 3], 256),
-                                         ([1001, 2000, 513], 4096)])
+                                         ([1001, 2000, 513], 4096), ([333, 21, 150], 14336)])
 def test_gemv_many_bit_exact(fmt, ncols, rows_list, K):
     import torch
     Ws = _mats(fmt, rows_list, K, seed=sum(rows_list) + ncols + fmt)
@@ -79,11 +79,13 @@ def test_gemv_many_bit_exact(fmt, ncols, rows_list, K):
 
 @pytest.mark.parametrize("fmt", FMTS)
 @pytest.mark.parametrize("ncols", [1, 3])
-@pytest.mark.parametrize("rows_list,K", [([700, 152 * 2 + 3, 64], 1024), ([1001, 2000, 513], 4096)])
+@pytest.mark.parametrize("rows_list,K", [([700, 152 * 2 + 3, 64], 1024), ([1001, 2000, 513], 4096),
+                                         ([1001, 20, 513], 14336), ([77, 130], 10240)])
 def test_matvec_many_matches_separate_calls(fmt, ncols, rows_list, K):
     """q_matvec_many (one launch for one column) against q_matvec per matrix;
-    at K = 4096 the group is under 33 rows a CTA (the warp-ring one-column
-    kernel), with matrix boundaries inside row pairs."""
+    the warp-ring one-column kernel takes K = 4096 (under 49 rows a CTA),
+    10240 and 14336 (rows in passes, the last one partial), with matrix
+    boundaries inside row pairs."""
     import torch
     Ws = [dev(W) for W in _mats(fmt, rows_list, K, seed=11 + fmt)]
     x = dev(synth.draw_act(np.random.default_rng(3), ncols, K, outlier_frac=0.001))

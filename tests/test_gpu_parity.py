@@ -431,6 +431,33 @@ def test_matvec_bit_exact(fmt, ncols, rows, K):
             qb.q_matvec(fmt, dev(W), rows, K, dev(x), out, workspace=None)
 
 
+@pytest.mark.parametrize("fmt", [synth.FMT_Q4K, synth.FMT_Q6K])
+@pytest.mark.parametrize("rows,K", [(307, 8192), (157, 10240), (2 * 152 + 3, 14336), (95, 16384), (3, 14336),
+                                    (4096, 14336)])
+def test_one_column_long_rows(fmt, rows, K):
+    """One column at K = 8192 .. 16384 (the down projection's 14336 among them):
+    rows streamed in passes of 16 blocks, the last pass partial at 10240 and
+    14336 (8 blocks), CTAs with an odd row count; both the product from a
+    quantized activation and the single-launch q_matvec equal the oracle."""
+    import torch
+    rng = np.random.default_rng(rows + K + fmt)
+    W = synth.pack(fmt, synth.draw(fmt, rng, rows, K))
+    x = synth.draw_act(rng, 1, K, outlier_frac=0.001)
+    x[0, 5 * 256:6 * 256] = 0.0                                 # a zero block
+    codes, m, e, s16, packed = oracle_act(x, 256)
+    want = oracle.gemv(fmt, W, rows, K, codes, m, e)
+    act = qb.alloc_act(1, K, 256)
+    qb.quantize_act(256, dev(x), *act)
+    out = torch.full((1, rows), float("nan"), dtype=torch.float32, device="cuda")
+    qb.q_gemv(fmt, dev(W), rows, K, act, 1, out)
+    torch.cuda.synchronize()
+    assert np.array_equal(bits(host(out)), bits(want))
+    out.fill_(float("nan"))
+    qb.q_matvec(fmt, dev(W), rows, K, dev(x), out)
+    torch.cuda.synchronize()
+    assert np.array_equal(bits(host(out)), bits(want))
+
+
 def test_matvec_repeated_launches_graph():
     """Many single-launch products back to back (programmatic dependent launch
     overlapping each launch's weight stream with the previous one) on distinct
