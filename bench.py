@@ -13,8 +13,9 @@ L2, so every step streams its weights from HBM.
                   [--workload q4k_4096x4096|q8_0_512x1024|q6k_14336x4096|f16_49152x576|...]
 
 Workloads ending in _sub32 run the ActScaling::Sub32 product (activation
-scales per 32 elements, one rounding per 256-element group): quantize_act_sub32
-then q_gemv_sub32, two launches a step.
+scales per 32 elements, one rounding per 256-element group) through
+q_matvec_sub32: one launch a step for one column (x quantized in the product
+kernel's prologue), quantize_act_sub32 then q_gemv_sub32 otherwise.
 
 Prints one JSON line.  --impl reference times the CPU oracle (test
 infrastructure; a deliberately plain scalar C program) on the host cores.
@@ -255,7 +256,8 @@ def roofline(fmt, ncols, single, achieved, peak, peak_kind, traffic, roof_bytes,
     name = (g6name if g6 else
             f"gemv_f16w_kernel<{ncols}{', single launch (f16 rounding in the prologue)' if single else ''}>"
             if fmt == synth.FMT_F16 else
-            f"s32_kernel<{synth.FORMAT_NAMES[fmt]}, {min(ncols, 2)} column(s) a thread group>" if sub32 else
+            (f"s32_kernel<{synth.FORMAT_NAMES[fmt]}, one column, single launch> (quantize + product)" if single
+             else f"s32_kernel<{synth.FORMAT_NAMES[fmt]}, {min(ncols, 2)} column(s) a thread group>") if sub32 else
             f"gemv3_kernel<{synth.FORMAT_NAMES[fmt]}, one column, single launch> (quantize + product)"
             if single and g3 else
             f"gemv2_kernel<{synth.FORMAT_NAMES[fmt]}, single launch> (quantize + product)" if single else
@@ -582,7 +584,10 @@ def run_ours(args, rank, world):
     ws = torch.empty(qb.q_matvec_sub32_workspace_bytes(K, ncols) if sub32 else
                      qb.q_matvec_workspace_bytes(fmt, K, ncols), dtype=torch.uint8, device=dev)
     # one launch per step where the single-launch product applies, else two
-    single = ((fmt != synth.FMT_F16 and ncols == 1 and K % 256 == 0 and not sub32) or
+    # (Sub32 too: its one-column kernel quantizes x in its prologue; PerBlock
+    # Q4_K-like rows of K >= 12288 given a workspace take quantize + product)
+    single = ((fmt != synth.FMT_F16 and ncols == 1 and K % 256 == 0 and
+               (sub32 or not (fmt == synth.FMT_Q4K and K >= 12288))) or
               (fmt == synth.FMT_F16 and ncols * K * 4 <= 227 * 1024))
     launches_per_step = 1 if single else 2
     stream = torch.cuda.Stream(dev)

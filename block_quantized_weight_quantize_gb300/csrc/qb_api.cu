@@ -492,6 +492,23 @@ int q_matvec_sub32(qb_fmt fmt, const void *W, int64_t rows, int64_t K, const flo
     if (!x || misaligned(x)) return QB_E_ARG;
     const int64_t need = q_matvec_sub32_workspace_bytes(K, ncols);
     if (need < 0) return (int)need;
+    if (ncols == 1) {  // one launch where the streaming kernel takes the shape (x quantized in its prologue)
+        const qb_act probe = {32, reinterpret_cast<const int8_t *>(x), reinterpret_cast<const qb_scale *>(x),
+                              reinterpret_cast<const int16_t *>(x)};
+        const int rc = check_sub32_args(fmt, W, rows, K, &probe, ncols, out);
+        if (rc) return rc;
+        if (rows == 0) return QB_OK;
+        if (K > 0) {
+            GemvArgs a = {};
+            a.W = W; a.rows = rows; a.K = K; a.ncols = 1; a.out = out; a.mode = 0;
+            cudaStream_t s = static_cast<cudaStream_t>(stream);
+            const int f = fmt_index(fmt);
+            const int r = f == kQ8_0 ? launch_matvec_sub32_q8_0(a, x, s)
+                        : f == kQ4K  ? launch_matvec_sub32_q4k(a, x, s)
+                                     : launch_matvec_sub32_q6k(a, x, s);
+            if (r != QB_E_ARG) return r;
+        }
+    }
     if (!workspace || (int64_t)workspace_bytes < need || misaligned(workspace)) return QB_E_ARG;
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     qb_act act;

@@ -78,7 +78,8 @@ __host__ __device__ inline Gemv3Smem gemv3_smem(int K, int ncols, int rec, int n
 }
 
 // Q4_K-like half block h for CG columns: 16*C[c] and O[c] over sub-blocks
-// 4h..4h+3.  a[c][k] holds unit 8j+k of column c.
+// 4h..4h+3.  a[c][k] holds unit 8j+k of column c; S[c][0] the unit-pair sums
+// of sub-blocks 4h, 4h+1 as 16-bit halves, S[c][1] those of 4h+2, 4h+3.
 template <int CG>
 __device__ __forceinline__ void half_q4k_cg(const uint8_t *blk, int h, const uint4 (&a)[CG][8],
                                             const uint32_t (&S)[CG][4], int (&C)[CG], int (&O)[CG], uint32_t &dd) {
@@ -89,31 +90,33 @@ __device__ __forceinline__ void half_q4k_cg(const uint8_t *blk, int h, const uin
     const uint32_t scm = (uint32_t)(sc48 >> (24 * h)), mnm = (uint32_t)(mn48 >> (24 * h));
     const uint8_t *qs = blk + 16 + 64 * h;
 #pragma unroll
-    for (int c = 0; c < CG; ++c) { C[c] = 0; O[c] = 0; }
+    for (int c = 0; c < CG; ++c) C[c] = 0;
 #pragma unroll
     for (int s = 0; s < 4; ++s) {
         const uint4 w = *reinterpret_cast<const uint4 *>(qs + 16 * s);
-        // both nibbles as 16*q (the low one shifted up), so one chain of
-        // eight dp4a gives 16 * (the sub-block's sum); C is returned as 16*C
-        // (|16*C| <= 16 * 63 * 15 * 127 * 256 < 2^31 over a whole block)
-        const uint32_t l0 = (w.x << 4) & 0xF0F0F0F0u, l1 = (w.y << 4) & 0xF0F0F0F0u;
-        const uint32_t l2 = (w.z << 4) & 0xF0F0F0F0u, l3 = (w.w << 4) & 0xF0F0F0F0u;
+        // the low nibbles as q, the high ones as 16*q (masked in place): two
+        // chains of four dp4a, 16 * (the sub-block's sum) = 16 * pl + ph, so
+        // C is returned as 16*C (|16*C| <= 16 * 63 * 15 * 127 * 256 < 2^31)
+        const uint32_t l0 = w.x & 0x0F0F0F0Fu, l1 = w.y & 0x0F0F0F0Fu, l2 = w.z & 0x0F0F0F0Fu, l3 = w.w & 0x0F0F0F0Fu;
         const uint32_t g0 = w.x & 0xF0F0F0F0u, g1 = w.y & 0xF0F0F0F0u, g2 = w.z & 0xF0F0F0F0u, g3 = w.w & 0xF0F0F0F0u;
-        const int sc = (int)((scm >> (6 * s)) & 63u), mn = (int)((mnm >> (6 * s)) & 63u);
+        const int sc = (int)((scm >> (6 * s)) & 63u);
 #pragma unroll
         for (int c = 0; c < CG; ++c) {
-            int p = dp4a_us(l0, a[c][2 * s].x, 0);
-            p = dp4a_us(l1, a[c][2 * s].y, p);
-            p = dp4a_us(l2, a[c][2 * s].z, p);
-            p = dp4a_us(l3, a[c][2 * s].w, p);
-            p = dp4a_us(g0, a[c][2 * s + 1].x, p);
-            p = dp4a_us(g1, a[c][2 * s + 1].y, p);
-            p = dp4a_us(g2, a[c][2 * s + 1].z, p);
-            p = dp4a_us(g3, a[c][2 * s + 1].w, p);
-            C[c] += sc * p;
-            O[c] += mn * (int)(int16_t)((S[c][s >> 1] >> (16 * (s & 1))) & 0xFFFFu);
+            int pl = dp4a_ss(l0, a[c][2 * s].x, 0);
+            pl = dp4a_ss(l1, a[c][2 * s].y, pl);
+            pl = dp4a_ss(l2, a[c][2 * s].z, pl);
+            pl = dp4a_ss(l3, a[c][2 * s].w, pl);
+            int ph = dp4a_us(g0, a[c][2 * s + 1].x, 0);
+            ph = dp4a_us(g1, a[c][2 * s + 1].y, ph);
+            ph = dp4a_us(g2, a[c][2 * s + 1].z, ph);
+            ph = dp4a_us(g3, a[c][2 * s + 1].w, ph);
+            C[c] += sc * (16 * pl + ph);
         }
     }
+    // O = sum over the four sub-blocks of mn * (the sub-block's activation sum)
+    const uint32_t mnb = spread6(mnm);
+#pragma unroll
+    for (int c = 0; c < CG; ++c) O[c] = dp2a_hi_su(S[c][1], mnb, dp2a_lo_su(S[c][0], mnb, 0));
 }
 
 // Q6_K-like half block h (32-element chunks 4h..4h+3) for CG columns.
@@ -238,6 +241,9 @@ __global__ void __launch_bounds__(gemv3_threads<CG>(), 1)
     };
     if (tid == 0)
         for (int it = 0; it < p.D && it < p.n_iter; ++it) fill(it);  // weights depend on no earlier kernel
+    // the next launch may be scheduled now: it reads nothing this one writes
+    // before its own pdl_wait, which returns once this grid has finished
+    pdl_launch_dependents();
     pdl_wait();
 
     // ---- the activation codes of every column, once per CTA: coalesced
@@ -335,7 +341,6 @@ __global__ void __launch_bounds__(gemv3_threads<CG>(), 1)
         }
     }
     __syncthreads();
-    pdl_launch_dependents();
     // codes of half-slice j (Q4_K/Q6_K: a[c][k] = unit 8j+k; Q8_0: unit 8j + (k ^ jj))
 #pragma unroll
     for (int c = 0; c < CG; ++c) {

@@ -44,10 +44,10 @@ constexpr int kG6K = 4096;     // K this kernel takes
 constexpr int kG6Warps = 16;   // warps a CTA
 
 // shared memory: D mbarriers per warp, the staged activation (codes, unit
-// sums, block scales), then the warps' rings
-__host__ __device__ inline int gemv6_ring_offset() {
-    return 1024 + kG6K + (kG6K / 16) * 2 + (kG6K / 256) * 4 + 128;
-}
+// sums, block scales), each warp's 32 block values for the row fold, then the
+// warps' rings
+__host__ __device__ inline int gemv6_fold_offset() { return 1024 + kG6K + (kG6K / 16) * 2 + (kG6K / 256) * 4 + 128; }
+__host__ __device__ inline int gemv6_ring_offset() { return gemv6_fold_offset() + kG6Warps * 32 * 4; }
 __host__ __device__ inline int gemv6_smem(int rec, int D) { return gemv6_ring_offset() + kG6Warps * D * 2 * rec; }
 
 template <int F, bool FUSED>
@@ -60,6 +60,7 @@ __global__ void __launch_bounds__(512, 1) gemv6_kernel(const Gemv6K p) {
     int16_t *asum = reinterpret_cast<int16_t *>(smem + 1024 + kG6K);
     uint32_t *ascl = reinterpret_cast<uint32_t *>(smem + 1024 + kG6K + (kG6K / 16) * 2);
     uint8_t *ring = smem + gemv6_ring_offset() + (int64_t)w * p.D * 2 * p.rec;
+    float *fv = reinterpret_cast<float *>(smem + gemv6_fold_offset()) + 32 * w;
 
     const int64_t c = blockIdx.x;
     const int64_t row0 = c * p.base + (c < p.rem ? c : p.rem);
@@ -81,6 +82,9 @@ __global__ void __launch_bounds__(512, 1) gemv6_kernel(const Gemv6K p) {
         fill_rows(p.mt, ring + (int64_t)slot * 2 * p.rec, row0 + 2 * pi, n, p.rec, bars + slot);
     };
     for (int k = 0; k < p.D; ++k) fill(k);  // weights depend on no earlier kernel
+    // the next launch may be scheduled now: it reads nothing this one writes
+    // before its own pdl_wait, which returns once this grid has finished
+    pdl_launch_dependents();
     pdl_wait();
 
     // ---- the activation, once per CTA: codes in the multi-column kernel's
@@ -118,7 +122,6 @@ __global__ void __launch_bounds__(512, 1) gemv6_kernel(const Gemv6K p) {
         }
     }
     __syncthreads();
-    pdl_launch_dependents();
     // my half-slice's codes, unit sums and block scale
     uint4 a[1][8];
 #pragma unroll
@@ -178,14 +181,26 @@ __global__ void __launch_bounds__(512, 1) gemv6_kernel(const Gemv6K p) {
             v = (F == kQ4K) ? lane_value_fast<1>(C, O, dd & 0xFFFFu, dd >> 16, m0, e0)
                             : lane_value_fast<0>(C, 0, dd, 0, m0, e0);
         }
-        // fold: lane 0 adds row A's blocks (lanes 0, 2, ..., 30) in order, lane 1 row B's
-        float acc = 0.0f;
-#pragma unroll
-        for (int b = 0; b < kG6K / 256; ++b) acc = fadd_ftz(acc, __shfl_sync(0xFFFFFFFFu, v, 2 * b + (lane & 1)));
+        // fold: the block values go to the warp's strip, row A's 16 (lanes 0,
+        // 2, ..., 30) then row B's; lane 0 adds row A's in block order from
+        // +0, lane 1 row B's
+        fv[16 * h + sb] = v;
+        __syncwarp();
         if (lane < 2 && (lane == 0 || hasB)) {
+            const float4 *q4 = reinterpret_cast<const float4 *>(fv + 16 * lane);
+            float acc = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float4 t = q4[i];
+                acc = fadd_ftz(acc, t.x);
+                acc = fadd_ftz(acc, t.y);
+                acc = fadd_ftz(acc, t.z);
+                acc = fadd_ftz(acc, t.w);
+            }
             if (acc != acc) acc = __uint_as_float(kEngineNaN);
             *out_ptr(p.mt, 0, row0 + 2 * pi + lane) = acc;
         }
+        __syncwarp();  // the strip is read before the next pair writes it
     }
 }
 

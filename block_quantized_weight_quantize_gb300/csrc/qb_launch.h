@@ -82,6 +82,10 @@ int launch_gemv_q6k(const GemvArgs &a, cudaStream_t stream);
 int launch_gemv_sub32_q8_0(const GemvArgs &a, cudaStream_t stream);
 int launch_gemv_sub32_q4k(const GemvArgs &a, cudaStream_t stream);
 int launch_gemv_sub32_q6k(const GemvArgs &a, cudaStream_t stream);
+// one column of Sub32 from the f32 activation in one launch; QB_E_ARG where the kernel does not take it
+int launch_matvec_sub32_q8_0(const GemvArgs &a, const float *x, cudaStream_t stream);
+int launch_matvec_sub32_q4k(const GemvArgs &a, const float *x, cudaStream_t stream);
+int launch_matvec_sub32_q6k(const GemvArgs &a, const float *x, cudaStream_t stream);
 // The single-launch product (activation quantized inside the kernel); returns
 // QB_E_ARG when that kernel does not apply to the shape.
 int launch_matvec_q8_0(const GemvArgs &a, const float *x, cudaStream_t stream);

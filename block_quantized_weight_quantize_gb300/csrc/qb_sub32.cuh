@@ -393,32 +393,41 @@ struct S32K {
     const int8_t *codes;  // column 0 of this launch
     const qb_scale *scales;
     const int16_t *sums16;
+    const float *x;  // FUSED: the f32 activation, quantized in the prologue
     int *fault;
 };
 
 struct S32Smem {
-    int bars, act, scl, val, ring, total;
+    int bars, act, scl, sums, val, ring, total;
 };
 
-__host__ __device__ inline S32Smem s32_smem(int K, int ncols, int rec, int nt, int ncp, int D, int H, int vstride) {
+// sums: the unit sums the single-launch form quantizes into (fused only)
+__host__ __device__ inline S32Smem s32_smem(int K, int ncols, int rec, int nt, int ncp, int D, int H, int vstride,
+                                            bool fused = false) {
     S32Smem s;
     s.bars = 0;
     s.act = 128;                                          // the launch's codes
     s.scl = s.act + ((ncols * K + 127) & ~127);           // its scales, K/32 a column
-    s.val = s.scl + ((ncols * (K / 32) * 4 + 127) & ~127);
+    s.sums = s.scl + ((ncols * (K / 32) * 4 + 127) & ~127);
+    s.val = s.sums + (fused ? ((K / 16 * 2 + 127) & ~127) : 0);
     s.ring = s.val + ((H * nt * 2 * ncp * vstride * 4 + 127) & ~127);
     s.total = s.ring + D * nt * 2 * rec;
     return s;
 }
 
-template <int F, int CG>
+// FUSED (one column): the f32 activation p.x is quantized under Sub32 in the
+// prologue (the quantize_act_sub32 arithmetic: a 32-element block on four
+// lanes) while the first weight fills are in flight.
+template <int F, int CG, bool FUSED = false>
 __global__ void __launch_bounds__(gemv3_threads<CG>(), 1) s32_kernel(const S32K p) {
+    static_assert(!FUSED || CG == 1, "the single-launch form takes one column");
     extern __shared__ __align__(128) uint8_t smem[];
     const int ncp = p.ncg * CG;
-    const S32Smem L = s32_smem(p.K, p.ncols, p.rec, p.nt, ncp, p.D, p.H, p.vstride);
+    const S32Smem L = s32_smem(p.K, p.ncols, p.rec, p.nt, ncp, p.D, p.H, p.vstride, FUSED);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L.bars);
     uint8_t *act = smem + L.act;
     uint32_t *ascl = reinterpret_cast<uint32_t *>(smem + L.scl);
+    int16_t *asum = reinterpret_cast<int16_t *>(smem + L.sums);
     float *val = reinterpret_cast<float *>(smem + L.val);
     uint8_t *ring = smem + L.ring;
 
@@ -452,8 +461,46 @@ __global__ void __launch_bounds__(gemv3_threads<CG>(), 1) s32_kernel(const S32K 
         for (int it = 0; it < p.D && it < p.n_iter; ++it) fill(it);  // weights depend on no earlier kernel
     pdl_wait();
 
-    // ---- the launch's codes (the multi-column kernel's staged layout) and scales
-    {
+    // ---- the launch's codes (the multi-column kernel's staged layout) and
+    // scales; the single-launch form quantizes x here instead: a thread takes
+    // 8 consecutive elements (a 32-element block is 4 consecutive lanes),
+    // up to four rounds of loads first, then the quantizer
+    if constexpr (FUSED) {
+        constexpr int kR = 4;
+        const int G = p.K / 8;  // a multiple of 32: whole warps are in or out of a round
+        for (int g0 = 0; g0 < G; g0 += kR * (int)blockDim.x) {
+            float4 xv[2 * kR];
+#pragma unroll
+            for (int r = 0; r < kR; ++r) {
+                const int g8 = g0 + tid + r * (int)blockDim.x;
+                const bool in = g8 < G;
+                xv[2 * r] = in ? ldg_f4_ordered(reinterpret_cast<const float4 *>(p.x) + 2 * g8) : make_float4(0, 0, 0, 0);
+                xv[2 * r + 1] = in ? ldg_f4_ordered(reinterpret_cast<const float4 *>(p.x) + 2 * g8 + 1)
+                                   : make_float4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int r = 0; r < kR; ++r) {
+                if (g0 + r * (int)blockDim.x >= G) break;  // uniform: whole warps are in or out
+                const int g8 = g0 + tid + r * (int)blockDim.x;
+                const uint32_t xb[8] = {__float_as_uint(xv[2 * r].x), __float_as_uint(xv[2 * r].y),
+                                        __float_as_uint(xv[2 * r].z), __float_as_uint(xv[2 * r].w),
+                                        __float_as_uint(xv[2 * r + 1].x), __float_as_uint(xv[2 * r + 1].y),
+                                        __float_as_uint(xv[2 * r + 1].z), __float_as_uint(xv[2 * r + 1].w)};
+                uint2 cq;
+                int usum;
+                uint32_t scale;
+                quantize8<4, true>(xb, cq, usum, scale);
+                if (g8 < G) {
+                    const int u = g8 >> 1;
+                    const int pos = (F == kQ8_0) ? u : ((u & ~7) | ((u & 7) ^ ((u >> 3) & 7)));
+                    *reinterpret_cast<uint2 *>(act + 16 * pos + 8 * (g8 & 1)) = cq;
+                    if ((g8 & 1) == 0) asum[u] = (int16_t)usum;
+                    if ((g8 & 3) == 0) ascl[g8 >> 2] = scale;
+                }
+            }
+        }
+        __syncthreads();
+    } else {
         const int nu = p.ncols * (p.K / 16);
         const uint4 *src = reinterpret_cast<const uint4 *>(p.codes);
         constexpr int kU = 4;
@@ -481,7 +528,8 @@ __global__ void __launch_bounds__(gemv3_threads<CG>(), 1) s32_kernel(const S32K 
         const int col = g * CG + c;
         S[c][0] = S[c][1] = S[c][2] = S[c][3] = 0;
         if (F != kQ8_0 && live && col < p.ncols) {
-            const uint4 sw = __ldg(reinterpret_cast<const uint4 *>(p.sums16 + (int64_t)col * (p.K / 16)) + j);
+            const uint4 sw = FUSED ? *reinterpret_cast<const uint4 *>(asum + 8 * j)
+                                   : __ldg(reinterpret_cast<const uint4 *>(p.sums16 + (int64_t)col * (p.K / 16)) + j);
             S[c][0] = sw.x; S[c][1] = sw.y; S[c][2] = sw.z; S[c][3] = sw.w;
         }
     }
@@ -645,7 +693,7 @@ __global__ void __launch_bounds__(256) s32_plain_kernel(const uint8_t *__restric
 // ------------------------------------------------------------------ launch
 
 template <int F, int CG>
-bool s32_shape(int64_t rows, int64_t K, int ncols, S32K &k, int &grid, int &threads, int &smem) {
+bool s32_shape(int64_t rows, int64_t K, int ncols, S32K &k, int &grid, int &threads, int &smem, bool fused = false) {
     constexpr int kThreads = gemv3_threads<CG>();
     const int ts = (int)(K / 128);
     const int ncg = (ncols + CG - 1) / CG, ncp = ncg * CG;
@@ -663,22 +711,24 @@ bool s32_shape(int64_t rows, int64_t K, int ncols, S32K &k, int &grid, int &thre
     const int64_t rpc = (rows + grid - 1) / grid;
     const int budget = 225 * 1024;
     k.nt = (int)std::min<int64_t>(kThreads / tpt, std::max<int64_t>(1, (rpc + 1) / 2));
-    while (k.nt > 1 && s32_smem(k.K, ncols, k.rec, k.nt, ncp, 2, 1, k.vstride).total > budget) --k.nt;
-    if (s32_smem(k.K, ncols, k.rec, k.nt, ncp, 1, 1, k.vstride).total > budget) return false;
+    while (k.nt > 1 && s32_smem(k.K, ncols, k.rec, k.nt, ncp, 2, 1, k.vstride, fused).total > budget) --k.nt;
+    if (s32_smem(k.K, ncols, k.rec, k.nt, ncp, 1, 1, k.vstride, fused).total > budget) return false;
     k.n_iter = (int)((rpc + 2LL * k.nt - 1) / (2LL * k.nt));
     k.base = rows / grid;
     k.rem = rows % grid;
     threads = (k.nt * tpt + 31) / 32 * 32;
     k.H = std::max(1, std::min({k.n_iter, 8, threads / (k.nt * 2 * ncp)}));
-    const int hist = s32_smem(k.K, ncols, k.rec, k.nt, ncp, 0, k.H, k.vstride).total;
+    const int hist = s32_smem(k.K, ncols, k.rec, k.nt, ncp, 0, k.H, k.vstride, fused).total;
     k.D = std::max(1, std::min({k.n_iter, 4, (budget - hist) / (2 * k.nt * k.rec)}));
-    while (s32_smem(k.K, ncols, k.rec, k.nt, ncp, k.D, k.H, k.vstride).total > budget && k.H > 1) --k.H;
-    smem = s32_smem(k.K, ncols, k.rec, k.nt, ncp, k.D, k.H, k.vstride).total;
+    while (s32_smem(k.K, ncols, k.rec, k.nt, ncp, k.D, k.H, k.vstride, fused).total > budget && k.H > 1) --k.H;
+    smem = s32_smem(k.K, ncols, k.rec, k.nt, ncp, k.D, k.H, k.vstride, fused).total;
     return smem <= 227 * 1024;
 }
 
 template <int F, int CG>
-int launch_s32_cg(const GemvArgs &a, cudaStream_t stream) {
+int launch_s32_cg(const GemvArgs &a, cudaStream_t stream, const float *x = nullptr) {
+    const bool fused = x != nullptr;
+    if (fused && (CG != 1 || a.ncols != 1)) return QB_E_ARG;
     const int ts = (int)(a.K / 128);
     const int per = (gemv3_threads<CG>() / ts) / CG * CG;
     if (per < 1) return QB_E_ARG;
@@ -687,26 +737,30 @@ int launch_s32_cg(const GemvArgs &a, cudaStream_t stream) {
     for (int c0 = 0; c0 < a.ncols; c0 += per) {
         S32K k;
         int grid, threads, smem;
-        if (!s32_shape<F, CG>(a.rows, a.K, std::min(per, a.ncols - c0), k, grid, threads, smem)) return QB_E_ARG;
+        if (!s32_shape<F, CG>(a.rows, a.K, std::min(per, a.ncols - c0), k, grid, threads, smem, fused)) return QB_E_ARG;
     }
-    static bool attr_set = false;
-    if (!attr_set) {
-        if (cudaFuncSetAttribute(s32_kernel<F, CG>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) !=
-            cudaSuccess)
+    static bool attr_set[2] = {false, false};
+    if (!attr_set[fused]) {
+        const void *f = fused ? reinterpret_cast<const void *>(s32_kernel<F, CG, (CG == 1)>)
+                              : reinterpret_cast<const void *>(s32_kernel<F, CG, false>);
+        if (cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) != cudaSuccess)
             return QB_E_CUDA;
-        attr_set = true;
+        attr_set[fused] = true;
     }
     for (int c0 = 0; c0 < a.ncols; c0 += per) {
         S32K k;
         int grid, threads, smem;
-        s32_shape<F, CG>(a.rows, a.K, std::min(per, a.ncols - c0), k, grid, threads, smem);
+        s32_shape<F, CG>(a.rows, a.K, std::min(per, a.ncols - c0), k, grid, threads, smem, fused);
         k.W = static_cast<const uint8_t *>(a.W);
         k.out = a.out + (int64_t)c0 * a.rows;
-        k.codes = a.codes + (int64_t)c0 * a.K;
-        k.scales = a.scales + (int64_t)c0 * (a.K / 32);
-        k.sums16 = a.sums16 ? a.sums16 + (int64_t)c0 * (a.K / 16) : nullptr;
+        k.codes = fused ? nullptr : a.codes + (int64_t)c0 * a.K;
+        k.scales = fused ? nullptr : a.scales + (int64_t)c0 * (a.K / 32);
+        k.sums16 = (fused || !a.sums16) ? nullptr : a.sums16 + (int64_t)c0 * (a.K / 16);
+        k.x = x;
         k.fault = fault;
-        const int rc = launch_pdl(s32_kernel<F, CG>, dim3(grid), dim3(threads), (size_t)smem, stream, k);
+        const int rc = fused ? launch_pdl(s32_kernel<F, CG, (CG == 1)>, dim3(grid), dim3(threads), (size_t)smem,
+                                          stream, k)
+                             : launch_pdl(s32_kernel<F, CG, false>, dim3(grid), dim3(threads), (size_t)smem, stream, k);
         if (rc) return rc;
     }
     return QB_OK;
@@ -723,6 +777,15 @@ int launch_gemv_sub32(const GemvArgs &a, cudaStream_t stream) {
     const unsigned grid = (unsigned)((warps + 7) / 8);
     return launch_pdl(s32_plain_kernel<F>, dim3(grid), dim3(256), 0, stream, static_cast<const uint8_t *>(a.W), a.rows,
                       (int)a.K, (int)record_bytes(F, a.K), a.ncols, a.codes, a.scales, a.out);
+}
+
+// One column from the f32 activation in a single launch (the streaming
+// kernel quantizing x in its prologue); QB_E_ARG where that kernel does not
+// take the shape.
+template <int F>
+int launch_matvec_sub32(const GemvArgs &a, const float *x, cudaStream_t stream) {
+    if (a.ncols != 1 || a.rows < 1 || a.K < 256 || a.K % 256 != 0) return QB_E_ARG;
+    return launch_s32_cg<F, 1>(a, stream, x);
 }
 
 }  // namespace qb

@@ -4,4 +4,7 @@
 
 namespace qb {
 int launch_gemv_sub32_q4k(const GemvArgs &a, cudaStream_t stream) { return launch_gemv_sub32<kQ4K>(a, stream); }
+int launch_matvec_sub32_q4k(const GemvArgs &a, const float *x, cudaStream_t stream) {
+    return launch_matvec_sub32<kQ4K>(a, x, stream);
+}
 }  // namespace qb

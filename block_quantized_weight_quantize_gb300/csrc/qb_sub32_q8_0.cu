@@ -4,4 +4,7 @@
 
 namespace qb {
 int launch_gemv_sub32_q8_0(const GemvArgs &a, cudaStream_t stream) { return launch_gemv_sub32<kQ8_0>(a, stream); }
+int launch_matvec_sub32_q8_0(const GemvArgs &a, const float *x, cudaStream_t stream) {
+    return launch_matvec_sub32<kQ8_0>(a, x, stream);
+}
 }  // namespace qb

@@ -272,7 +272,10 @@ QB_API int64_t q_matvec_sub32_workspace_bytes(int64_t K, int ncols);
 
 /* quantize_act_sub32 into `workspace` (16-byte aligned, at least
  * q_matvec_sub32_workspace_bytes(K, ncols) bytes), then q_gemv_sub32: two
- * launches on `stream`. */
+ * launches on `stream`, bit for bit the same results.  For one column of a
+ * matrix whose rows the streaming kernel takes (K % 256 == 0 and K/128
+ * threads a row team) it is a single launch that quantizes x inside the
+ * product kernel and needs no workspace (`workspace` may be NULL). */
 QB_API int q_matvec_sub32(qb_fmt fmt, const void *W, int64_t rows, int64_t K, const float *x, int ncols,
                           float *out, void *workspace, size_t workspace_bytes, void *stream);
 

@@ -234,6 +234,36 @@ def test_matvec_sub32_pipeline(fmt, ncols):
     assert np.array_equal(bits(host(out)), bits(want))
 
 
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("rows,K", [(300, 4096), (1000, 256), (77, 1024), (2 * 152 + 5, 2048), (40, 14336)])
+def test_matvec_sub32_one_launch(fmt, rows, K):
+    """One column of q_matvec_sub32 without a workspace: the product kernel
+    quantizes x in its prologue.  Bit for bit the oracle's quantize then dot,
+    with 32-element blocks many binades apart in one group (the exact group
+    sum), a zero block, a NaN, a denormal and an infinity among the inputs;
+    the same call given a workspace agrees."""
+    import torch
+    rng = np.random.default_rng(rows + K + fmt)
+    W = synth.pack(fmt, synth.draw(fmt, rng, rows, K))
+    x = _spread_blocks(synth.draw_act(rng, 1, K, outlier_frac=0.001), [0, -40, 37, 5, -90, 0, 60, -3])
+    x[0, 64:96] = 0.0                                   # a zero block
+    x[0, 100] = np.nan
+    x[0, 130] = np.uint32(0x00012345).view(np.float32)  # a denormal element
+    if K == 2048:
+        x[0, 700] = np.inf                              # a block with an infinity: every row NaN
+    codes, m, e, _ = oracle.quantize_sub32(x)
+    want = oracle.gemv_sub32(fmt, W, rows, K, codes, m, e)
+    out = torch.full((1, rows), float("nan"), dtype=torch.float32, device="cuda")
+    qb.q_matvec_sub32(fmt, dev(W), rows, K, dev(x), out, workspace=None)
+    torch.cuda.synchronize()
+    assert np.array_equal(bits(host(out)), bits(want))
+    ws = torch.empty(qb.q_matvec_sub32_workspace_bytes(K, 1), dtype=torch.uint8, device="cuda")
+    out.fill_(float("nan"))
+    qb.q_matvec_sub32(fmt, dev(W), rows, K, dev(x), out, workspace=ws)
+    torch.cuda.synchronize()
+    assert np.array_equal(bits(host(out)), bits(want))
+
+
 def test_sub32_argument_checks():
     import torch
     K = 512
