@@ -9,7 +9,8 @@
 // around the exact dot of the dequantized weights.
 //
 // Decode in registers (the page's S = 1 form, no weight buffer): the
-// hardware's exact e4m3x2 -> f16x2 conversion, then f16 -> f32.  One warp
+// hardware's exact e4m3x2 -> f16x2 conversion on both half words of a 32-bit
+// weight word, then f16 -> f32.  One warp
 // takes a row at a time; lane l owns the 16-byte chunks l, l + 32, ... (16
 // weights each, all in one scale block), so a warp's loads are 512 contiguous
 // bytes; per chunk the 16 products are summed by an FMA chain and added into
@@ -26,10 +27,15 @@
 
 namespace qb {
 
-__device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t two) {
-    uint32_t h2;
-    asm("{ .reg .b16 t; cvt.u16.u32 t, %1; cvt.rn.f16x2.e4m3x2 %0, t; }" : "=r"(h2) : "r"(two));
-    return __half22float2(*reinterpret_cast<const __half2 *>(&h2));
+// four E4M3 bytes (byte i of the word is weight i) to f32, exactly: the
+// hardware's e4m3x2 -> f16x2 conversion on each half word, then f16 -> f32
+__device__ __forceinline__ void e4m3x4_to_f32(uint32_t four, float &w0, float &w1, float &w2, float &w3) {
+    uint32_t h01, h23;
+    asm("{ .reg .b16 lo, hi; mov.b32 {lo, hi}, %2; cvt.rn.f16x2.e4m3x2 %0, lo; cvt.rn.f16x2.e4m3x2 %1, hi; }"
+        : "=r"(h01), "=r"(h23) : "r"(four));
+    const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&h01));
+    const float2 b = __half22float2(*reinterpret_cast<const __half2 *>(&h23));
+    w0 = a.x; w1 = a.y; w2 = b.x; w3 = b.y;
 }
 
 struct Fp8K {
@@ -46,8 +52,10 @@ struct Fp8K {
 // RPW rows a warp at a time (two for four or more columns: each staged
 // activation read then serves both rows).  The first batch of a warp's
 // weights is loaded before the programmatic-dependent-launch wait and the
-// activation staging (weights depend on no earlier kernel).
-template <int NC, int RPW>
+// activation staging (weights depend on no earlier kernel).  FULL: K a
+// multiple of 4096 (a lane's 16-byte chunks come in whole batches of 8 rounds
+// of 32), so no chunk needs a bounds test.
+template <int NC, int RPW, bool FULL>
 __global__ void __launch_bounds__(256) gemv_fp8_kernel(const Fp8K p) {
     extern __shared__ __align__(16) float4 xs[];  // [NC][128 * nj] in lane order
     const int lane = threadIdx.x & 31;
@@ -69,7 +77,7 @@ __global__ void __launch_bounds__(256) gemv_fp8_kernel(const Fp8K p) {
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
                 const int ch = lane + 32 * (j0 + u);
-                const bool in = rin && j0 + u < nj && ch < nch;
+                const bool in = rin && (FULL || (j0 + u < nj && ch < nch));
                 w[q][u] = in ? __ldg(reinterpret_cast<const uint4 *>(wr) + ch) : make_uint4(0, 0, 0, 0);
                 s[q][u] = in ? __ldg(sr + (ch >> 3)) : 0.0f;
             }
@@ -79,12 +87,13 @@ __global__ void __launch_bounds__(256) gemv_fp8_kernel(const Fp8K p) {
 
     pdl_launch_dependents();
     pdl_wait();
-    for (int i = threadIdx.x; i < NC * nf; i += blockDim.x) {
-        const int c = i / nf, f = i - c * nf;
-        const int ch = f >> 2, q = f & 3, l = ch & 31, j = ch >> 5;
-        xs[c * cs + (4 * j + q) * 32 + l] =
-            c < p.nc ? __ldg(reinterpret_cast<const float4 *>(p.x + (int64_t)c * p.K) + f) : make_float4(0, 0, 0, 0);
-    }
+#pragma unroll
+    for (int c = 0; c < NC; ++c)
+        for (int f = threadIdx.x; f < nf; f += blockDim.x) {
+            const int ch = f >> 2, q = f & 3, l = ch & 31, j = ch >> 5;
+            xs[c * cs + (4 * j + q) * 32 + l] =
+                c < p.nc ? __ldg(reinterpret_cast<const float4 *>(p.x + (int64_t)c * p.K) + f) : make_float4(0, 0, 0, 0);
+        }
     __syncthreads();
     bool first = true;
     for (int64_t r = r0; r < p.rows; r += nw * RPW) {
@@ -99,19 +108,14 @@ __global__ void __launch_bounds__(256) gemv_fp8_kernel(const Fp8K p) {
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
                 const int j = j0 + u;
-                if (j >= nj || lane + 32 * j >= nch) break;
+                if (!FULL && (j >= nj || lane + 32 * j >= nch)) break;
                 float wf[RPW][16];
 #pragma unroll
                 for (int q = 0; q < RPW; ++q) {
                     const uint32_t wv[4] = {w[q][u].x, w[q][u].y, w[q][u].z, w[q][u].w};
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const float2 lo = e4m3x2_to_float2(wv[k] & 0xFFFFu), hi = e4m3x2_to_float2(wv[k] >> 16);
-                        wf[q][4 * k] = lo.x;
-                        wf[q][4 * k + 1] = lo.y;
-                        wf[q][4 * k + 2] = hi.x;
-                        wf[q][4 * k + 3] = hi.y;
-                    }
+                    for (int k = 0; k < 4; ++k)
+                        e4m3x4_to_f32(wv[k], wf[q][4 * k], wf[q][4 * k + 1], wf[q][4 * k + 2], wf[q][4 * k + 3]);
                 }
 #pragma unroll
                 for (int c = 0; c < NC; ++c) {
@@ -154,17 +158,20 @@ template <int NC>
 static int launch_fp8_nc(const Fp8K &k, cudaStream_t stream) {
     constexpr int RPW = NC >= 4 ? 2 : 1;
     const size_t smem = fp8_smem(NC, k.K);
-    static bool attr_set = false;
-    if (!attr_set) {
-        if (cudaFuncSetAttribute(gemv_fp8_kernel<NC, RPW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 200 * 1024) != cudaSuccess)
+    const bool full = k.K % 4096 == 0;  // a lane's chunks come in whole batches of 8 rounds of 32
+    static bool attr_set[2] = {false, false};
+    if (!attr_set[full]) {
+        const void *f = full ? reinterpret_cast<const void *>(gemv_fp8_kernel<NC, RPW, true>)
+                             : reinterpret_cast<const void *>(gemv_fp8_kernel<NC, RPW, false>);
+        if (cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024) != cudaSuccess)
             return QB_E_CUDA;
-        attr_set = true;
+        attr_set[full] = true;
     }
     const int per_sm = (int)std::max<size_t>(1, std::min<size_t>(8, (220 * 1024) / (smem + 1024)));
     const int64_t blocks = (k.rows + 8 * RPW - 1) / (8 * RPW);
     const unsigned grid = (unsigned)std::max<int64_t>(1, std::min<int64_t>(blocks, (int64_t)num_sms() * per_sm));
-    return launch_pdl(gemv_fp8_kernel<NC, RPW>, dim3(grid), dim3(256), smem, stream, k);
+    return full ? launch_pdl(gemv_fp8_kernel<NC, RPW, true>, dim3(grid), dim3(256), smem, stream, k)
+                : launch_pdl(gemv_fp8_kernel<NC, RPW, false>, dim3(grid), dim3(256), smem, stream, k);
 }
 
 // Columns in launches of at most 16 (a power of two) that fit 200 KB of
