@@ -154,9 +154,14 @@ __global__ void __launch_bounds__(256) gemv_fp8_kernel(const Fp8K p) {
 
 __host__ __device__ inline size_t fp8_smem(int NC, int64_t K) { return (size_t)NC * ((K / 16 + 31) / 32) * 2048; }
 
+// Two rows a warp for every column count: at one row a warp, 4096 rows took
+// 512 CTAs of 256 threads, more than the register file holds at once (three
+// a SM at 78 registers), so the last CTAs ran as a second wave.  The grid is
+// clamped to what is resident at once (the occupancy calculator); the rows
+// past it loop within the warps.
 template <int NC>
 static int launch_fp8_nc(const Fp8K &k, cudaStream_t stream) {
-    constexpr int RPW = NC >= 4 ? 2 : 1;
+    constexpr int RPW = 2;
     const size_t smem = fp8_smem(NC, k.K);
     const bool full = k.K % 4096 == 0;  // a lane's chunks come in whole batches of 8 rounds of 32
     static bool attr_set[2] = {false, false};
@@ -167,7 +172,14 @@ static int launch_fp8_nc(const Fp8K &k, cudaStream_t stream) {
             return QB_E_CUDA;
         attr_set[full] = true;
     }
-    const int per_sm = (int)std::max<size_t>(1, std::min<size_t>(8, (220 * 1024) / (smem + 1024)));
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+            &per_sm,
+            full ? reinterpret_cast<const void *>(gemv_fp8_kernel<NC, RPW, true>)
+                 : reinterpret_cast<const void *>(gemv_fp8_kernel<NC, RPW, false>),
+            256, smem) != cudaSuccess)
+        return QB_E_CUDA;
+    per_sm = std::max(1, per_sm);
     const int64_t blocks = (k.rows + 8 * RPW - 1) / (8 * RPW);
     const unsigned grid = (unsigned)std::max<int64_t>(1, std::min<int64_t>(blocks, (int64_t)num_sms() * per_sm));
     return full ? launch_pdl(gemv_fp8_kernel<NC, RPW, true>, dim3(grid), dim3(256), smem, stream, k)
