@@ -71,7 +71,8 @@ __device__ __forceinline__ int int8_code(float x, float inv, bool zero) {
 __global__ void __launch_bounds__(256) kv_cache_rows_kernel(const float *__restrict__ x, int64_t n, int d,
                                                             int8_t *__restrict__ codes,
                                                             uint16_t *__restrict__ scales) {
-    pdl_launch_dependents();
+    // no early launch_dependents: the score kernel reads key rows before its
+    // own pdl_wait, so the kernel after this one starts when it has finished
     pdl_wait();
     const int64_t row = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
@@ -228,47 +229,12 @@ template <bool S32, int NB>
 __global__ void __launch_bounds__(256, 2) kv_scores_kernel(const KvK p) {
     extern __shared__ __align__(16) int hsm[];
     constexpr int kW = 2 + NB, kD = kv_ring_depth<NB>(), kPitch = 32 * NB + 32, kTile = 16 * kPitch;
-    pdl_launch_dependents();
-    pdl_wait();
-    for (int h = threadIdx.x; h < p.nh; h += blockDim.x) {
-        const uint32_t *qs = reinterpret_cast<const uint32_t *>(p.qs) + (int64_t)h * p.nbq;
-        int *w = hsm + h * kW;
-        if (!S32) {
-            const uint32_t sw = qs[0];
-            w[0] = (sw & 0xFFu) == 0u ? 2 : 0;
-            w[1] = (int)(int16_t)(sw >> 16);
-            for (int b = 0; b < NB; ++b) w[2 + b] = (int)(sw & 0xFFu);
-        } else {
-            bool zero = false;
-            int lo = INT_MAX, hi = INT_MIN;
-            for (int b = 0; b < p.nbq; ++b) {
-                const uint32_t sw = qs[b];
-                zero |= (sw & 0xFFu) == 0u;
-                if (b < NB) {
-                    const int e = (int)(int16_t)(sw >> 16);
-                    lo = min(lo, e);
-                    hi = max(hi, e);
-                }
-            }
-            int mode = zero ? 2 : (hi - lo > 12 ? 1 : 0);
-            for (int b = 0; b < NB; ++b) {
-                const uint32_t sw = qs[b];
-                const uint32_t M = mode == 0 ? (sw & 0xFFu) << ((int)(int16_t)(sw >> 16) - lo) : 0u;
-                if (M > 0xFFFFu) mode = 1;
-                w[2 + b] = (int)M;
-            }
-            w[0] = mode;
-            w[1] = lo;
-        }
-    }
-    __syncthreads();
-
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
     uint8_t *ring = reinterpret_cast<uint8_t *>(hsm) + ((p.nh * kW * 4 + 15) & ~15) + warp * kD * kTile;
     const int64_t nw = (int64_t)gridDim.x * (blockDim.x >> 5);
     const int64_t wid = (int64_t)blockIdx.x * (blockDim.x >> 5) + warp;
     const int64_t t_begin = wid * p.ntiles / nw, t_end = (wid + 1) * p.ntiles / nw;
-    if (t_begin >= t_end) return;
+    const bool any = t_begin < t_end;
     const int ntr = (int)p.ntr;
 
     // this lane's copies within a tile: chunk ci = lane + 32q is row ci / (2NB),
@@ -317,8 +283,13 @@ __global__ void __launch_bounds__(256, 2) kv_scores_kernel(const KvK p) {
         ++itile;
         islot = (islot + 1 == kD) ? 0 : islot + 1;
     };
+    // the key cache depends on no earlier kernel (kv_cache_rows, which writes
+    // it, lets its successor start only when it has finished): the first kD
+    // tiles and key scales are requested before the wait
+    if (any) {
 #pragma unroll
-    for (int i = 0; i < kD; ++i) issue();
+        for (int i = 0; i < kD; ++i) issue();
+    }
 
     // key scales of a tile's rows g and g + 8 (0 past L; never read there)
     auto ks_load = [&](const Pos &x, uint32_t &a, uint32_t &b) {
@@ -327,9 +298,48 @@ __global__ void __launch_bounds__(256, 2) kv_scores_kernel(const KvK p) {
         a = r < p.L ? __ldg(base) : 0u;
         b = r + 8 < p.L ? __ldg(base + 8) : 0u;
     };
-    uint32_t ks0, ks1;
-    ks_load(cur, ks0, ks1);
+    uint32_t ks0 = 0, ks1 = 0;
+    if (any) ks_load(cur, ks0, ks1);
 
+    pdl_launch_dependents();
+    pdl_wait();
+    // per query head, the block multipliers (after the wait: the query scales
+    // are the previous kernel's output)
+
+    for (int h = threadIdx.x; h < p.nh; h += blockDim.x) {
+        const uint32_t *qs = reinterpret_cast<const uint32_t *>(p.qs) + (int64_t)h * p.nbq;
+        int *w = hsm + h * kW;
+        if (!S32) {
+            const uint32_t sw = qs[0];
+            w[0] = (sw & 0xFFu) == 0u ? 2 : 0;
+            w[1] = (int)(int16_t)(sw >> 16);
+            for (int b = 0; b < NB; ++b) w[2 + b] = (int)(sw & 0xFFu);
+        } else {
+            bool zero = false;
+            int lo = INT_MAX, hi = INT_MIN;
+            for (int b = 0; b < p.nbq; ++b) {
+                const uint32_t sw = qs[b];
+                zero |= (sw & 0xFFu) == 0u;
+                if (b < NB) {
+                    const int e = (int)(int16_t)(sw >> 16);
+                    lo = min(lo, e);
+                    hi = max(hi, e);
+                }
+            }
+            int mode = zero ? 2 : (hi - lo > 12 ? 1 : 0);
+            for (int b = 0; b < NB; ++b) {
+                const uint32_t sw = qs[b];
+                const uint32_t M = mode == 0 ? (sw & 0xFFu) << ((int)(int16_t)(sw >> 16) - lo) : 0u;
+                if (M > 0xFFFFu) mode = 1;
+                w[2 + b] = (int)M;
+            }
+            w[0] = mode;
+            w[1] = lo;
+        }
+    }
+    __syncthreads();
+
+    if (!any) return;  // after the barrier: every thread takes part in the table
     int held = -1;  // key head * nchunk + chunk of the fragments held
     uint2 B[NB];
     int M0[NB], M1[NB];

@@ -26,8 +26,12 @@
  * cudaStream_t passed as void*, NULL = the legacy default stream), except
  * q_check_weights, which synchronizes that stream.  Kernels are launched with
  * programmatic dependent launch: a product kernel may start streaming its
- * weights while the previous kernel on the stream finishes, and waits for it
- * before it reads activations or writes outputs.
+ * weights (kv_scores: its first key tiles) while the previous kernel on the
+ * stream finishes, and waits for it before it reads activations or writes
+ * outputs.  So weights and the key cache must be complete before that
+ * previous kernel signals its dependents: true for any kernel that does not
+ * trigger them early, and for kv_cache_rows, which lets its successor start
+ * only when it has finished.
  *
  * Errors: 0 on success, else a negative QB_E_* code (argument checks happen
  * on the host before any launch; nothing is launched on error).

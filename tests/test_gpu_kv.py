@@ -126,22 +126,32 @@ def test_kv_scores_long_context(scaling):
     assert np.array_equal(bits(got), bits(want))
 
 
-def test_kv_pipeline():
+@pytest.mark.parametrize("rows_last", [False, True])
+def test_kv_pipeline(rows_last):
     """kv_cache_rows and kv_quantize_heads on the GPU, then kv_scores, against
-    the oracle's cache_row, quantize_head and scores."""
+    the oracle's cache_row, quantize_head and scores.  rows_last: the cache
+    rows are written by the launch right before kv_scores, on the same stream
+    with no synchronisation between (the score kernel requests key tiles
+    before its dependency wait; kv_cache_rows lets it start only once the rows
+    are written), the cache filled with stale bytes beforehand."""
     import torch
     rng = np.random.default_rng(123)
     nh, nkv, d, L = 16, 4, 128, 1000
     q = rng.standard_normal((nh, d)).astype(np.float32)
     k = rng.standard_normal((nkv * L, d)).astype(np.float32)
     for scaling in (qb.PERBLOCK, qb.SUB32):
-        kc = torch.empty((nkv, L, d), dtype=torch.int8, device="cuda")
-        ks = torch.empty((nkv, L), dtype=torch.int16, device="cuda")
-        qb.kv_cache_rows(dev(k), kc.view(nkv * L, d), ks.view(-1))
+        kc = torch.full((nkv, L, d), 77, dtype=torch.int8, device="cuda")
+        ks = torch.full((nkv, L), 0x3C00, dtype=torch.int16, device="cuda")
         dp = qb.kv_head_codes(scaling, d)
         qc = torch.empty((nh, dp), dtype=torch.int8, device="cuda")
         qs = torch.empty((nh, dp // 32 if scaling == qb.SUB32 else 1), dtype=torch.int32, device="cuda")
-        qb.kv_quantize_heads(scaling, dev(q), qc, qs)
+        torch.cuda.synchronize()
+        if rows_last:
+            qb.kv_quantize_heads(scaling, dev(q), qc, qs)
+            qb.kv_cache_rows(dev(k), kc.view(nkv * L, d), ks.view(-1))
+        else:
+            qb.kv_cache_rows(dev(k), kc.view(nkv * L, d), ks.view(-1))
+            qb.kv_quantize_heads(scaling, dev(q), qc, qs)
         out = torch.empty((nh, L), dtype=torch.float32, device="cuda")
         qb.kv_scores(scaling, qc, qs, d, kc, ks, L, 0.125, out)
         torch.cuda.synchronize()
