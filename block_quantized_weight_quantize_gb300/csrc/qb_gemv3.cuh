@@ -239,8 +239,12 @@ __global__ void __launch_bounds__(gemv3_threads<CG>(), 1)
         if constexpr (MULTI) fill_rows(p.mt, dst, row0 + first, n, p.rec, bars + slot);
         else bulk_g2s(dst, p.W + (row0 + first) * p.rec, bytes, bars + slot);
     };
+    // weights depend on no earlier kernel.  One column: only the first slot
+    // ahead of the activation, whose loads would otherwise queue behind the
+    // whole ring's fills; the rest once it is staged
+    const int pre = CG == 1 ? 1 : p.D;
     if (tid == 0)
-        for (int it = 0; it < p.D && it < p.n_iter; ++it) fill(it);  // weights depend on no earlier kernel
+        for (int it = 0; it < pre && it < p.n_iter; ++it) fill(it);
     // the next launch may be scheduled now: it reads nothing this one writes
     // before its own pdl_wait, which returns once this grid has finished
     pdl_launch_dependents();
@@ -341,6 +345,8 @@ __global__ void __launch_bounds__(gemv3_threads<CG>(), 1)
         }
     }
     __syncthreads();
+    if (tid == 0)
+        for (int it = pre; it < p.D && it < p.n_iter; ++it) fill(it);
     // codes of half-slice j (Q4_K/Q6_K: a[c][k] = unit 8j+k; Q8_0: unit 8j + (k ^ jj))
 #pragma unroll
     for (int c = 0; c < CG; ++c) {
