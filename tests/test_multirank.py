@@ -86,3 +86,20 @@ def test_reference_arm_rank0_prints_one_line():
     assert len(lines) == 1
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["value"] > 0 and d["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_reference_arm_ffn_block():
+    """The reference arm on the Q6_K-like FFN block (gate and up from one
+    activation, down at K = 14336): one JSON line timing the oracle over
+    sampled rows of all three matrices."""
+    env = dict(os.environ, RANK="0", WORLD_SIZE="1", LOCAL_RANK="0")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload",
+                        "q6k_ffn_14336x4096", "--steps", "1", "--warmup", "1"], capture_output=True, text=True,
+                       env=env, timeout=900)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["value"] > 0 and d["cpu_baseline"]["kind"] == "oracle"
+    assert d["config"]["down"] == [4096, 14336] and d["config"]["gate_up_rows"] == [14336, 14336]
+
