@@ -521,7 +521,7 @@ def run_grouped(args, rank, world):
     stream.synchronize()
     e2e_s = max_over_ranks(time.perf_counter() - t0, dev)
     assert qb.q_device_status() == qb.QB_OK
-    return {
+    res = {
         "metric": f"weight GB/s ({desc})",
         "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": max(1, args.steps // G) * G,
         "warmup": args.warmup, "ms_per_step": round(ms, 6), "higher_is_better": True, "scaling": "weak",
@@ -550,6 +550,45 @@ def run_grouped(args, rank, world):
                 "steps": n_e2e,
                 "how": "per step: pinned x -> device, q_matvec_many through the Python binding, outputs -> pinned "
                        "host; host wall clock over all steps"},
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, n, sample = sampled_oracle_rate([(fmt, r, K, W, x, 1.0) for r, W in zip(rows_list, Whs)],
+                                           args.cpu_seconds)
+        res["cpu_baseline"] = {"value": round(v, 4), "unit": "GB/s", "cores": n, "kind": "oracle", "sample": sample}
+    return res
+
+
+def run_grouped_reference(args):
+    """The reference arm on a grouped workload: the oracle over the group's
+    matrices (one shared activation), sampled rows a step."""
+    fmt, rows_list, K, ncols, seed, outl, desc = GROUPED[args.workload]
+    rng = np.random.default_rng(seed)
+    Whs = [synth.pack(fmt, synth.draw(fmt, rng, r, K)) for r in rows_list]
+    x = synth.draw_act(rng, ncols, K, outlier_frac=outl)
+    mats = [(fmt, r, K, W, x, 1.0) for r, W in zip(rows_list, Whs)]
+    n = _oracle_threads()
+    t0 = time.perf_counter()
+    sampled_oracle_pass(mats, n, 1.0)
+    full = time.perf_counter() - t0
+    frac = max(1e-3, min(1.0, (100.0 / max(1, args.steps + args.warmup)) / max(full, 1e-6)))
+    for _ in range(args.warmup):
+        sampled_oracle_pass(mats, n, frac)
+    done, t0 = 0, time.perf_counter()
+    for _ in range(args.steps):
+        done += sampled_oracle_pass(mats, n, frac)
+    el = time.perf_counter() - t0
+    value = done / el / 1e9
+    sample = (f"each step: quantize + {frac:.3g} of the rows of each of the {len(rows_list)} matrices, split over "
+              f"{n} threads of the scalar C oracle")
+    return {
+        "impl": "reference", "metric": f"weight GB/s ({desc})",
+        "value": round(value, 4), "unit": "GB/s", "n_gpus": 0, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(el * 1e3 / args.steps, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "int64/int128 exact, f32 rounding (scalar C)",
+        "data": "synthetic (seeded PCG64)",
+        "config": {"workload": desc, "rows": rows_list, "K": K, "ncols": ncols, "format": synth.FORMAT_NAMES[fmt]},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": n, "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
 
@@ -807,6 +846,40 @@ def cpu_baseline(fmt, rows, K, ncols, Wh, x, wbytes, budget_s=10.0, sub32=False)
                       f"threads of the scalar C oracle"}
 
 
+def sampled_oracle_pass(mats, n, frac):
+    """The oracle (quantize + product) over a fraction of the rows of every
+    (fmt, rows, K, weights, activation, weight) entry of a step, the fraction
+    for an entry being frac * weight (at most 1); returns the weight bytes
+    processed."""
+    done = 0
+    for fmt, rows, K, W, x, wt in mats:
+        r = max(1, min(rows, int(rows * frac * wt)))
+        oracle_pass(fmt, rows, K, W, x, n, row_limit=r)
+        done += synth.record_bytes(fmt, K) * r
+    return done
+
+
+def sampled_oracle_rate(mats, budget_s):
+    """Weight GB/s of the oracle over repeated sampled passes of a step's
+    matrices, about budget_s seconds of host work in all (the sample sized
+    from a timed small pass); returns (GB/s, threads, description)."""
+    n = _oracle_threads()
+    t0 = time.perf_counter()
+    sampled_oracle_pass(mats, n, 0.002)                    # warm (and builds the oracle)
+    small = time.perf_counter() - t0
+    frac = max(0.002, min(1.0, 0.002 * (budget_s / 5.0) / max(small, 1e-6)))
+    done, reps, t0 = 0, 0, time.perf_counter()
+    while True:
+        done += sampled_oracle_pass(mats, n, frac)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    return done / el / 1e9, n, (f"{reps} passes over {frac:.3g} of the rows of each of the step's {len(mats)} matrix "
+                                f"shapes (quantize + product), rows split over {n} threads of the scalar C oracle, "
+                                f"{el:.1f} s")
+
+
 def _ffn_host(rng_seed):
     """The FFN workload's three matrices and two activations, drawn on the host."""
     fmt, rows, K, drows, seed, desc = FFN["q6k_ffn_14336x4096"]
@@ -999,6 +1072,29 @@ def run_ffn_reference(args):
     }
 
 
+def _stack_host(ncols, seed):
+    """The stack's drawn matrices on the host (one per shape, and the first
+    eighth of the output matrix, which the device tiles eight times) and its
+    two activations, in the draw order the bench uses."""
+    rng = np.random.default_rng(seed)
+    hmats = [synth.pack(fmt, synth.draw(fmt, rng, rows, K)) for _, fmt, rows, K in STACK_MATS]
+    _, ofmt, orows, oK = STACK_OUT
+    Wo = synth.pack(ofmt, synth.draw(ofmt, rng, orows // 8, oK))
+    xh = {k: synth.draw_act(rng, ncols, k) for k in (4096, 14336)}
+    return hmats, Wo, xh
+
+
+def _stack_oracle_mats(hmats, Wo, xh):
+    """The stack's matrices for the sampled oracle, each weighted by how often
+    a step reads it: the layer shapes 1 (32 times a step), the output
+    matrix's drawn eighth 8/32 (8 times a step), so a pass has the step's mix
+    of bytes."""
+    _, ofmt, orows, oK = STACK_OUT
+    mats = [(fmt, rows, K, W, xh[K], 1.0) for (_, fmt, rows, K), W in zip(STACK_MATS, hmats)]
+    mats.append((ofmt, orows // 8, oK, Wo, xh[oK], 8.0 / STACK_LAYERS))
+    return mats
+
+
 def run_stack(args, rank, world):
     """One step = the 129 products of an 8B-class decode step (every layer's
     weights its own copy in HBM, 4.36 GB in all), each a q_matvec call from
@@ -1010,24 +1106,19 @@ def run_stack(args, rank, world):
     ncols = STACK[args.workload]
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
-    rng = np.random.default_rng(9 + 1000 * rank)
+    hmats, Wo, xhost = _stack_host(ncols, 9 + 1000 * rank)
     mats = []  # (name, fmt, rows, K, device weights per layer)
-    for name, fmt, rows, K in STACK_MATS:
-        Wh = synth.pack(fmt, synth.draw(fmt, rng, rows, K))
+    for (name, fmt, rows, K), Wh in zip(STACK_MATS, hmats):
         w0 = torch.from_numpy(Wh).to(dev)
         layers = [w0] + [w0.clone() for _ in range(STACK_LAYERS - 1)]
         mats.append((name, fmt, rows, K, layers))
-        del Wh
     oname, ofmt, orows, oK = STACK_OUT
-    part = orows // 8  # drawn once, tiled 8 times on the device
-    Wo = synth.pack(ofmt, synth.draw(ofmt, rng, part, oK))
     wo = torch.empty(orows * synth.record_bytes(ofmt, oK), dtype=torch.uint8, device=dev)
     for i in range(8):
         wo[i * Wo.size:(i + 1) * Wo.size].copy_(torch.from_numpy(Wo))
-    del Wo
     wbytes = sum(synth.weight_bytes(f, r, k) for _, f, r, k in STACK_MATS) * STACK_LAYERS + \
         synth.weight_bytes(ofmt, orows, oK)
-    xs = {k: torch.from_numpy(synth.draw_act(rng, ncols, k)).to(dev) for k in (4096, 14336)}
+    xs = {k: torch.from_numpy(v).to(dev) for k, v in xhost.items()}
     outs = {name: torch.empty((ncols, rows), dtype=torch.float32, device=dev) for name, _, rows, _, _ in mats}
     logits = torch.empty((ncols, orows), dtype=torch.float32, device=dev)
     wsb = max(qb.q_matvec_workspace_bytes(f, k, ncols) for _, f, _, k in STACK_MATS + [STACK_OUT])
@@ -1145,7 +1236,47 @@ def run_stack(args, rank, world):
                 "steps": n_e2e, "how": "per step the 129 calls through the binding, the first (QKV) and the last "
                 "(output) q_matvec_host with pinned host buffers; host wall clock"},
     }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, n, sample = sampled_oracle_rate(_stack_oracle_mats(hmats, Wo, xhost), args.cpu_seconds)
+        res["cpu_baseline"] = {"value": round(v, 4), "unit": "GB/s", "cores": n, "kind": "oracle", "sample": sample}
     return res
+
+
+def run_stack_reference(args):
+    """The reference arm on the stack: the oracle over sampled rows of the
+    step's matrices (the layer shapes and the output matrix in the step's mix
+    of bytes), each step's sample sized so the run stays within ~2 minutes."""
+    ncols = STACK[args.workload]
+    hmats, Wo, xhost = _stack_host(ncols, 9)
+    mats = _stack_oracle_mats(hmats, Wo, xhost)
+    n = _oracle_threads()
+    t0 = time.perf_counter()
+    sampled_oracle_pass(mats, n, 0.002)
+    small = time.perf_counter() - t0
+    frac = max(0.002, min(1.0, 0.002 * (100.0 / max(1, args.steps + args.warmup)) / max(small, 1e-6)))
+    for _ in range(args.warmup):
+        sampled_oracle_pass(mats, n, frac)
+    done, t0 = 0, time.perf_counter()
+    for _ in range(args.steps):
+        done += sampled_oracle_pass(mats, n, frac)
+    el = time.perf_counter() - t0
+    value = done / el / 1e9
+    sample = (f"each step: {frac:.3g} of the rows of every layer shape and 8/32 of that of the output matrix's "
+              f"drawn eighth ({ncols} column(s), quantize + product), split over {n} threads of the scalar C oracle")
+    return {
+        "impl": "reference",
+        "metric": f"weight GB/s (8B-class decode stack, {ncols} column(s): 32 layers of Q4_K-like QKV 6144x4096, "
+                  f"O 4096x4096, gate+up 28672x4096, down 4096x14336 + Q6_K-like output 128256x4096)",
+        "value": round(value, 4), "unit": "GB/s", "n_gpus": 0, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(el * 1e3 / args.steps, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "int64/int128 exact, f32 rounding (scalar C)",
+        "data": "synthetic (seeded PCG64)",
+        "config": {"workload": f"8B-class decode stack, {ncols} column(s)", "layers": STACK_LAYERS,
+                   "matrices": [[nm, synth.FORMAT_NAMES[f], r, k] for nm, f, r, k in STACK_MATS + [STACK_OUT]],
+                   "ncols": ncols},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": n, "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
 
 
 def _fp8_inputs(rows, K, ncols, seed):
@@ -1447,8 +1578,7 @@ def main():
     if args.impl == "reference":
         if rank == 0:
             if args.workload in GROUPED:
-                print(json.dumps({"impl": "reference", "unavailable": "the reference arm times single-matrix "
-                                  "workloads; the grouped workload has no oracle timing"}), flush=True)
+                print(json.dumps(run_grouped_reference(args)), flush=True)
             elif args.workload in FFN:
                 print(json.dumps(run_ffn_reference(args)), flush=True)
             elif args.workload in KV:
@@ -1456,9 +1586,7 @@ def main():
             elif args.workload in FP8:
                 print(json.dumps(run_fp8_reference(args)), flush=True)
             elif args.workload in STACK:
-                print(json.dumps({"impl": "reference", "unavailable": "the reference arm times single-matrix "
-                                  "workloads; the 8B-class stack (4.36 GB a step) has no oracle timing"}),
-                      flush=True)
+                print(json.dumps(run_stack_reference(args)), flush=True)
             else:
                 print(json.dumps(run_reference(args)), flush=True)
         return

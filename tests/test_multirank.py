@@ -103,3 +103,19 @@ def test_reference_arm_ffn_block():
     assert d["impl"] == "reference" and d["value"] > 0 and d["cpu_baseline"]["kind"] == "oracle"
     assert d["config"]["down"] == [4096, 14336] and d["config"]["gate_up_rows"] == [14336, 14336]
 
+
+@pytest.mark.parametrize("workload", ["q4k_qkv_4096", "stack_8b_b1"])
+def test_reference_arm_grouped_and_stack(workload):
+    """The reference arm on the grouped Q/K/V workload and on the 8B-class
+    stack: the oracle over sampled rows of the step's matrices, one JSON line."""
+    env = dict(os.environ, RANK="0", WORLD_SIZE="1", LOCAL_RANK="0")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload",
+                        workload, "--steps", "1", "--warmup", "1"], capture_output=True, text=True, env=env,
+                       timeout=900)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["value"] > 0 and d["cpu_baseline"]["kind"] == "oracle"
+    assert d["e2e"]["h2d_bytes_per_step"] == 0
+
