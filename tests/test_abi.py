@@ -85,3 +85,81 @@ def test_matvec_host_argument_checks():
     assert L.q_matvec_host(qb.PERBLOCK, qb.Q4K, P(4096), 4, 256, None, 1, P(4096), P(4096), n, None) == qb.QB_E_ARG
     assert L.q_matvec_host(qb.PERBLOCK, qb.Q4K, P(4096), 4, 256, P(4096), 1, P(4096), P(4096), n - 16,
                            None) == qb.QB_E_ARG
+
+
+def _a16(n):
+    return (n + 15) // 16 * 16
+
+
+def test_workspace_sizes_follow_the_layout():
+    """q_matvec / q_matvec_sub32 workspaces: codes, scales and unit sums, each
+    16-byte aligned (F16: the rounded activation); bad requests refused."""
+    L = qb.lib()
+    for fmt, blk in ((qb.Q8_0, 32), (qb.Q4K, 256), (qb.Q6K, 256)):
+        for K, nc in ((256, 1), (4096, 1), (14336, 3), (1024, 16)):
+            want = _a16(K * nc) + _a16(4 * (K // blk) * nc) + _a16(2 * (K // 16) * nc)
+            assert L.q_matvec_workspace_bytes(fmt, K, nc) == want
+    assert L.q_matvec_workspace_bytes(qb.F16, 576, 2) == _a16(2 * 576 * 2)
+    assert L.q_matvec_workspace_bytes(qb.F16, 12, 1) == qb.QB_E_ARG
+    assert L.q_matvec_workspace_bytes(qb.Q4K, 100, 1) == qb.QB_E_ARG
+    assert L.q_matvec_workspace_bytes(qb.Q4K, 256, 17) == qb.QB_E_ARG
+    assert L.q_matvec_workspace_bytes(99, 256, 1) == qb.QB_E_FORMAT
+    for K, nc in ((256, 1), (4096, 1), (14336, 16)):
+        assert L.q_matvec_sub32_workspace_bytes(K, nc) == _a16(K * nc) + _a16(4 * (K // 32) * nc) + \
+            _a16(2 * (K // 16) * nc)
+    assert L.q_matvec_sub32_workspace_bytes(288, 1) == qb.QB_E_ARG
+    assert L.q_matvec_sub32_workspace_bytes(256, 0) == qb.QB_E_ARG
+
+
+def test_sub32_kv_fp8_grouped_host_checks():
+    """The later entry points' argument checks answer on the host, before any
+    CUDA call; empty requests return 0 without a launch."""
+    L = qb.lib()
+    P = ctypes.c_void_p
+    a, odd = P(4096), P(4097)
+    # Sub32
+    assert L.quantize_act_sub32(a, 288, 1, a, a, a, None) == qb.QB_E_ARG
+    assert L.quantize_act_sub32(a, 256, 17, a, a, a, None) == qb.QB_E_ARG
+    assert L.quantize_act_sub32(odd, 256, 1, a, a, a, None) == qb.QB_E_ARG
+    assert L.quantize_act_sub32(a, 0, 1, a, a, a, None) == qb.QB_OK
+    act256 = qb._Act(256, 4096, 4096, 4096)
+    act32 = qb._Act(32, 4096, 4096, 4096)
+    assert L.q_gemv_sub32(qb.Q4K, a, 4, 256, ctypes.byref(act256), 1, a, None) == qb.QB_E_BLOCK
+    assert L.q_gemv_sub32(qb.F16, a, 4, 256, ctypes.byref(act32), 1, a, None) == qb.QB_E_FORMAT
+    assert L.q_gemv_sub32(qb.Q4K, a, 4, 288, ctypes.byref(act32), 1, a, None) == qb.QB_E_ARG
+    assert L.q_matvec_sub32(99, a, 4, 256, a, 1, a, None, 0, None) == qb.QB_E_FORMAT
+    assert L.q_matvec_sub32(qb.Q4K, a, 0, 256, a, 1, a, None, 0, None) == qb.QB_OK      # no rows
+    assert L.q_matvec_sub32(qb.Q4K, a, 4, 256, a, 3, a, None, 0, None) == qb.QB_E_ARG   # 3 columns need a workspace
+    # the int8 cache
+    assert L.kv_head_codes(qb.SUB32, 128) == 256 and L.kv_head_codes(qb.PERBLOCK, 128) == 128
+    assert L.kv_head_codes(qb.SUB32, 320) == 512
+    for bad in ((2, 128), (qb.PERBLOCK, 8), (qb.PERBLOCK, 1040), (qb.SUB32, 100)):
+        assert L.kv_head_codes(*bad) == qb.QB_E_ARG
+    assert L.kv_cache_rows(None, 4, 128, a, a, None) == qb.QB_E_ARG
+    assert L.kv_cache_rows(a, 4, 100, a, a, None) == qb.QB_E_ARG
+    assert L.kv_cache_rows(odd, 4, 128, a, a, None) == qb.QB_E_ARG
+    assert L.kv_cache_rows(a, 0, 128, a, a, None) == qb.QB_OK
+    assert L.kv_quantize_heads(qb.SUB32, a, 0, 128, a, a, None) == qb.QB_E_ARG
+    assert L.kv_quantize_heads(qb.SUB32, a, 4, 100, a, a, None) == qb.QB_E_ARG
+    args = dict(scaling=qb.PERBLOCK, nh=32, d=128, L=100, lcap=128, nkv=8)
+    def scores(**kw):
+        k = dict(args, **kw)
+        return L.kv_scores(k["scaling"], a, a, k["nh"], k["d"], a, a, k["L"], k["lcap"], k["nkv"], 1.0, a, None)
+    assert scores(nkv=6) == qb.QB_E_ARG          # 32 heads do not share 6 key heads evenly
+    assert scores(lcap=99) == qb.QB_E_ARG        # the cache holds fewer rows than L
+    assert scores(d=100) == qb.QB_E_ARG
+    assert scores(L=0) == qb.QB_OK               # no positions: nothing launched
+    # FP8
+    assert L.q_gemv_fp8(a, a, 4, 40, a, 1, a, None) == qb.QB_E_ARG       # K % 16
+    assert L.q_gemv_fp8(a, a, 4, 48, a, 17, a, None) == qb.QB_E_ARG      # 17 columns
+    assert L.q_gemv_fp8(a, a, 4, 65536, a, 1, a, None) == qb.QB_E_ARG    # K past 32768
+    assert L.q_gemv_fp8(odd, a, 4, 48, a, 1, a, None) == qb.QB_E_ARG
+    assert L.q_gemv_fp8(a, a, 0, 48, a, 1, a, None) == qb.QB_OK
+    # grouped: 1..QB_MAX_MATS matrices, host arrays
+    Ws = (ctypes.c_void_p * 5)(*([4096] * 5))
+    rows = (ctypes.c_int64 * 5)(*([4] * 5))
+    outs = (ctypes.c_void_p * 5)(*([4096] * 5))
+    act = qb._Act(256, 4096, 4096, 4096)
+    assert L.q_gemv_many(qb.Q4K, 0, Ws, rows, 256, ctypes.byref(act), 1, outs, None) == qb.QB_E_ARG
+    assert L.q_gemv_many(qb.Q4K, 5, Ws, rows, 256, ctypes.byref(act), 1, outs, None) == qb.QB_E_ARG
+    assert L.q_gemv_many(qb.Q4K, 2, None, rows, 256, ctypes.byref(act), 1, outs, None) == qb.QB_E_ARG
