@@ -110,6 +110,20 @@ STACK_MATS = [("qkv", synth.FMT_Q4K, 6144, 4096), ("o", synth.FMT_Q4K, 4096, 409
 STACK_OUT = ("output", synth.FMT_Q6K, 128256, 4096)
 
 
+def metric_for(workload):
+    """The metric string of a workload, the same on both arms."""
+    if workload == "q4k_4096x4096":
+        return "weight GB/s at batch 1 (Q4_K-like GEMV 4096x4096, rows/s and fraction of 8 TB/s alongside)"
+    if workload in STACK:
+        return (f"weight GB/s (8B-class decode stack, {STACK[workload]} column(s): 32 layers of Q4_K-like QKV "
+                f"6144x4096, O 4096x4096, gate+up 28672x4096, down 4096x14336 + Q6_K-like output 128256x4096)")
+    if workload in KV:
+        return f"key-cache GB/s ({KV[workload][-1]})"
+    desc = (WORKLOADS[workload][-1] if workload in WORKLOADS else GROUPED[workload][-1] if workload in GROUPED
+            else FFN[workload][-1] if workload in FFN else FP8[workload][-1])
+    return f"weight GB/s ({desc})"
+
+
 def kernel_sources_sha() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "block_quantized_weight_quantize_gb300", "csrc")
@@ -392,7 +406,7 @@ def run_kv(args, rank, world):
     step_s = ms / 1e3
     value = world * kbytes / step_s / 1e9
     res = {
-        "metric": f"key-cache GB/s ({desc})",
+        "metric": metric_for(args.workload),
         "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": nrep * G, "warmup": args.warmup,
         "ms_per_step": round(ms, 6), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "int8 codes x int8 codes (tensor-core s8 MMA), exact int64, f32 rounding",
@@ -522,7 +536,7 @@ def run_grouped(args, rank, world):
     e2e_s = max_over_ranks(time.perf_counter() - t0, dev)
     assert qb.q_device_status() == qb.QB_OK
     res = {
-        "metric": f"weight GB/s ({desc})",
+        "metric": metric_for(args.workload),
         "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": max(1, args.steps // G) * G,
         "warmup": args.warmup, "ms_per_step": round(ms, 6), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "int8 codes x int8 codes, exact int32/int64, f32 rounding",
@@ -581,7 +595,7 @@ def run_grouped_reference(args):
     sample = (f"each step: quantize + {frac:.3g} of the rows of each of the {len(rows_list)} matrices, split over "
               f"{n} threads of the scalar C oracle")
     return {
-        "impl": "reference", "metric": f"weight GB/s ({desc})",
+        "impl": "reference", "metric": metric_for(args.workload),
         "value": round(value, 4), "unit": "GB/s", "n_gpus": 0, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(el * 1e3 / args.steps, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "int64/int128 exact, f32 rounding (scalar C)",
@@ -741,8 +755,7 @@ def run_ours(args, rank, world):
     step_s = ms / 1e3 / args.steps
     value = world * wbytes / step_s / 1e9
     res = {
-        "metric": "weight GB/s at batch 1 (Q4_K-like GEMV 4096x4096, rows/s and fraction of 8 TB/s alongside)"
-        if args.workload == "q4k_4096x4096" else f"weight GB/s ({desc})",
+        "metric": metric_for(args.workload),
         "value": round(value, 2),
         "unit": "GB/s",
         "n_gpus": world,
@@ -993,7 +1006,7 @@ def run_ffn(args, rank, world):
     gu_bytes = sizes[0] + sizes[1] + 4 * K + 8 * rows
     two = False  # Q6_K-like down: the single-launch form (q_matvec's rule)
     res = {
-        "metric": f"weight GB/s ({desc})",
+        "metric": metric_for(args.workload),
         "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": max(1, args.steps // G) * G,
         "warmup": args.warmup, "ms_per_step": round(ms, 6), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "int8 codes x int8 codes, exact int32/int64, f32 rounding",
@@ -1060,7 +1073,7 @@ def run_ffn_reference(args):
     sample = (f"each step: quantize x and h + {frac:.3g} of the rows of gate, up and down, split over {n} threads "
               f"of the scalar C oracle")
     return {
-        "impl": "reference", "metric": f"weight GB/s ({desc})",
+        "impl": "reference", "metric": metric_for(args.workload),
         "value": round(value, 4), "unit": "GB/s", "n_gpus": 0, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(el * 1e3 / args.steps, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "int64/int128 exact, f32 rounding (scalar C)",
@@ -1204,8 +1217,7 @@ def run_stack(args, rank, world):
     nrows = sum(r for _, _, r, _ in STACK_MATS) * STACK_LAYERS + orows
     ops = 2 * ncols * (sum(r * k for _, _, r, k in STACK_MATS) * STACK_LAYERS + orows * oK)
     res = {
-        "metric": f"weight GB/s (8B-class decode stack, {ncols} column(s): 32 layers of Q4_K-like QKV 6144x4096, "
-                  f"O 4096x4096, gate+up 28672x4096, down 4096x14336 + Q6_K-like output 128256x4096)",
+        "metric": metric_for(args.workload),
         "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": nrep * G, "warmup": args.warmup,
         "ms_per_step": round(ms, 6), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "int8 codes x int8 codes, exact int32/int64, f32 rounding",
@@ -1265,8 +1277,7 @@ def run_stack_reference(args):
               f"drawn eighth ({ncols} column(s), quantize + product), split over {n} threads of the scalar C oracle")
     return {
         "impl": "reference",
-        "metric": f"weight GB/s (8B-class decode stack, {ncols} column(s): 32 layers of Q4_K-like QKV 6144x4096, "
-                  f"O 4096x4096, gate+up 28672x4096, down 4096x14336 + Q6_K-like output 128256x4096)",
+        "metric": metric_for(args.workload),
         "value": round(value, 4), "unit": "GB/s", "n_gpus": 0, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(el * 1e3 / args.steps, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "int64/int128 exact, f32 rounding (scalar C)",
@@ -1371,7 +1382,7 @@ def run_fp8(args, rank, world):
         cmax //= 2
     launches = -(-ncols // cmax)
     res = {
-        "metric": f"weight GB/s ({desc})", "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "metric": metric_for(args.workload), "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": nrep * G, "warmup": args.warmup, "ms_per_step": round(ms, 6), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 weights decoded to f32, f32 x, f32 FMA",
         "data": "synthetic (seeded PCG64: uniform E4M3 codes without NaN, log-uniform 2^-12..2^-4 block scales, "
@@ -1485,7 +1496,7 @@ def run_kv_reference(args):
     value = kbytes * (P / L) * args.steps / el / 1e9
     sample = f"each step: cache rows, query heads and scores of {P} of {L} positions, key heads over {n} threads"
     return {
-        "impl": "reference", "metric": f"key-cache GB/s ({desc})", "value": round(value, 4), "unit": "GB/s",
+        "impl": "reference", "metric": metric_for(args.workload), "value": round(value, 4), "unit": "GB/s",
         "n_gpus": 0, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el * 1e3 / args.steps, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "int64 exact, f32 rounding (scalar C)", "data": "synthetic (seeded PCG64)",
@@ -1514,7 +1525,7 @@ def run_fp8_reference(args):
     value = wbytes * (R / rows) * args.steps / el / 1e9
     sample = f"each step: {R} of {rows} rows, over {n} threads of the scalar C oracle"
     return {
-        "impl": "reference", "metric": f"weight GB/s ({desc})", "value": round(value, 4), "unit": "GB/s",
+        "impl": "reference", "metric": metric_for(args.workload), "value": round(value, 4), "unit": "GB/s",
         "n_gpus": 0, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el * 1e3 / args.steps, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 dot (scalar C)",
         "data": "synthetic (seeded PCG64)", "config": {"workload": desc, "rows": rows, "K": K, "ncols": ncols},
@@ -1548,8 +1559,7 @@ def run_reference(args):
     sample = f"each step: quantize + {rows_s} of {rows} rows, split over {n} threads of the scalar C oracle"
     return {
         "impl": "reference",
-        "metric": "weight GB/s at batch 1 (Q4_K-like GEMV 4096x4096, rows/s and fraction of 8 TB/s alongside)"
-        if args.workload == "q4k_4096x4096" else f"weight GB/s ({desc})",
+        "metric": metric_for(args.workload),
         "value": round(value, 4), "unit": "GB/s", "n_gpus": 0, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(el * 1e3 / args.steps, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "int64/int128 exact, f32 rounding (scalar C)",

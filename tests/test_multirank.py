@@ -75,19 +75,6 @@ def test_reference_arm_other_ranks_exit_quietly(rank):
     assert r.stdout.strip() == ""
 
 
-def test_reference_arm_rank0_prints_one_line():
-    """Rank 0 of the reference arm prints one JSON line (a small KV workload keeps it short)."""
-    env = dict(os.environ, RANK="0", WORLD_SIZE="1", LOCAL_RANK="0")
-    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload",
-                        "fp8_4096x4096", "--steps", "1", "--warmup", "1"], capture_output=True, text=True, env=env,
-                       timeout=600)
-    assert r.returncode == 0, r.stderr[-2000:]
-    lines = [l for l in r.stdout.splitlines() if l.strip()]
-    assert len(lines) == 1
-    d = json.loads(lines[0])
-    assert d["impl"] == "reference" and d["value"] > 0 and d["cpu_baseline"]["kind"] == "oracle"
-
-
 def test_reference_arm_ffn_block():
     """The reference arm on the Q6_K-like FFN block (gate and up from one
     activation, down at K = 14336): one JSON line timing the oracle over
@@ -104,10 +91,20 @@ def test_reference_arm_ffn_block():
     assert d["config"]["down"] == [4096, 14336] and d["config"]["gate_up_rows"] == [14336, 14336]
 
 
-@pytest.mark.parametrize("workload", ["q4k_qkv_4096", "stack_8b_b1"])
-def test_reference_arm_grouped_and_stack(workload):
-    """The reference arm on the grouped Q/K/V workload and on the 8B-class
-    stack: the oracle over sampled rows of the step's matrices, one JSON line."""
+def _all_workloads():
+    sys.path.insert(0, ROOT)
+    import bench
+    return (sorted(bench.WORKLOADS) + sorted(bench.GROUPED) + sorted(bench.FFN) + sorted(bench.KV) +
+            sorted(bench.FP8) + sorted(bench.STACK))
+
+
+@pytest.mark.parametrize("workload", _all_workloads())
+def test_reference_arm_every_workload(workload):
+    """Every workload's reference arm (the oracle on the host cores) prints one
+    line with the metric, unit and direction the GPU arm reports, so the two
+    lines compare."""
+    sys.path.insert(0, ROOT)
+    import bench
     env = dict(os.environ, RANK="0", WORLD_SIZE="1", LOCAL_RANK="0")
     r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload",
                         workload, "--steps", "1", "--warmup", "1"], capture_output=True, text=True, env=env,
@@ -116,6 +113,7 @@ def test_reference_arm_grouped_and_stack(workload):
     lines = [l for l in r.stdout.splitlines() if l.strip()]
     assert len(lines) == 1
     d = json.loads(lines[0])
-    assert d["impl"] == "reference" and d["value"] > 0 and d["cpu_baseline"]["kind"] == "oracle"
-    assert d["e2e"]["h2d_bytes_per_step"] == 0
-
+    assert d["impl"] == "reference" and d["value"] > 0
+    assert d["metric"] == bench.metric_for(workload)
+    assert d["unit"] == "GB/s" and d["higher_is_better"] is True
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
