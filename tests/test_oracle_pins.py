@@ -83,6 +83,28 @@ def test_f16_scale_exhaustive(orc):
             assert Fraction(sig) * Fraction(2) ** ex == Fraction(vals[h]), hex(h)
 
 
+def test_f16_to_f32_exhaustive(orc):
+    """The oracle's binary16 -> f32 widening (used by fdot and the key-cache
+    scales) against numpy's, all 65536 patterns: every finite value and the
+    infinities exactly, subnormals included; NaN to NaN."""
+    allh = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    want = allh.view(np.float16).astype(np.float32)
+    for h in range(65536):
+        got = orc.f16_to_f32(h)
+        if np.isnan(want[h]):
+            assert np.isnan(got), hex(h)
+        else:
+            assert bits(got) == bits(want[h]), hex(h)
+
+
+def test_head_width_pads_to_whole_groups(orc):
+    """A quantized query head holds d codes under PerBlock and d rounded up to
+    whole 256-element groups under Sub32 (numerics page: quantize_head, GROUP)."""
+    for d, sub32 in ((64, 256), (96, 256), (128, 256), (256, 256), (320, 512), (1024, 1024)):
+        assert orc.head_width(0, d) == d
+        assert orc.head_width(1, d) == sub32
+
+
 # ---------------------------------------------------------------- absmax
 
 def test_absmax_rules(orc):
