@@ -109,7 +109,20 @@ def _check(rc: int, where: str):
 
 
 def _ptr(t):
-    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+    """Device pointer of a CUDA tensor (None -> NULL).  A CPU tensor is refused
+    here: a kernel handed its host address would fault."""
+    if t is None:
+        return ctypes.c_void_p(0)
+    if not t.is_cuda:
+        raise ValueError("device memory expected, got a CPU tensor")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _hptr(t):
+    """Host pointer of a CPU tensor (q_matvec_host's activation and result)."""
+    if t.is_cuda:
+        raise ValueError("host memory expected, got a CUDA tensor")
+    return ctypes.c_void_p(t.data_ptr())
 
 
 def _stream(stream):
@@ -226,12 +239,12 @@ def q_matvec_host(fmt: int, W, rows: int, K: int, x_host, out_host, workspace, s
     q_matvec_sub32 with scaling=SUB32) and the result copied into out_host f32
     [ncols, rows] (CPU); synchronize the stream before reading it."""
     ncols = x_host.shape[0]
-    _check(lib().q_matvec_host(scaling, fmt, _ptr(W), rows, K, _ptr(x_host), ncols, _ptr(out_host), _ptr(workspace),
+    _check(lib().q_matvec_host(scaling, fmt, _ptr(W), rows, K, _hptr(x_host), ncols, _hptr(out_host), _ptr(workspace),
                                workspace.numel() * workspace.element_size(), _stream(stream)), "q_matvec_host")
 
 
 def _act(block, codes, scales, sums16):
-    return _Act(block, codes.data_ptr(), scales.data_ptr(), sums16.data_ptr() if sums16 is not None else 0)
+    return _Act(block, _ptr(codes).value or 0, _ptr(scales).value or 0, _ptr(sums16).value or 0)
 
 
 def q_gemv(fmt: int, W, rows: int, K: int, act, ncols: int, out, stream=None) -> None:
@@ -315,9 +328,9 @@ def _tables(Ws, rows, outs):
     n = len(Ws)
     if not (len(rows) == n == len(outs)):
         raise ValueError("Ws, rows and outs must have the same length")
-    Wa = (ctypes.c_void_p * n)(*[W.data_ptr() for W in Ws])
+    Wa = (ctypes.c_void_p * n)(*[_ptr(W).value for W in Ws])
     Ra = (ctypes.c_int64 * n)(*[int(r) for r in rows])
-    Oa = (ctypes.c_void_p * n)(*[o.data_ptr() for o in outs])
+    Oa = (ctypes.c_void_p * n)(*[_ptr(o).value for o in outs])
     return n, Wa, Ra, Oa
 
 

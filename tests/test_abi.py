@@ -163,3 +163,26 @@ def test_sub32_kv_fp8_grouped_host_checks():
     assert L.q_gemv_many(qb.Q4K, 0, Ws, rows, 256, ctypes.byref(act), 1, outs, None) == qb.QB_E_ARG
     assert L.q_gemv_many(qb.Q4K, 5, Ws, rows, 256, ctypes.byref(act), 1, outs, None) == qb.QB_E_ARG
     assert L.q_gemv_many(qb.Q4K, 2, None, rows, 256, ctypes.byref(act), 1, outs, None) == qb.QB_E_ARG
+
+
+def test_binding_refuses_host_tensors_for_device_arguments():
+    """A CPU tensor where the library reads or writes device memory is refused
+    by the binding (ValueError) before the library is called -- a kernel handed
+    its host address would fault."""
+    import torch
+    W = torch.zeros(144 * 4, dtype=torch.uint8)
+    x = torch.zeros((1, 256), dtype=torch.float32)
+    out = torch.zeros((1, 4), dtype=torch.float32)
+    with pytest.raises(ValueError):
+        qb.q_matvec(qb.Q4K, W, 4, 256, x, out)
+    act = (torch.zeros((1, 256), dtype=torch.int8), torch.zeros((1, 1), dtype=torch.int32),
+           torch.zeros((1, 16), dtype=torch.int16))
+    with pytest.raises(ValueError):
+        qb.q_gemv(qb.Q4K, W, 4, 256, act, 1, out)
+    with pytest.raises(ValueError):
+        qb.q_gemv_many(qb.Q4K, [W, W], [4, 4], 256, act, 1, [out, out])
+    with pytest.raises(ValueError):
+        qb.q_gemv_fp8(W, torch.ones((1, 2)), 4, 256, x, out)
+    with pytest.raises(ValueError):
+        qb.kv_cache_rows(torch.zeros((4, 128)), torch.zeros((4, 128), dtype=torch.int8),
+                         torch.zeros(4, dtype=torch.int16))
