@@ -319,7 +319,7 @@ def q_matvec_static(fmt: int, W, rows: int, K: int, x, out, stream=None) -> None
     address; make it before any stream capture."""
     ncols = x.shape[0]
     _check(lib().q_matvec_static(fmt, _ptr(W), rows, K, _ptr(x), ncols, _ptr(out), _stream(stream)),
-           "q_matvec_static", "q_gemv_many", "q_gemv_f16_many", "q_matvec_many")
+           "q_matvec_static")
 
 
 # ------------------------------------------------------------------ several matrices, one activation

@@ -14,6 +14,7 @@
 // the process exits.  Host code cannot use the array's name as a device
 // address, so the first call on each device looks the address up with
 // cudaGetSymbolAddress (with that device current) and caches it.
+#include <atomic>
 #include <cstdint>
 
 #include "qb_common.cuh"
@@ -26,17 +27,19 @@ constexpr int64_t kStaticScratchBytes = QB_STATIC_SCRATCH_BYTES;
 static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
 
 // Device address of the scratch array on the current device; the lookup runs
-// once per device and is cached.  Returns nullptr on a CUDA error.
+// once per device and is cached (an entry is only ever set to the one address
+// the device's module gives, so relaxed atomics suffice between host
+// threads).  Returns nullptr on a CUDA error.
 void *static_scratch_address() {
-    static void *cache[64] = {nullptr};
+    static std::atomic<void *> cache[64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-    if (!cache[dev]) {
-        void *p = nullptr;
+    void *p = cache[dev].load(std::memory_order_relaxed);
+    if (!p) {
         if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || p == nullptr) return nullptr;
-        cache[dev] = p;
+        cache[dev].store(p, std::memory_order_relaxed);
     }
-    return cache[dev];
+    return p;
 }
 
 bool misaligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; }
@@ -56,6 +59,14 @@ extern "C" int q_matvec_static(qb_fmt fmt, const void *W, int64_t rows, int64_t 
     } else if (K > (int64_t(1) << 18)) {
         return QB_E_ARG;
     }
+    // no rows, or rows of no blocks: as q_matvec, nothing to launch, or an
+    // output of +0 (the fold of no terms)
+    if (rows == 0) return QB_OK;
+    if (K == 0)
+        return cudaMemsetAsync(out, 0, (size_t)ncols * rows * sizeof(float), static_cast<cudaStream_t>(stream)) ==
+                       cudaSuccess
+                   ? QB_OK
+                   : QB_E_CUDA;
     uint8_t *ws = static_cast<uint8_t *>(static_scratch_address());
     if (!ws) return QB_E_CUDA;
     if (fmt == QB_F16) {

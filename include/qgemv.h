@@ -164,7 +164,12 @@ QB_API int q_matvec(qb_fmt fmt, const void *W, int64_t rows, int64_t K, const fl
  * allocated, by the library or by any routine it calls.
  * - Set-up: the first call on a device (with that device current) looks up
  *   the array's device address (cudaGetSymbolAddress) and caches it; make
- *   that first call before any stream capture.
+ *   that first call before any stream capture.  The cached address belongs
+ *   to the device's context as it was then: after cudaDeviceReset (or any
+ *   other end of that primary context) the library must not be called again
+ *   in the process on that device.
+ * - rows == 0 launches nothing; K == 0 writes +0 to every output (as
+ *   q_matvec) without touching the array.
  * - Sharing: every call on a device uses the same array.  Its contents are
  *   whatever the last call left; nothing in it needs to start at zero, since
  *   each call writes all of the quantized activation it then reads.  Calls

@@ -186,3 +186,5 @@ def test_binding_refuses_host_tensors_for_device_arguments():
     with pytest.raises(ValueError):
         qb.kv_cache_rows(torch.zeros((4, 128)), torch.zeros((4, 128), dtype=torch.int8),
                          torch.zeros(4, dtype=torch.int16))
+    with pytest.raises(ValueError):
+        qb.q_matvec_static(qb.Q4K, W, 4, 256, x, out)

@@ -61,6 +61,41 @@ def test_static_scratch_matches_q_matvec(fmt, rows, K, ncols):
     assert qb.q_device_status() == qb.QB_OK
 
 
+def test_python_wrapper_matches_q_matvec():
+    """The binding's q_matvec_static (argument marshalling only) gives q_matvec's bits."""
+    import torch
+    fmt, rows, K, ncols = synth.FMT_Q4K, 4096, 4096, 1
+    rng = np.random.default_rng(77)
+    W = _dev(synth.pack(fmt, synth.draw(fmt, rng, rows, K)))
+    x = _dev(synth.draw_act(rng, ncols, K, outlier_frac=0.001))
+    got = torch.full((ncols, rows), float("nan"), dtype=torch.float32, device="cuda")
+    want = torch.full((ncols, rows), float("nan"), dtype=torch.float32, device="cuda")
+    for _ in range(2):
+        qb.q_matvec_static(fmt, W, rows, K, x, got)
+        qb.q_matvec(fmt, W, rows, K, x, want)
+        torch.cuda.synchronize()
+        assert np.array_equal(got.cpu().numpy().view(np.uint32), want.cpu().numpy().view(np.uint32))
+
+
+@pytest.mark.parametrize("fmt", [synth.FMT_Q4K, synth.FMT_Q8_0, synth.FMT_F16])
+def test_static_scratch_empty_shapes(fmt):
+    """rows == 0 writes nothing; K == 0 writes +0 to every output (the fold of
+    no terms), as q_matvec does."""
+    import torch
+    W = torch.zeros(64, dtype=torch.uint8, device="cuda")
+    x = torch.zeros((2, 16), dtype=torch.float32, device="cuda")
+    sentinel = torch.full((2, 8), -1.0, dtype=torch.float32, device="cuda")
+    assert _c_static(fmt, W, 0, 0, x, sentinel) == qb.QB_OK
+    K = 256 if fmt != synth.FMT_F16 else 8
+    xk = torch.zeros((2, K), dtype=torch.float32, device="cuda")
+    assert _c_static(fmt, W, 0, K, xk, sentinel) == qb.QB_OK
+    torch.cuda.synchronize()
+    assert bool((sentinel == -1.0).all())
+    assert _c_static(fmt, W, 8, 0, x, sentinel) == qb.QB_OK
+    torch.cuda.synchronize()
+    assert sentinel.cpu().numpy().view(np.uint32).tolist() == [[0] * 8] * 2
+
+
 def test_static_scratch_rejects_oversize_requests():
     import torch
     K, ncols = 1 << 18, 16   # needs ~4.6 MiB of scratch: beyond the 1 MiB array
