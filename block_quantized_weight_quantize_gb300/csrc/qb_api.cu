@@ -4,7 +4,10 @@
 // the device fault word.
 #include <cstdint>
 #include <algorithm>
+#include <atomic>
 #include <cstring>
+#include <mutex>
+#include <vector>
 
 #include "qb_common.cuh"
 #include "qb_launch.h"
@@ -14,28 +17,54 @@ namespace qb {
 __device__ int g_fault = 0;
 __device__ int g_unreadable = 0;
 
+// Per-device caches: each entry is written once per device with the same
+// value by whichever thread gets there first, so relaxed atomics suffice.
 int *fault_word() {
-    static int *cache[64] = {nullptr};
+    static std::atomic<int *> cache[kMaxDevices];
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-    if (!cache[dev]) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_fault) != cudaSuccess) return nullptr;
-        cache[dev] = static_cast<int *>(p);
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    int *p = cache[dev].load(std::memory_order_relaxed);
+    if (!p) {
+        void *q = nullptr;
+        if (cudaGetSymbolAddress(&q, g_fault) != cudaSuccess) return nullptr;
+        p = static_cast<int *>(q);
+        cache[dev].store(p, std::memory_order_relaxed);
     }
-    return cache[dev];
+    return p;
 }
 
 int num_sms() {
-    static int cache[64] = {0};
+    static std::atomic<int> cache[kMaxDevices];
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
-    if (cache[dev] == 0) {
-        int n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 148;
+    int n = cache[dev].load(std::memory_order_relaxed);
+    if (n == 0) {
         if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
-        cache[dev] = n;
+        cache[dev].store(n, std::memory_order_relaxed);
     }
-    return cache[dev];
+    return n;
+}
+
+// The dynamic shared-memory limit is a property of a kernel in one device's
+// context: raise it on the current device the first time a launch there needs
+// it.  The record is per (kernel, device) under a mutex, so host threads that
+// drive one or several devices may launch concurrently.
+int ensure_smem_limit(const void *kernel, int bytes) {
+    if (bytes <= 48 * 1024) return QB_OK;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return QB_E_CUDA;
+    struct Entry { const void *k; int dev; int bytes; };
+    static std::mutex mu;
+    static std::vector<Entry> done;
+    std::lock_guard<std::mutex> lock(mu);
+    for (const Entry &e : done)
+        if (e.k == kernel && e.dev == dev && e.bytes >= bytes) return QB_OK;
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
+        return QB_E_CUDA;
+    for (Entry &e : done)
+        if (e.k == kernel && e.dev == dev) { e.bytes = bytes; return QB_OK; }
+    done.push_back({kernel, dev, bytes});
+    return QB_OK;
 }
 
 // One thread per weight block: an f16 scale with exponent field 31 (inf/NaN).

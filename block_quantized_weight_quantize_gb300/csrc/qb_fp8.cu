@@ -164,13 +164,10 @@ static int launch_fp8_nc(const Fp8K &k, cudaStream_t stream) {
     constexpr int RPW = 2;
     const size_t smem = fp8_smem(NC, k.K);
     const bool full = k.K % 4096 == 0;  // a lane's chunks come in whole batches of 8 rounds of 32
-    static bool attr_set[2] = {false, false};
-    if (!attr_set[full]) {
+    {
         const void *f = full ? reinterpret_cast<const void *>(gemv_fp8_kernel<NC, RPW, true>)
                              : reinterpret_cast<const void *>(gemv_fp8_kernel<NC, RPW, false>);
-        if (cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024) != cudaSuccess)
-            return QB_E_CUDA;
-        attr_set[full] = true;
+        if (ensure_smem_limit(f, 200 * 1024) != QB_OK) return QB_E_CUDA;
     }
     int per_sm = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(

@@ -346,13 +346,8 @@ __global__ void __launch_bounds__(256) gemv_kernel(const GemvK p) {
 
 template <int F, int NC, int MODE>
 int launch_gemv_nc(const GemvK &k, int threads, int smem, unsigned grid, cudaStream_t stream) {
-    static bool attr_set = false;  // per template instance
-    if (!attr_set) {
-        if (cudaFuncSetAttribute(gemv_kernel<F, NC, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 227 * 1024) != cudaSuccess)
-            return QB_E_CUDA;
-        attr_set = true;
-    }
+    if (ensure_smem_limit(reinterpret_cast<const void *>(gemv_kernel<F, NC, MODE>), 227 * 1024) != QB_OK)
+        return QB_E_CUDA;
     return launch_pdl(gemv_kernel<F, NC, MODE>, dim3(grid), dim3(threads), (size_t)smem, stream, k);
 }
 

@@ -570,15 +570,7 @@ int launch_gemv2(const GemvArgs &a, cudaStream_t stream, const float *x = nullpt
     if (L.total > 227 * 1024) return QB_E_ARG;
     const int threads = (k.nt * ts + 31) / 32 * 32;
     if (x && K / 8 > 4 * threads) return QB_E_ARG;  // the in-kernel quantizer holds at most 4 groups a thread
-    static bool attr_set[4] = {false, false, false, false};
-    const int ai = (x ? 2 : 0) + (k.mt.n > 1 ? 1 : 0);
-    auto set_attr = [&](const void *f) {
-        if (attr_set[ai]) return true;
-        if (cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) != cudaSuccess)
-            return false;
-        attr_set[ai] = true;
-        return true;
-    };
+    auto set_attr = [&](const void *f) { return ensure_smem_limit(f, 227 * 1024) == QB_OK; };
     const Gemv2K &k1 = k;  // a one-matrix launch takes the plain parameters
     if (k.mt.n > 1) {
         auto kern = x ? gemv2_kernel<F, true, true> : gemv2_kernel<F, false, true>;

@@ -510,17 +510,11 @@ int launch_gemv3_one(const GemvArgs &a, cudaStream_t stream, const float *x) {
     k.x = x;
     k.fault = fault;
     const bool multi = mt.n > 1;
-    static bool attr_set[4] = {false, false, false, false};
-    const int ai = (multi ? 1 : 0) + (fused ? 2 : 0);
     const void *f = multi ? (fused ? reinterpret_cast<const void *>(gemv3_kernel<F, 1, true, true>)
                                    : reinterpret_cast<const void *>(gemv3_kernel<F, 1, true, false>))
                           : (fused ? reinterpret_cast<const void *>(gemv3_kernel<F, 1, false, true>)
                                    : reinterpret_cast<const void *>(gemv3_kernel<F, 1, false, false>));
-    if (!attr_set[ai]) {
-        if (cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) != cudaSuccess)
-            return QB_E_CUDA;
-        attr_set[ai] = true;
-    }
+    if (ensure_smem_limit(f, 227 * 1024) != QB_OK) return QB_E_CUDA;
     const Gemv3K &k1 = k;
     if (multi)
         return fused ? launch_pdl(gemv3_kernel<F, 1, true, true>, dim3(grid), dim3(threads), (size_t)smem, stream, k)
@@ -548,13 +542,10 @@ int launch_gemv3_cg(const GemvArgs &a, cudaStream_t stream) {
         if (!gemv3_shape<F, CG>(rows, a.K, std::min(per, a.ncols - c0), k, grid, threads, smem)) return QB_E_ARG;
     }
     const bool multi = mt.n > 1;
-    static bool attr_set[2] = {false, false};
-    if (!attr_set[multi]) {
+    {
         const void *f = multi ? reinterpret_cast<const void *>(gemv3_kernel<F, CG, true>)
                               : reinterpret_cast<const void *>(gemv3_kernel<F, CG, false>);
-        if (cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) != cudaSuccess)
-            return QB_E_CUDA;
-        attr_set[multi] = true;
+        if (ensure_smem_limit(f, 227 * 1024) != QB_OK) return QB_E_CUDA;
     }
     for (int c0 = 0; c0 < a.ncols; c0 += per) {
         Gemv3KM k;

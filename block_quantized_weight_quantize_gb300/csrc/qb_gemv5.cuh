@@ -394,13 +394,7 @@ int launch_gemv5(const GemvArgs &a, cudaStream_t stream) {
     k.fault = fault_word();
     if (!k.fault) return QB_E_CUDA;
     const int smem = gemv5_smem(k.K, k.pitch, k.R, k.D, k.vstride).total;
-    static bool attr_set = false;
-    if (!attr_set) {
-        if (cudaFuncSetAttribute(gemv5_kernel<F>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) !=
-            cudaSuccess)
-            return QB_E_CUDA;
-        attr_set = true;
-    }
+    if (ensure_smem_limit(reinterpret_cast<const void *>(gemv5_kernel<F>), 227 * 1024) != QB_OK) return QB_E_CUDA;
     return launch_pdl(gemv5_kernel<F>, dim3(grid), dim3(512), (size_t)smem, stream, k);
 }
 

@@ -239,13 +239,10 @@ int launch_gemv6(const GemvArgs &a, cudaStream_t stream, const float *x) {
     if (!k.fault) return QB_E_CUDA;
     const int smem = gemv6_smem(k.rec, k.D);
     const bool fused = x != nullptr;
-    static bool attr_set[2] = {false, false};
-    if (!attr_set[fused]) {
+    {
         const void *f = fused ? reinterpret_cast<const void *>(gemv6_kernel<F, true>)
                               : reinterpret_cast<const void *>(gemv6_kernel<F, false>);
-        if (cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) != cudaSuccess)
-            return QB_E_CUDA;
-        attr_set[fused] = true;
+        if (ensure_smem_limit(f, 227 * 1024) != QB_OK) return QB_E_CUDA;
     }
     return fused ? launch_pdl(gemv6_kernel<F, true>, dim3(grid), dim3(512), (size_t)smem, stream, k)
                  : launch_pdl(gemv6_kernel<F, false>, dim3(grid), dim3(512), (size_t)smem, stream, k);

@@ -239,14 +239,9 @@ __global__ void __launch_bounds__(256) gemv_f16w_kernel(const F16WK p) {
 
 template <int NC>
 static int launch_f16w_nc(const F16WK &k, int smem, unsigned grid, bool fused, cudaStream_t stream) {
-    static bool attr_set[2] = {false, false};
     const void *f = fused ? reinterpret_cast<const void *>(gemv_f16w_kernel<NC, true>)
                           : reinterpret_cast<const void *>(gemv_f16w_kernel<NC, false>);
-    if (!attr_set[fused]) {
-        if (cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) != cudaSuccess)
-            return QB_E_CUDA;
-        attr_set[fused] = true;
-    }
+    if (ensure_smem_limit(f, 227 * 1024) != QB_OK) return QB_E_CUDA;
     return fused ? launch_pdl(gemv_f16w_kernel<NC, true>, dim3(grid), dim3(32 * k.nw), (size_t)smem, stream, k)
                  : launch_pdl(gemv_f16w_kernel<NC, false>, dim3(grid), dim3(32 * k.nw), (size_t)smem, stream, k);
 }
@@ -361,26 +356,16 @@ template <int NC>
 static int launch_f16_rowthread(const uint16_t *W, int64_t rows, int64_t K, const uint16_t *x16, float *out,
                                 cudaStream_t stream) {
     const size_t smem = (size_t)NC * K * sizeof(float);
-    static bool attr_set = false;
-    if (!attr_set) {
-        if (cudaFuncSetAttribute(gemv_f16_rowthread_kernel<NC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 227 * 1024) != cudaSuccess)
-            return QB_E_CUDA;
-        attr_set = true;
-    }
+    if (ensure_smem_limit(reinterpret_cast<const void *>(gemv_f16_rowthread_kernel<NC>), 227 * 1024) != QB_OK)
+        return QB_E_CUDA;
     const unsigned grid = (unsigned)((rows + 127) / 128);
     return launch_pdl(gemv_f16_rowthread_kernel<NC>, dim3(grid), dim3(128), smem, stream, W, rows, (int)K, x16, out);
 }
 
 template <int NC>
 static int launch_f16_nc(const F16K &k, int smem, unsigned grid, int threads, cudaStream_t stream) {
-    static bool attr_set = false;
-    if (!attr_set) {
-        if (cudaFuncSetAttribute(gemv_f16_kernel<NC>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) !=
-            cudaSuccess)
-            return QB_E_CUDA;
-        attr_set = true;
-    }
+    if (ensure_smem_limit(reinterpret_cast<const void *>(gemv_f16_kernel<NC>), 227 * 1024) != QB_OK)
+        return QB_E_CUDA;
     return launch_pdl(gemv_f16_kernel<NC>, dim3(grid), dim3(threads), (size_t)smem, stream, k);
 }
 

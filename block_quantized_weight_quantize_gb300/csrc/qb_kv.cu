@@ -483,13 +483,8 @@ template <bool S32, int NB>
 static int launch_scores_nb(const KvK &k, cudaStream_t stream) {
     const int smem = kv_smem_bytes<NB>(k.nh);
     if (smem > 113 * 1024) return QB_E_ARG;
-    static bool attr_set = false;
-    if (!attr_set) {
-        if (cudaFuncSetAttribute(kv_scores_kernel<S32, NB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 113 * 1024) != cudaSuccess)
-            return QB_E_CUDA;
-        attr_set = true;
-    }
+    if (ensure_smem_limit(reinterpret_cast<const void *>(kv_scores_kernel<S32, NB>), 113 * 1024) != QB_OK)
+        return QB_E_CUDA;
     // persistent: two CTAs of 8 warps a SM, each warp a contiguous range of tiles
     const int64_t blocks = (k.ntiles + 7) / 8;
     const unsigned grid = (unsigned)std::max<int64_t>(1, std::min<int64_t>(blocks, (int64_t)num_sms() * 2));

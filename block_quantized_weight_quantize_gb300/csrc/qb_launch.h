@@ -109,8 +109,12 @@ int launch_kv_scores(int scaling, const int8_t *qc, const qb_scale *qs, int nh, 
                      const uint16_t *ks, int64_t L, int64_t lcap, int nkv, float scale, float *out,
                      cudaStream_t stream);
 
+constexpr int kMaxDevices = 64;
 int num_sms();
 // Device address of the library's fault word on the current device (NULL on failure).
 int *fault_word();
+// Raises `kernel`'s dynamic shared-memory limit to at least `bytes` on the
+// current device (once per kernel and device; thread-safe).  QB_OK or QB_E_CUDA.
+int ensure_smem_limit(const void *kernel, int bytes);
 
 }  // namespace qb

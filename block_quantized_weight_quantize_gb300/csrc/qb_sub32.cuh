@@ -739,13 +739,10 @@ int launch_s32_cg(const GemvArgs &a, cudaStream_t stream, const float *x = nullp
         int grid, threads, smem;
         if (!s32_shape<F, CG>(a.rows, a.K, std::min(per, a.ncols - c0), k, grid, threads, smem, fused)) return QB_E_ARG;
     }
-    static bool attr_set[2] = {false, false};
-    if (!attr_set[fused]) {
+    {
         const void *f = fused ? reinterpret_cast<const void *>(s32_kernel<F, CG, (CG == 1)>)
                               : reinterpret_cast<const void *>(s32_kernel<F, CG, false>);
-        if (cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) != cudaSuccess)
-            return QB_E_CUDA;
-        attr_set[fused] = true;
+        if (ensure_smem_limit(f, 227 * 1024) != QB_OK) return QB_E_CUDA;
     }
     for (int c0 = 0; c0 < a.ncols; c0 += per) {
         S32K k;
