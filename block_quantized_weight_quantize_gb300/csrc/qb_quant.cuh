@@ -88,7 +88,8 @@ static __device__ __noinline__ int rne_div1_exact(uint32_t xbits, int m, int e) 
 // RN(x' * RN(1/m)) for x' = x * 2^-e, within |x/s| * 2^-23 (1 + 2^-23) <
 // 2^-16 of x/s (|x/s| <= 127).  So unless qf lies within 2^-16 of a
 // half-integer, x/s lies on the same side of every half-integer as qf and its
-// nearest integer is rint(qf).  Elements in that band (exact ties among
+// nearest integer is that of qf, found by one add of 1.5*2^23 (all on the FMA
+// pipe; no conversion instruction).  Elements in that band (exact ties among
 // them), and blocks with e outside the range, take the exact routine.
 // S32: the scale is block_scale (ActScaling::Sub32) instead of wide_scale.
 template <int L, bool S32 = false>
@@ -109,7 +110,7 @@ __device__ __forceinline__ void quantize8(const uint32_t (&xb)[8], uint2 &codes,
     int m, e;
     if (S32) block_scale_bits(amax, m, e);
     else wide_scale_bits(amax, m, e);
-    int q[8];
+    int q[8];  // byte 0 of each: the element's code
     if ((m != 0) & (e >= (S32 ? -130 : -134)) & (e <= (S32 ? 122 : 118))) {
         const float inv_m = __frcp_rn((float)m);
         const float c = __uint_as_float(__float_as_uint(inv_m) - ((uint32_t)e << 23));
@@ -117,8 +118,15 @@ __device__ __forceinline__ void quantize8(const uint32_t (&xb)[8], uint2 &codes,
         for (int i = 0; i < 8; ++i) {
             float qf;
             asm("mul.rn.ftz.f32 %0, %1, %2;" : "=f"(qf) : "f"(__uint_as_float(xb[i])), "f"(c));
-            int v = __float2int_rn(qf);  // NaN: 0
-            if (fabsf(qf - rintf(qf)) >= 0.5f - 0x1p-16f) v = rne_div1_exact(xb[i], m, e);
+            // the nearest integer n of qf, ties to even, on the FMA pipe: |qf| <=
+            // 127 + 2^-16, so qf + 1.5*2^23 rounds (to nearest even) to
+            // 1.5*2^23 + n, an f32 whose bits are 0x4B400000 + n -- byte 0 is n
+            // as an int8; d = qf - n is exact.  The band, and NaN (which fails
+            // every comparison), take the exact routine.
+            const float r = __fadd_rn(qf, 12582912.0f);
+            const float d = __fsub_rn(qf, __fsub_rn(r, 12582912.0f));
+            int v = (int)__float_as_uint(r);
+            if (!(fabsf(d) < 0.5f - 0x1p-16f)) v = rne_div1_exact(xb[i], m, e);
             q[i] = v;
         }
     } else {
