@@ -5,6 +5,7 @@
 #include "qb_gemv.cuh"
 #include "qb_gemv3.cuh"
 #include "qb_gemv6.cuh"
+#include "qb_gemv7.cuh"
 #include "qb_gemv5.cuh"
 
 namespace qb {
@@ -15,6 +16,12 @@ int launch_skinny<kQ4K>(const GemvArgs &a, cudaStream_t stream) {
 }
 template <>
 int launch_one_col3<kQ4K>(const GemvArgs &a, cudaStream_t stream, const float *x) {
+    // K = 4096 (qb_gemv7.cuh): up to 32 rows a CTA with each lane's block held
+    // in registers before the dependency wait, up to 64 rows from shared
+    // memory; two CTAs a SM.  Longer row ranges stream through rings.
+    int r7 = launch_gemv7<kQ4K, 2, 8, true>(a, stream, x);
+    if (r7 == QB_E_ARG) r7 = launch_gemv7<kQ4K, 2, 2, false>(a, stream, x);
+    if (r7 != QB_E_ARG) return r7;
     const int r6 = launch_gemv6<kQ4K>(a, stream, x);  // K = 4096 (qb_gemv6.cuh: which shapes)
     if (r6 != QB_E_ARG) return r6;
     return launch_gemv3_one<kQ4K>(a, stream, x);

@@ -3,6 +3,7 @@
 #include "qb_gemv.cuh"
 #include "qb_gemv3.cuh"
 #include "qb_gemv6.cuh"
+#include "qb_gemv7.cuh"
 
 namespace qb {
 template <>
@@ -11,6 +12,10 @@ int launch_skinny<kQ6K>(const GemvArgs &a, cudaStream_t stream) {
 }
 template <>
 int launch_one_col3<kQ6K>(const GemvArgs &a, cudaStream_t stream, const float *x) {
+    // K = 4096 and up to 64 rows a CTA: a warp per block, a lane per row, two
+    // CTAs a SM (qb_gemv7.cuh); longer row ranges stream through rings
+    const int r7 = launch_gemv7<kQ6K, 2, 4, false>(a, stream, x);
+    if (r7 != QB_E_ARG) return r7;
     const int r6 = launch_gemv6<kQ6K>(a, stream, x);  // K = 4096 (qb_gemv6.cuh: which shapes)
     if (r6 != QB_E_ARG) return r6;
     return launch_gemv3_one<kQ6K>(a, stream, x);

@@ -458,6 +458,35 @@ def test_one_column_long_rows(fmt, rows, K):
     assert np.array_equal(bits(host(out)), bits(want))
 
 
+@pytest.mark.parametrize("fmt", [synth.FMT_Q4K, synth.FMT_Q6K])
+@pytest.mark.parametrize("rows", [1, 31, 152, 152 * 31 + 7, 152 * 32, 152 * 32 + 1, 152 * 64, 152 * 64 + 1])
+def test_k4096_row_ranges(fmt, rows):
+    """One column at K = 4096 across the row counts where the kernel changes
+    form: up to 32 rows a CTA (a lane per row, each lane's block held in
+    registers from before the dependency wait), 33..64 (blocks read from
+    shared memory, two rows a lane), and past the shared-memory budget (the
+    warp-ring kernel) -- from a quantized activation and from the f32
+    activation in one launch, both equal to the oracle."""
+    import torch
+    K = 4096
+    x = _edge_activation(1, K, 256, seed=rows + fmt)
+    x[0, 5 * 256 + 1] = 3.0   # no infinity: every row a finite value, not the engine's NaN
+    rng = np.random.default_rng(rows * 7 + fmt)
+    W = synth.pack(fmt, synth.draw(fmt, rng, rows, K))
+    codes, m, e, s16, packed = oracle_act(x, 256)
+    want = oracle.gemv(fmt, W, rows, K, codes, m, e)
+    act = qb.alloc_act(1, K, 256)
+    qb.quantize_act(256, dev(x), *act)
+    out = torch.full((1, rows), float("nan"), dtype=torch.float32, device="cuda")
+    qb.q_gemv(fmt, dev(W), rows, K, act, 1, out)
+    torch.cuda.synchronize()
+    assert np.array_equal(bits(host(out)), bits(want))
+    out.fill_(float("nan"))
+    qb.q_matvec(fmt, dev(W), rows, K, dev(x), out)
+    torch.cuda.synchronize()
+    assert np.array_equal(bits(host(out)), bits(want))
+
+
 def test_matvec_repeated_launches_graph():
     """Many single-launch products back to back (programmatic dependent launch
     overlapping each launch's weight stream with the previous one) on distinct
