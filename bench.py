@@ -152,6 +152,82 @@ def max_over_ranks(v, device=None) -> float:
     return float(t.item())
 
 
+def lead_in(stream) -> None:
+    """Queues ~0.1 ms of spinning on the stream right before the timed region's
+    first event, so that the host has submitted the timed graph before the GPU
+    reaches it: otherwise the first replay's host-side submission (tens of us)
+    is counted as idle GPU time inside the region, which at a few dozen steps
+    inflates the step time by tens of percent."""
+    import torch
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(200_000)
+
+
+def one_graph_timing(capture_steps, stream, warmup, steps, max_steps=1000):
+    """For a run of at most `max_steps` timed steps: captures one CUDA graph of
+    `warmup` untimed steps followed by the `steps` timed ones, with the start
+    event recorded on a branch that waits for the last warm-up step to
+    complete and the end event after the last timed step.  The launch chain
+    itself is left as in a long run -- each step's launch may begin while its
+    predecessor drains (programmatic dependent launch) -- so the events span
+    exactly `steps` step completions of a running pipeline: an event between
+    two launches would instead hold the next one back until the previous one
+    finished.  Replays the graph once untimed and returns (graph, start
+    event, end event), or None where this torch cannot record events as graph
+    nodes, or the run is longer."""
+    import torch
+    if steps > max_steps:
+        return None
+    try:
+        t0 = torch.cuda.Event(enable_timing=True, external=True)
+        t1 = torch.cuda.Event(enable_timing=True, external=True)
+    except TypeError:  # no event record nodes in this torch
+        return None
+    side = torch.cuda.Stream(stream.device)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        g.capture_begin()
+        try:
+            capture_steps(0, max(1, warmup))
+            fork = torch.cuda.Event()
+            fork.record(stream)
+            side.wait_event(fork)
+            t0.record(side)
+            capture_steps(max(1, warmup), steps)
+            t1.record(stream)
+            join = torch.cuda.Event()
+            join.record(side)
+            stream.wait_event(join)
+        finally:
+            g.capture_end()
+    with torch.cuda.stream(stream):
+        g.replay()
+    stream.synchronize()
+    return g, t0, t1
+
+
+def prime_graph(g, stream) -> str:
+    """Readies a captured CUDA graph so that its first replay inside a timed
+    region costs what every later one does: the instantiated graph is uploaded
+    to the device (cuGraphUpload) ahead of the timing.  Where the executable
+    graph's handle is not reachable from this torch, the graph is replayed once,
+    untimed, instead.  Returns which of the two was done."""
+    import ctypes
+    import torch
+    try:
+        h = g.raw_cuda_graph_exec()
+        rc = ctypes.CDLL("libcuda.so.1").cuGraphUpload(ctypes.c_void_p(h), ctypes.c_void_p(stream.cuda_stream))
+        if rc == 0:
+            stream.synchronize()
+            return "uploaded before timing"
+    except Exception:
+        pass
+    with torch.cuda.stream(stream):
+        g.replay()
+    stream.synchronize()
+    return "replayed once untimed before timing"
+
+
 def traffic_for(workload):
     """DRAM bytes per launch of the workload's dominant kernel from the committed
     ncu summary, or None when the kernels changed since that capture."""
@@ -261,13 +337,29 @@ def one_col_gemv6(fmt, rows, K):
     return fmt == synth.FMT_Q6K or (rows + g - 1) // g <= 48
 
 
+def one_col_gemv7(fmt, rows, K):
+    """The library's rule for the block-per-warp one-column kernel: K = 4096,
+    rows a CTA (over min(152, rows) CTAs) up to 32, or as many as fit the
+    shared-memory budget of two CTAs a SM (Q4_K-like 45, Q6_K-like 31)."""
+    if fmt not in (synth.FMT_Q4K, synth.FMT_Q6K) or K != 4096 or rows < 1:
+        return False
+    g = max(1, min(152, rows))
+    per = (rows + g - 1) // g
+    pitch = synth.weight_bytes(fmt, 1, K) + 16
+    smem = 9088 + per * pitch   # codes, sums, the block-value table, the rows
+    return (fmt == synth.FMT_Q4K and per <= 32) or smem <= (228 * 1024) // 2 - 1024 - 256
+
+
 def roofline(fmt, ncols, single, achieved, peak, peak_kind, traffic, roof_bytes, per_launch_s, prod_s, abytes,
              ops_per_step, roof_launches, sub32=False, rows=0, K=0):
-    g6 = ncols == 1 and not sub32 and fmt != synth.FMT_F16 and one_col_gemv6(fmt, rows, K)
+    g7 = ncols == 1 and not sub32 and fmt != synth.FMT_F16 and one_col_gemv7(fmt, rows, K)
+    g6 = ncols == 1 and not sub32 and fmt != synth.FMT_F16 and not g7 and one_col_gemv6(fmt, rows, K)
     g3 = ncols == 1 and not sub32 and fmt != synth.FMT_F16 and not g6 and one_col_gemv3(fmt, rows, K)
     g6name = (f"gemv6_kernel<{synth.FORMAT_NAMES[fmt]}, one column, warp rings" +
               (", single launch> (quantize + product)" if single else ">"))
-    name = (g6name if g6 else
+    g7name = (f"gemv7_kernel<{synth.FORMAT_NAMES[fmt]}, one column, a warp per block, a lane per row" +
+              (", single launch> (quantize + product)" if single else ">"))
+    name = (g7name if g7 else g6name if g6 else
             f"gemv_f16w_kernel<{ncols}{', single launch (f16 rounding in the prologue)' if single else ''}>"
             if fmt == synth.FMT_F16 else
             (f"s32_kernel<{synth.FORMAT_NAMES[fmt]}, one column, single launch> (quantize + product)" if single
@@ -365,10 +457,12 @@ def run_kv(args, rank, world):
         for _ in range(max(1, args.warmup // max(1, min(args.warmup, G)))):
             g_w.replay()
     stream.synchronize()
+    primed = prime_graph(g_main, stream)
     nrep = max(1, args.steps // G)
     with ClockSampler(dev.index) as clk:
         barrier()
         torch.cuda.synchronize()
+        lead_in(stream)
         with torch.cuda.stream(stream):
             e0.record(stream)
             for _ in range(nrep):
@@ -416,7 +510,7 @@ def run_kv(args, rank, world):
                    "l2": f"each step reads a different one of {ncopy} key caches ({ncopy * kbytes / 2**20:.0f} MiB "
                          f"> 4x L2); no flush",
                    "timing": f"CUDA graphs of {G} steps (kv_quantize_heads + kv_scores, 2 launches a step); "
-                             f"CUDA events on the launching stream",
+                             f"CUDA events on the launching stream; the timed graph {primed}",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "scores_per_s": round(world * nh * L / step_s, 1),
         "frac_of_8tbs": round(value / 8000.0, 4), "frac_of_measured_copy": round(value / peak, 4),
@@ -497,11 +591,13 @@ def run_grouped(args, rank, world):
             for _ in range(max(1, args.warmup // max(1, min(args.warmup, G)))):
                 gw.replay()
         stream.synchronize()
+        prime_graph(g, stream)
         sampler = ClockSampler(dev.index) if clocks else None
         if sampler:
             sampler.__enter__()
         barrier()
         torch.cuda.synchronize()
+        lead_in(stream)
         with torch.cuda.stream(stream):
             e0.record(stream)
             for _ in range(max(1, steps // G)):
@@ -553,7 +649,7 @@ def run_grouped(args, rank, world):
         "frac_of_8tbs": round(value / 8000.0, 4), "frac_of_measured_copy": round(value / peak, 4),
         "gpu_launches": max(1, args.steps // G) * G, "clocks": clocks,
         "roofline": {"bound": "hbm",
-                     "kernel": f"{'gemv6_kernel' if one_col_gemv6(fmt, sum(rows_list), K) else 'gemv3_kernel' if one_col_gemv3(fmt, sum(rows_list), K) else 'gemv2_kernel'}"
+                     "kernel": f"{'gemv7_kernel' if one_col_gemv7(fmt, sum(rows_list), K) else 'gemv6_kernel' if one_col_gemv6(fmt, sum(rows_list), K) else 'gemv3_kernel' if one_col_gemv3(fmt, sum(rows_list), K) else 'gemv2_kernel'}"
                                f"<{synth.FORMAT_NAMES[fmt]}, one column, single launch, grouped>",
                      "achieved": round(roof_bytes / step_s / 1e9, 1), "peak": peak,
                      "peak_kind": f"{peak_kind} (HBM copy, burst)", "unit": "GB/s",
@@ -691,19 +787,37 @@ def run_ours(args, rank, world):
         for _ in range(max(1, args.warmup // max(1, min(args.warmup, G)))):
             g_w.replay()
     stream.synchronize()
+    primed = prime_graph(g_main, stream)
+    if g_rem is not None:
+        prime_graph(g_rem, stream)
 
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
+    g_one = one_graph_timing(capture_steps=lambda n0, n: [step(n0 + i, stream) for i in range(n)],
+                             stream=stream, warmup=args.warmup, steps=args.steps)
     with ClockSampler(dev.index) as clk:
         barrier()
         torch.cuda.synchronize()
-        with torch.cuda.stream(stream):
-            e0.record(stream)
-            replay_steps(args.steps // G, g_rem)
-            e1.record(stream)
-        torch.cuda.synchronize()
-        barrier()
-    ms = max_over_ranks(e0.elapsed_time(e1), dev)
+        if g_one is not None:
+            # W warm-up steps, then the K timed steps between two event nodes,
+            # all in one graph: the first timed step follows a warm pipeline
+            g, t0, t1 = g_one
+            with torch.cuda.stream(stream):
+                g.replay()
+            torch.cuda.synchronize()
+            barrier()
+            ms = max_over_ranks(t0.elapsed_time(t1), dev)
+            primed = ("holds the W warm-up steps and the K timed ones; the start event waits on a branch for the "
+                      "last warm-up step, the end event follows the last timed step (one untimed replay first)")
+        else:
+            lead_in(stream)
+            with torch.cuda.stream(stream):
+                e0.record(stream)
+                replay_steps(args.steps // G, g_rem)
+                e1.record(stream)
+            torch.cuda.synchronize()
+            barrier()
+            ms = max_over_ranks(e0.elapsed_time(e1), dev)
     clocks = clk.summary()
 
     # ---- roofline: the step's dominant kernel, live, over rotating copies.  For a
@@ -777,7 +891,7 @@ def run_ours(args, rank, world):
             "timing": f"CUDA graphs of {G} steps ({'q_matvec_sub32' if sub32 else 'q_matvec'}: activation "
                       f"quantization + product, "
                       f"{launches_per_step} launch(es) a step, programmatic dependent launch) replayed; "
-                      f"CUDA events on the launching stream",
+                      f"CUDA events on the launching stream; the timed graph {primed}",
             "parallelism": "replicas" if world > 1 else "single GPU",
         },
         "rows_per_s": round(world * rows / step_s, 1),
@@ -968,6 +1082,7 @@ def run_ffn(args, rank, world):
             sampler.__enter__()
         barrier()
         torch.cuda.synchronize()
+        lead_in(stream)
         with torch.cuda.stream(stream):
             e0.record(stream)
             for _ in range(max(1, steps // G)):
@@ -1173,6 +1288,7 @@ def run_stack(args, rank, world):
     with ClockSampler(dev.index) as clk:
         barrier()
         torch.cuda.synchronize()
+        lead_in(stream)
         with torch.cuda.stream(stream):
             e0.record(stream)
             for _ in range(nrep):
@@ -1345,10 +1461,12 @@ def run_fp8(args, rank, world):
         for _ in range(max(1, args.warmup // max(1, min(args.warmup, G)))):
             g_w.replay()
     stream.synchronize()
+    primed = prime_graph(g_main, stream)
     nrep = max(1, args.steps // G)
     with ClockSampler(dev.index) as clk:
         barrier()
         torch.cuda.synchronize()
+        lead_in(stream)
         with torch.cuda.stream(stream):
             e0.record(stream)
             for _ in range(nrep):
@@ -1390,7 +1508,8 @@ def run_fp8(args, rank, world):
         "config": {"workload": desc, "rows": rows, "K": K, "ncols": ncols, "weight_bytes_per_step": wbytes,
                    "l2": f"each step reads a different one of {ncopy} weight copies "
                          f"({ncopy * wbytes / 2**20:.0f} MiB > 4x L2); no flush",
-                   "timing": f"CUDA graphs of {G} steps, one q_gemv_fp8 launch a step; CUDA events",
+                   "timing": f"CUDA graphs of {G} steps, one q_gemv_fp8 launch a step; CUDA events; "
+                             f"the timed graph {primed}",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "rows_per_s": round(world * rows / step_s, 1), "tops": round(world * ops / step_s / 1e12, 3),
         "frac_of_8tbs": round(value / 8000.0, 4), "frac_of_measured_copy": round(value / peak, 4),
