@@ -94,18 +94,22 @@ static __device__ __noinline__ int rne_div1_exact(uint32_t xbits, int m, int e) 
 // S32: the scale is block_scale (ActScaling::Sub32) instead of wide_scale.
 template <int L, bool S32 = false>
 __device__ __forceinline__ void quantize8(const uint32_t (&xb)[8], uint2 &codes, int &unit_sum, uint32_t &scale) {
-    float am = 0.0f;
+    float ax[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        float ax;
-        asm("abs.ftz.f32 %0, %1;" : "=f"(ax) : "f"(__uint_as_float(xb[i])));
-        am = fmaxf(am, ax);
-    }
-    uint32_t amax = __float_as_uint(am);
+    for (int i = 0; i < 8; ++i) asm("abs.ftz.f32 %0, %1;" : "=f"(ax[i]) : "f"(__uint_as_float(xb[i])));
+    // a tree of fmaxf (a NaN operand yields the other), then against +0: the
+    // same maximum as folding from +0 in any order
+    const float am = fmaxf(0.0f, fmaxf(fmaxf(fmaxf(ax[0], ax[1]), fmaxf(ax[2], ax[3])),
+                                       fmaxf(fmaxf(ax[4], ax[5]), fmaxf(ax[6], ax[7]))));
+    uint32_t amax = __float_as_uint(am);  // non-negative: ordered as an unsigned integer
+    if (L == 32) {
+        amax = __reduce_max_sync(0xFFFFFFFFu, amax);
+    } else {
 #pragma unroll
-    for (int o = L / 2; o > 0; o >>= 1) {
-        const uint32_t u = __shfl_xor_sync(0xFFFFFFFFu, amax, o);
-        amax = u > amax ? u : amax;
+        for (int o = L / 2; o > 0; o >>= 1) {
+            const uint32_t u = __shfl_xor_sync(0xFFFFFFFFu, amax, o);
+            amax = u > amax ? u : amax;
+        }
     }
     int m, e;
     if (S32) block_scale_bits(amax, m, e);

@@ -88,6 +88,43 @@ def test_quantize_act_bit_exact(block, K, ncols):
     assert np.array_equal(host(gsum), s16)
 
 
+def test_quantize_every_scale_significand():
+    """Blocks whose absmax is exactly 127*m*2^e for every m in 128..255 (so
+    wide_scale picks that m), filled with values drawn over the whole range and
+    with halfway points k*s + s/2, quantized by quantize_act and inside the
+    single-launch product's prologue (q_matvec), equal the oracle's codes and
+    rows: the reciprocal of each m the fast path scales by is the right one."""
+    import torch
+    rng = np.random.default_rng(4242)
+    nb = 128
+    K = 256 * nb
+    x = np.empty((1, K), np.float32)
+    for i, m in enumerate(range(128, 256)):
+        e = int(rng.integers(-20, 10))
+        s = np.float64(m) * 2.0 ** e
+        blk = rng.uniform(-127 * s, 127 * s, 256)
+        blk[:64] = (rng.integers(-127, 127, 64) + 0.5) * s        # halfway points, exact in f32
+        blk[64] = 127 * s                                           # the block's absmax
+        x[0, 256 * i:256 * (i + 1)] = blk.astype(np.float32)
+    codes, m, e, s16, packed = oracle_act(x, 256)
+    assert sorted(set(m.ravel().tolist())) == list(range(128, 256))
+    gc, gs, gsum = gpu_quantize(x, 256)
+    assert np.array_equal(host(gc), codes)
+    gm, ge = unpack_scales(host(gs))
+    assert np.array_equal(gm, m) and np.array_equal(ge, e)
+    assert np.array_equal(host(gsum), s16)
+    # the same blocks through the single-launch product (K = 4096 slices)
+    for j in range(nb // 16):
+        xs = np.ascontiguousarray(x[:, 4096 * j:4096 * (j + 1)])
+        W = synth.pack_q4k(**synth.draw_q4k(rng, 300, 4096))
+        cj, mj, ej, _, _ = oracle_act(xs, 256)
+        want = oracle.gemv(synth.FMT_Q4K, W, 300, 4096, cj, mj, ej)
+        out = torch.full((1, 300), float("nan"), dtype=torch.float32, device="cuda")
+        qb.q_matvec(synth.FMT_Q4K, dev(W), 300, 4096, dev(xs), out)
+        torch.cuda.synchronize()
+        assert np.array_equal(bits(host(out)), bits(want)), j
+
+
 # ---------------------------------------------------------------- block values (the lane)
 
 SHAPES = {synth.FMT_Q8_0: [(37, 1024), (129, 2048), (5, 32)],
