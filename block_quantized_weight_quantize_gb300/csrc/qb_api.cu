@@ -291,9 +291,11 @@ int q_matvec(qb_fmt fmt, const void *W, int64_t rows, int64_t K, const float *x,
         // other way round).
         const bool two = f == kQ4K && K >= 12288 && workspace && (int64_t)workspace_bytes >= need &&
                          !misaligned(workspace);
-        if (ncols == 1 && !two) {
+        // one launch: a single column, or 2..4 columns of the 256-element
+        // formats at K = 4096 (each warp quantizes its block of every column)
+        if ((ncols == 1 || (ncols <= 4 && K == 4096 && f != kQ8_0)) && !two) {
             GemvArgs a = {};
-            a.W = W; a.rows = rows; a.K = K; a.ncols = 1; a.out = out; a.mode = 0;
+            a.W = W; a.rows = rows; a.K = K; a.ncols = ncols; a.out = out; a.mode = 0;
             const int r = f == kQ8_0 ? launch_matvec_q8_0(a, x, s)
                         : f == kQ4K  ? launch_matvec_q4k(a, x, s)
                                      : launch_matvec_q6k(a, x, s);

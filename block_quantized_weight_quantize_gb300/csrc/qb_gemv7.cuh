@@ -91,6 +91,58 @@ __device__ __forceinline__ void block_q4k(const uint8_t *blk, const uint8_t *a, 
     O = dp2a_hi_su(sw.w, mb1, dp2a_lo_su(sw.z, mb1, dp2a_hi_su(sw.y, mb0, dp2a_lo_su(sw.x, mb0, 0))));
 }
 
+// block_q4k for two activation columns at once (codes a0/a1, sums S0/S1): the
+// weights are read and unpacked once for both.
+template <int UNR>
+__device__ __forceinline__ void block_q4k_pair(const uint8_t *blk, const uint8_t *a0, const uint8_t *a1,
+                                               const int16_t *S0, const int16_t *S1, int &C0, int &O0, int &C1,
+                                               int &O1, uint32_t &dd) {
+    const uint4 meta = *reinterpret_cast<const uint4 *>(blk);
+    dd = meta.x;
+    const unsigned long long sc48 = (unsigned long long)meta.y | ((unsigned long long)(meta.z & 0xFFFFu) << 32);
+    const unsigned long long mn48 = (unsigned long long)(meta.z >> 16) | ((unsigned long long)meta.w << 16);
+    int c0 = 0, c1 = 0;
+#pragma unroll UNR
+    for (int s = 0; s < 8; ++s) {
+        const uint4 w = *reinterpret_cast<const uint4 *>(blk + 16 + 16 * s);
+        const uint32_t l[4] = {w.x & 0x0F0F0F0Fu, w.y & 0x0F0F0F0Fu, w.z & 0x0F0F0F0Fu, w.w & 0x0F0F0F0Fu};
+        const uint32_t g[4] = {w.x & 0xF0F0F0F0u, w.y & 0xF0F0F0F0u, w.z & 0xF0F0F0F0u, w.w & 0xF0F0F0F0u};
+        const int sc = (int)((sc48 >> (6 * s)) & 63u);
+        {
+            const uint4 al = *reinterpret_cast<const uint4 *>(a0 + 32 * s);
+            const uint4 ah = *reinterpret_cast<const uint4 *>(a0 + 32 * s + 16);
+            int pl = dp4a_ss(l[0], al.x, 0);
+            pl = dp4a_ss(l[1], al.y, pl);
+            pl = dp4a_ss(l[2], al.z, pl);
+            pl = dp4a_ss(l[3], al.w, pl);
+            int ph = dp4a_us(g[0], ah.x, 0);
+            ph = dp4a_us(g[1], ah.y, ph);
+            ph = dp4a_us(g[2], ah.z, ph);
+            ph = dp4a_us(g[3], ah.w, ph);
+            c0 += sc * (16 * pl + ph);
+        }
+        {
+            const uint4 al = *reinterpret_cast<const uint4 *>(a1 + 32 * s);
+            const uint4 ah = *reinterpret_cast<const uint4 *>(a1 + 32 * s + 16);
+            int pl = dp4a_ss(l[0], al.x, 0);
+            pl = dp4a_ss(l[1], al.y, pl);
+            pl = dp4a_ss(l[2], al.z, pl);
+            pl = dp4a_ss(l[3], al.w, pl);
+            int ph = dp4a_us(g[0], ah.x, 0);
+            ph = dp4a_us(g[1], ah.y, ph);
+            ph = dp4a_us(g[2], ah.z, ph);
+            ph = dp4a_us(g[3], ah.w, ph);
+            c1 += sc * (16 * pl + ph);
+        }
+    }
+    C0 = c0;
+    C1 = c1;
+    const uint32_t mb0 = spread6((uint32_t)mn48 & 0xFFFFFFu), mb1 = spread6((uint32_t)(mn48 >> 24));
+    const uint4 s0 = *reinterpret_cast<const uint4 *>(S0), s1 = *reinterpret_cast<const uint4 *>(S1);
+    O0 = dp2a_hi_su(s0.w, mb1, dp2a_lo_su(s0.z, mb1, dp2a_hi_su(s0.y, mb0, dp2a_lo_su(s0.x, mb0, 0))));
+    O1 = dp2a_hi_su(s1.w, mb1, dp2a_lo_su(s1.z, mb1, dp2a_hi_su(s1.y, mb0, dp2a_lo_su(s1.x, mb0, 0))));
+}
+
 // Q6_K-like block at blk (ql, qh, 16 int8 sub-scales) against the warp's codes a
 // and unit sums S (16 int16): C = sum over the 16 units of sc_u * sum (q - 32)*a.
 template <int UNR>
@@ -311,6 +363,201 @@ int launch_gemv7(const GemvArgs &a, cudaStream_t stream, const float *x) {
     auto kern = x ? gemv7_kernel<F, true, MINB, UNR, PRE> : gemv7_kernel<F, false, MINB, UNR, PRE>;
     if (ensure_smem_limit(reinterpret_cast<const void *>(kern), smem) != QB_OK) return QB_E_CUDA;
     return launch_pdl(kern, dim3(grid), dim3(kG7Warps * 32), (size_t)smem, stream, k);
+}
+
+// shared memory for NC columns: the mbarrier, each column's block scales,
+// codes (each warp's 256) and int16 sums (each warp's 16), the block-value table ([row][column][17],
+// its row stride made odd so the lanes of a warp -- one row each -- write
+// different banks), then the rows
+__host__ __device__ constexpr int gemv7m_vs(int nc) { return (nc * 17) | 1; }
+struct Gemv7MSmem {
+    int scl, act, sums, vals, slab;
+};
+__host__ __device__ inline Gemv7MSmem gemv7m_layout(int nc) {
+    Gemv7MSmem s;
+    s.scl = 128;  // nc x 16 block scales
+    s.act = s.scl + ((nc * kG7Warps * 4 + 127) & ~127);
+    s.sums = s.act + nc * kG7K;
+    s.vals = s.sums + nc * kG7Warps * 32;
+    s.slab = s.vals + ((kG7MaxRows * gemv7m_vs(nc) * 4 + 127) & ~127);
+    return s;
+}
+__host__ __device__ inline int gemv7m_smem(int nc, int rows, int pitch) { return gemv7m_layout(nc).slab + rows * pitch; }
+
+// NC activation columns (2..4) in one launch: each warp prepares block w of
+// every column (quantizing it in the single-launch form), each lane forms its
+// rows' block w for every column from the one copy of the weights in shared
+// memory, column by column.
+template <int F, bool FUSED, int MINB, int UNR, int NC>
+__global__ void __launch_bounds__(kG7Warps * 32, MINB) gemv7m_kernel(const Gemv7K p) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    const Gemv7MSmem Lo = gemv7m_layout(NC);
+    constexpr int VS = gemv7m_vs(NC);
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem);
+    uint32_t *sclw = reinterpret_cast<uint32_t *>(smem + Lo.scl) + w;  // column c at + c * 16
+    uint8_t *aw = smem + Lo.act + 256 * w;                             // column c at + c * K
+    int16_t *Sw = reinterpret_cast<int16_t *>(smem + Lo.sums + 32 * w);  // column c at + c * 256
+    float *vals = reinterpret_cast<float *>(smem + Lo.vals);
+    uint8_t *slab = smem + Lo.slab;
+
+    const int64_t c = blockIdx.x;
+    const int64_t row0 = c * p.base + (c < p.rem ? c : p.rem);
+    const int count = (int)(p.base + (c < p.rem ? 1 : 0));
+
+    if (tid == 0) {
+        mbar_init(bar, 1);
+        fence_mbar_init();
+        mbar_arrive_expect_tx(bar, (uint32_t)(count * p.rec));
+    }
+    __syncthreads();
+    // the CTA's rows (weights depend on no earlier kernel)
+    if (w == 0)
+        for (int r = lane; r < count; r += 32)
+            bulk_g2s(slab + r * p.pitch, row_ptr(p.mt, row0 + r, p.rec), (uint32_t)p.rec, bar);
+    // the next launch may be scheduled now: it reads nothing this one writes
+    // before its own pdl_wait, which returns once this grid has finished
+    pdl_launch_dependents();
+    pdl_wait();
+
+    // ---- block w of the activation, each column: codes (natural order), the
+    // sums the format needs (Q4_K-like: per 32-element sub-block; Q6_K-like:
+    // per 16-element unit) and the block's scale
+#pragma unroll
+    for (int col = 0; col < NC; ++col) {
+        uint32_t scale;
+        uint8_t *ac = aw + col * kG7K;
+        int16_t *Sc = Sw + col * (kG7Warps * 16);
+        if constexpr (FUSED) {
+            const float4 *xp = reinterpret_cast<const float4 *>(p.x + (int64_t)col * kG7K + 256 * w + 8 * lane);
+            const float4 v0 = ldg_f4_ordered(xp), v1 = ldg_f4_ordered(xp + 1);
+            const uint32_t xb[8] = {__float_as_uint(v0.x), __float_as_uint(v0.y), __float_as_uint(v0.z),
+                                    __float_as_uint(v0.w), __float_as_uint(v1.x), __float_as_uint(v1.y),
+                                    __float_as_uint(v1.z), __float_as_uint(v1.w)};
+            uint2 cd;
+            int usum;  // the sum of the 16-element unit of this lane pair
+            quantize8<32>(xb, cd, usum, scale);
+            *reinterpret_cast<uint2 *>(ac + 8 * lane) = cd;
+            if (F == kQ4K) {
+                const int s2 = usum + __shfl_down_sync(0xFFFFFFFFu, usum, 2);
+                if ((lane & 3) == 0) Sc[lane >> 2] = (int16_t)s2;
+            } else {
+                if ((lane & 1) == 0) Sc[lane >> 1] = (int16_t)usum;
+            }
+        } else {
+            const uint2 cd = *reinterpret_cast<const uint2 *>(p.codes + (int64_t)col * kG7K + 256 * w + 8 * lane);
+            *reinterpret_cast<uint2 *>(ac + 8 * lane) = cd;
+            const int us = lane < 16 ? (int)p.sums16[(int64_t)col * (kG7K / 16) + 16 * w + lane] : 0;
+            if (F == kQ4K) {
+                const int s2 = us + __shfl_down_sync(0xFFFFFFFFu, us, 1);
+                if (lane < 16 && (lane & 1) == 0) Sc[lane >> 1] = (int16_t)s2;
+            } else {
+                if (lane < 16) Sc[lane] = (int16_t)us;
+            }
+            scale = reinterpret_cast<const uint32_t *>(p.scales)[col * kG7Warps + w];
+        }
+        if (lane == 0) sclw[col * kG7Warps] = scale;
+    }
+    __syncwarp();
+
+    // ---- block w of each of my rows, each column
+    {
+        const bool ok = mbar_wait_bounded(bar, 0, p.fault);
+        if (!__syncthreads_and(ok)) return;  // the slab never completed: fault word raised
+        for (int r = lane; r < count; r += 32) {
+            const uint8_t *row = slab + r * p.pitch;
+            int col = 0;
+            if (F == kQ4K) {  // columns in pairs: the weights unpacked once for two
+#pragma unroll 1
+                for (; col + 1 < NC; col += 2) {
+                    int C0, O0, C1, O1;
+                    uint32_t dd;
+                    block_q4k_pair<UNR>(row + 144 * w, aw + col * kG7K, aw + (col + 1) * kG7K,
+                                        Sw + col * (kG7Warps * 16), Sw + (col + 1) * (kG7Warps * 16), C0, O0, C1, O1,
+                                        dd);
+                    const uint32_t sv0 = sclw[col * kG7Warps], sv1 = sclw[(col + 1) * kG7Warps];
+                    vals[r * VS + col * 17 + w] = lane_value_fast<1>(C0 >> 4, O0, dd & 0xFFFFu, dd >> 16,
+                                                                     (int)(sv0 & 0xFFu), (int)(int16_t)(sv0 >> 16));
+                    vals[r * VS + (col + 1) * 17 + w] = lane_value_fast<1>(
+                        C1 >> 4, O1, dd & 0xFFFFu, dd >> 16, (int)(sv1 & 0xFFu), (int)(int16_t)(sv1 >> 16));
+                }
+            }
+#pragma unroll 1
+            for (; col < NC; ++col) {
+                const uint8_t *ac = aw + col * kG7K;
+                const int16_t *Sc = Sw + col * (kG7Warps * 16);
+                const uint32_t sv = sclw[col * kG7Warps];
+                const int m0 = (int)(sv & 0xFFu), e0 = (int)(int16_t)(sv >> 16);
+                float v;
+                if (F == kQ4K) {
+                    int C16, O;
+                    uint32_t dd;
+                    block_q4k<UNR>(row + 144 * w, ac, Sc, C16, O, dd);
+                    v = lane_value_fast<1>(C16 >> 4, O, dd & 0xFFFFu, dd >> 16, m0, e0);  // 16*C: exact shift
+                } else {
+                    const int C = block_q6k<UNR>(row + 208 * w, ac, Sc);
+                    const uint32_t d = *reinterpret_cast<const uint16_t *>(row + 208 * kG7Warps + 2 * w);
+                    v = lane_value_fast<0>(C, 0, d, 0, m0, e0);
+                }
+                vals[r * VS + col * 17 + w] = v;
+            }
+        }
+    }
+    __syncthreads();
+    // ---- fold: thread (r, col) adds row r's 16 block values of that column in
+    // block order from +0
+    for (int t = tid; t < count * NC; t += kG7Warps * 32) {
+        const int r = t / NC, col = t - r * NC;
+        const float *vr = vals + r * VS + col * 17;
+        float acc = 0.0f;
+#pragma unroll
+        for (int b = 0; b < kG7Warps; ++b) acc = fadd_ftz(acc, vr[b]);
+        if (acc != acc) acc = __uint_as_float(kEngineNaN);
+        *out_ptr(p.mt, col, row0 + r) = acc;
+    }
+}
+
+// NC columns (2..4) of a Q4_K-like or Q6_K-like matrix (or a table of them)
+// at K = 4096 with at most 64 rows a CTA and MINB CTAs a SM.  QB_E_ARG when
+// the shape does not fit.
+template <int F, int MINB, int UNR, int NC>
+int launch_gemv7m(const GemvArgs &a, cudaStream_t stream, const float *x) {
+    if ((F != kQ4K && F != kQ6K) || a.ncols != NC || a.mode != 0 || a.K != kG7K) return QB_E_ARG;
+    Gemv7K k;
+    k.mt = a.mats ? *a.mats : single_table(a.W, a.rows, a.out);
+    k.rows = k.mt.start[k.mt.n];
+    if (k.rows < 1) return QB_E_ARG;
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(num_sms(), k.rows));
+    const int64_t per_cta = (k.rows + grid - 1) / grid;
+    if (per_cta > kG7MaxRows) return QB_E_ARG;
+    k.rec = (int)record_bytes(F, kG7K);
+    k.pitch = k.rec + 16;
+    const int smem = gemv7m_smem(NC, (int)per_cta, k.pitch);
+    if (smem > (228 * 1024) / MINB - 1024 - 256) return QB_E_ARG;
+    k.base = k.rows / grid;
+    k.rem = k.rows % grid;
+    k.codes = a.codes;
+    k.scales = a.scales;
+    k.sums16 = a.sums16;
+    k.x = x;
+    k.fault = fault_word();
+    if (!k.fault) return QB_E_CUDA;
+    auto kern = x ? gemv7m_kernel<F, true, MINB, UNR, NC> : gemv7m_kernel<F, false, MINB, UNR, NC>;
+    if (ensure_smem_limit(reinterpret_cast<const void *>(kern), smem) != QB_OK) return QB_E_CUDA;
+    return launch_pdl(kern, dim3(grid), dim3(kG7Warps * 32), (size_t)smem, stream, k);
+}
+
+// 2..4 columns at K = 4096 (the multi-column form above); QB_E_ARG where it
+// does not apply.
+template <int F>
+int launch_gemv7_cols(const GemvArgs &a, cudaStream_t stream, const float *x) {
+    constexpr int U = F == kQ4K ? 2 : 4;
+    switch (a.ncols) {
+    case 2: return launch_gemv7m<F, 2, U, 2>(a, stream, x);
+    case 3: return launch_gemv7m<F, 2, U, 3>(a, stream, x);
+    case 4: return launch_gemv7m<F, 2, U, 4>(a, stream, x);
+    default: return QB_E_ARG;
+    }
 }
 
 }  // namespace qb

@@ -11,11 +11,14 @@
 namespace qb {
 template <>
 int launch_skinny<kQ4K>(const GemvArgs &a, cudaStream_t stream) {
+    const int r7 = launch_gemv7_cols<kQ4K>(a, stream, nullptr);  // 2..4 columns at K = 4096
+    if (r7 != QB_E_ARG) return r7;
     const int rc = launch_gemv5<kQ4K>(a, stream);
     return rc == QB_E_ARG ? launch_gemv3<kQ4K>(a, stream) : rc;
 }
 template <>
 int launch_one_col3<kQ4K>(const GemvArgs &a, cudaStream_t stream, const float *x) {
+    if (a.ncols > 1) return launch_gemv7_cols<kQ4K>(a, stream, x);  // 2..4 columns from x in one launch
     // K = 4096 (qb_gemv7.cuh): up to 32 rows a CTA with each lane's block held
     // in registers before the dependency wait, up to 64 rows from shared
     // memory; two CTAs a SM.  Longer row ranges stream through rings.

@@ -8,10 +8,13 @@
 namespace qb {
 template <>
 int launch_skinny<kQ6K>(const GemvArgs &a, cudaStream_t stream) {
+    const int r7 = launch_gemv7_cols<kQ6K>(a, stream, nullptr);  // 2..4 columns at K = 4096
+    if (r7 != QB_E_ARG) return r7;
     return launch_gemv3<kQ6K>(a, stream);
 }
 template <>
 int launch_one_col3<kQ6K>(const GemvArgs &a, cudaStream_t stream, const float *x) {
+    if (a.ncols > 1) return launch_gemv7_cols<kQ6K>(a, stream, x);  // 2..4 columns from x in one launch
     // K = 4096 and up to 64 rows a CTA: a warp per block, a lane per row, two
     // CTAs a SM (qb_gemv7.cuh); longer row ranges stream through rings
     const int r7 = launch_gemv7<kQ6K, 2, 4, false>(a, stream, x);

@@ -463,9 +463,16 @@ def test_matvec_bit_exact(fmt, ncols, rows, K):
     qb.q_matvec(fmt, dev(W), rows, K, dev(x), out, workspace=ws if ncols > 1 else None)
     torch.cuda.synchronize()
     assert np.array_equal(bits(host(out)), bits(want))
-    if ncols > 1:
-        with pytest.raises(qb.QbError):
+    if ncols > 1:  # without a workspace: one launch where the shape allows it, else refused
+        out.fill_(float("nan"))
+        try:
             qb.q_matvec(fmt, dev(W), rows, K, dev(x), out, workspace=None)
+        except qb.QbError as exc:
+            assert exc.status == qb.QB_E_ARG
+        else:
+            torch.cuda.synchronize()
+            assert fmt != synth.FMT_Q8_0 and K == 4096 and ncols <= 4
+            assert np.array_equal(bits(host(out)), bits(want))
 
 
 @pytest.mark.parametrize("fmt", [synth.FMT_Q4K, synth.FMT_Q6K])
@@ -496,30 +503,32 @@ def test_one_column_long_rows(fmt, rows, K):
 
 
 @pytest.mark.parametrize("fmt", [synth.FMT_Q4K, synth.FMT_Q6K])
+@pytest.mark.parametrize("ncols", [1, 2, 3, 4])
 @pytest.mark.parametrize("rows", [1, 31, 152, 152 * 31 + 7, 152 * 32, 152 * 32 + 1, 152 * 64, 152 * 64 + 1])
-def test_k4096_row_ranges(fmt, rows):
-    """One column at K = 4096 across the row counts where the kernel changes
-    form: up to 32 rows a CTA (a lane per row, each lane's block held in
-    registers from before the dependency wait), 33..64 (blocks read from
-    shared memory, two rows a lane), and past the shared-memory budget (the
-    warp-ring kernel) -- from a quantized activation and from the f32
-    activation in one launch, both equal to the oracle."""
+def test_k4096_row_ranges(fmt, ncols, rows):
+    """1..4 columns at K = 4096 across the row counts where the kernel changes
+    form: up to 32 rows a CTA (a lane per row; one column: each lane's block
+    held in registers from before the dependency wait), 33..64 (blocks read
+    from shared memory, two rows a lane), and past the shared-memory budget (the
+    ring kernels) -- from a quantized activation and from the f32 activation
+    (one launch up to 4 columns), both equal to the oracle."""
     import torch
     K = 4096
-    x = _edge_activation(1, K, 256, seed=rows + fmt)
+    x = _edge_activation(ncols, K, 256, seed=rows + fmt + 10 * ncols)
     x[0, 5 * 256 + 1] = 3.0   # no infinity: every row a finite value, not the engine's NaN
-    rng = np.random.default_rng(rows * 7 + fmt)
+    rng = np.random.default_rng(rows * 7 + fmt + ncols)
     W = synth.pack(fmt, synth.draw(fmt, rng, rows, K))
     codes, m, e, s16, packed = oracle_act(x, 256)
     want = oracle.gemv(fmt, W, rows, K, codes, m, e)
-    act = qb.alloc_act(1, K, 256)
+    act = qb.alloc_act(ncols, K, 256)
     qb.quantize_act(256, dev(x), *act)
-    out = torch.full((1, rows), float("nan"), dtype=torch.float32, device="cuda")
-    qb.q_gemv(fmt, dev(W), rows, K, act, 1, out)
+    out = torch.full((ncols, rows), float("nan"), dtype=torch.float32, device="cuda")
+    qb.q_gemv(fmt, dev(W), rows, K, act, ncols, out)
     torch.cuda.synchronize()
     assert np.array_equal(bits(host(out)), bits(want))
     out.fill_(float("nan"))
-    qb.q_matvec(fmt, dev(W), rows, K, dev(x), out)
+    ws = torch.empty(qb.q_matvec_workspace_bytes(fmt, K, ncols), dtype=torch.uint8, device="cuda")
+    qb.q_matvec(fmt, dev(W), rows, K, dev(x), out, workspace=ws)
     torch.cuda.synchronize()
     assert np.array_equal(bits(host(out)), bits(want))
 
