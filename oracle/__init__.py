@@ -87,6 +87,7 @@ def lib():
         L.or_kv_scores.restype = i32
         L.or_e4m3_to_f32.argtypes, L.or_e4m3_to_f32.restype = [ctypes.c_uint8], ctypes.c_float
         L.or_gemv_fp8.argtypes, L.or_gemv_fp8.restype = [P, P, i64, i64, P, i32, P, P], i32
+        L.or_exact_dot_f32.argtypes, L.or_exact_dot_f32.restype = [P, P, i64], ctypes.c_float
     return _lib
 
 
@@ -382,6 +383,15 @@ def kv_scores(scaling: int, qc, qm, qe, d: int, kc, ks, L: int, nkv: int, scale:
 def e4m3_to_f32(b: int) -> np.float32:
     """e4m3ToF32 (colizig OPS page, FP8) of one byte."""
     return np.float32(lib().or_e4m3_to_f32(int(b) & 0xFF))
+
+
+def exact_dot_f32(x: np.ndarray, w: np.ndarray) -> np.float32:
+    """The exact dot of two f32 vectors rounded once to the nearest f32 (the FP8
+    path's sum)."""
+    x = np.ascontiguousarray(x, np.float32)
+    w = np.ascontiguousarray(w, np.float32)
+    assert x.shape == w.shape and x.ndim == 1
+    return np.float32(lib().or_exact_dot_f32(_p(x), _p(w), x.size))
 
 
 def gemv_fp8(W: np.ndarray, scales: np.ndarray, rows: int, K: int, x: np.ndarray):

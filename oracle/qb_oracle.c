@@ -49,9 +49,10 @@
  *       taken is the f32 quotient 1/s, correctly rounded (the page's recip
  *       seeds Newton steps from a table it does not print).
  *   R19 (FP8) matmulFp8 is read as the page's own check: each weight the f32
- *       product of its decoded byte and its block scale, the dot exact (in
- *       double), rounded once; a GPU result is held to the f32 summation
- *       bound (K + 4) * 2^-24 * sum |x_i * w_i| around it.
+ *       product of its decoded byte and its block scale, the dot exact (a
+ *       640-bit integer), rounded once to nearest even, subnormals kept; a
+ *       GPU result is held to the f32 summation bound
+ *       (K + 4) * 2^-24 * sum |x_i * w_i| around it.
  *   R18 (int8 cache) a score against a key row whose f16 scale is infinite
  *       or NaN (a row whose amax*INV_127 overflows binary16) is NAN, as an
  *       unreadable weight scale is (R7); a query block without a scale too.
@@ -1022,13 +1023,120 @@ float or_e4m3_to_f32(uint8_t b) {
 }
 
 /* ---------------------------------------------------------------------
+ * The exact dot of n f32 pairs, rounded once: every product x_i * w_i is an
+ * integer times a power of two (24-bit by 24-bit significands), added exactly
+ * into a two's-complement integer of 640 bits whose bit j weighs 2^(j - 298)
+ * (products of finite f32 values lie between 2^-298 and 2^256, and 2^31 terms
+ * add 31 more places); the sum is then rounded to nearest even on the f32
+ * grid, subnormals kept (ordinary f32 arithmetic: the FP8 path has no flush
+ * rule), past the top infinite.  A NaN operand, an infinity times zero, or
+ * infinities of both signs give NaN; otherwise an infinite product gives that
+ * infinity.  An exact zero is +0.
+ * ------------------------------------------------------------------- */
+#define OR_DL 20   /* 32-bit limbs: 640 bits */
+#define OR_DOFF 298
+
+static void dot_add(uint32_t *acc, uint64_t mag, int neg, int pos) {
+    /* acc += (neg ? -1 : 1) * mag * 2^pos, 0 <= pos, pos + 64 < 640 */
+    uint32_t t[OR_DL];
+    memset(t, 0, sizeof t);
+    int limb = pos / 32, bit = pos % 32;
+    u128 v = (u128)mag << bit;
+    for (int i = 0; i < 4 && limb + i < OR_DL; i++) t[limb + i] = (uint32_t)(v >> (32 * i));
+    if (neg) {
+        uint64_t carry = 1;
+        for (int i = 0; i < OR_DL; i++) {
+            uint64_t y = (uint64_t)(uint32_t)~t[i] + carry;
+            t[i] = (uint32_t)y;
+            carry = y >> 32;
+        }
+    }
+    uint64_t carry = 0;
+    for (int i = 0; i < OR_DL; i++) {
+        uint64_t y = (uint64_t)acc[i] + t[i] + carry;
+        acc[i] = (uint32_t)y;
+        carry = y >> 32;
+    }
+}
+
+/* an f32 as sig * 2^e with sig < 2^24 (zero: sig 0) */
+static void f32_parts(float f, uint64_t *sig, int *e, int *neg) {
+    uint32_t b;
+    memcpy(&b, &f, 4);
+    *neg = (int)(b >> 31);
+    int E = (int)((b >> 23) & 0xFF);
+    uint32_t m = b & 0x7FFFFF;
+    *sig = E ? (m | 0x800000u) : m;
+    *e = (E ? E : 1) - 150;
+}
+
+float or_exact_dot_f32(const float *x, const float *w, int64_t n) {
+    uint32_t acc[OR_DL];
+    memset(acc, 0, sizeof acc);
+    int pinf = 0, ninf = 0;
+    for (int64_t i = 0; i < n; i++) {
+        const float a = x[i], b = w[i];
+        if (isnan(a) || isnan(b)) return engine_nan();
+        if (isinf(a) || isinf(b)) {
+            if (a == 0.0f || b == 0.0f) return engine_nan();   /* infinity times zero */
+            if ((a < 0) != (b < 0)) ninf = 1; else pinf = 1;
+            continue;
+        }
+        uint64_t sa, sb;
+        int ea, eb, na, nb;
+        f32_parts(a, &sa, &ea, &na);
+        f32_parts(b, &sb, &eb, &nb);
+        if (sa == 0 || sb == 0) continue;
+        dot_add(acc, sa * sb, na != nb, ea + eb + OR_DOFF);
+    }
+    if (pinf && ninf) return engine_nan();
+    if (pinf) return INFINITY;
+    if (ninf) return -INFINITY;
+    int neg = (int)((acc[OR_DL - 1] >> 31) & 1);
+    if (neg) {
+        uint64_t carry = 1;
+        for (int i = 0; i < OR_DL; i++) {
+            uint64_t y = (uint64_t)(uint32_t)~acc[i] + carry;
+            acc[i] = (uint32_t)y;
+            carry = y >> 32;
+        }
+    }
+    int p = -1;  /* leading place of the magnitude */
+    for (int i = OR_DL - 1; i >= 0 && p < 0; i--)
+        if (acc[i]) for (int k = 31; k >= 0; k--) if ((acc[i] >> k) & 1) { p = 32 * i + k; break; }
+    if (p < 0) return 0.0f;
+    int x2 = p - OR_DOFF;                       /* leading exponent */
+    int qe = x2 < -126 ? -149 : x2 - 23;        /* the f32 quantum there */
+    int q = qe + OR_DOFF;                       /* its bit position */
+    /* mantissa = acc >> q (at most 25 bits), then nearest even on the rest */
+    uint64_t mant = 0;
+    for (int k = p; k >= q; k--) mant = (mant << 1) | ((acc[k / 32] >> (k % 32)) & 1);
+    int half = q >= 1 ? (int)((acc[(q - 1) / 32] >> ((q - 1) % 32)) & 1) : 0;
+    int sticky = 0;
+    for (int k = q - 2; k >= 0 && !sticky; k--) sticky = (acc[k / 32] >> (k % 32)) & 1;
+    if (half && (sticky || (mant & 1))) mant++;
+    if (mant == (1ull << 24)) { mant >>= 1; qe++; }
+    float r;
+    if (mant < (1ull << 23)) {                  /* subnormal (qe = -149) */
+        uint32_t bits = (uint32_t)mant;
+        memcpy(&r, &bits, 4);
+    } else {
+        int e2 = qe + 23;                       /* exponent of the leading bit */
+        if (e2 > 127) return neg ? -INFINITY : INFINITY;
+        uint32_t bits = ((uint32_t)(e2 + 127) << 23) | ((uint32_t)mant & 0x7FFFFFu);
+        memcpy(&r, &bits, 4);
+    }
+    return neg ? -r : r;
+}
+
+/* ---------------------------------------------------------------------
  * matmulFp8 read as "dequantize then f32 matmul" (the page's own check): the
  * weight W[r][i] is the f32 product of its decoded byte and its 128x128 block
  * scale (dequantRow folds the scale), rounded to nearest; the row's dot with
- * each activation column x[c][:] is then taken in double and rounded once to
- * f32.  Scales [ceil(rows/128)][ceil(K/128)].  Also the sum of |x_i * w_i| in
- * double (absdot), against which a GPU's f32 summation error is bounded.
- * A NaN result is the engine's NaN.
+ * each activation column x[c][:] is then taken exactly and rounded once to
+ * f32 (or_exact_dot_f32).  Scales [ceil(rows/128)][ceil(K/128)].  Also the
+ * sum of |x_i * w_i| in double (absdot), the scale against which a GPU's f32
+ * summation error is bounded.  A NaN result is the engine's NaN.
  * ------------------------------------------------------------------- */
 int or_gemv_fp8(const uint8_t *W, const float *scales, int64_t rows, int64_t K, const float *x, int ncols,
                 float *out, double *absdot) {
@@ -1041,15 +1149,14 @@ int or_gemv_fp8(const uint8_t *W, const float *scales, int64_t rows, int64_t K, 
             w[i] = or_e4m3_to_f32(W[r * K + i]) * s;   /* one f32 product, to nearest */
         }
         for (int c = 0; c < ncols; c++) {
-            double acc = 0.0, ab = 0.0;
-            for (int64_t i = 0; i < K; i++) {
-                double t = (double)x[(int64_t)c * K + i] * (double)w[i];
-                acc += t;
-                ab += fabs(t);
-            }
-            float v = (float)acc;
+            const float *xc = x + (int64_t)c * K;
+            float v = or_exact_dot_f32(xc, w, K);
             out[(int64_t)c * rows + r] = isnan(v) ? engine_nan() : v;
-            if (absdot) absdot[(int64_t)c * rows + r] = ab;
+            if (absdot) {
+                double ab = 0.0;
+                for (int64_t i = 0; i < K; i++) ab += fabs((double)xc[i] * (double)w[i]);
+                absdot[(int64_t)c * rows + r] = ab;
+            }
         }
     }
     free(w);

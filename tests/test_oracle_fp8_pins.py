@@ -79,9 +79,37 @@ def test_exact_sums(orc):
                                          for i in range(K)))
 
 
-def test_random_within_double_rounding(orc):
-    """Random data: the oracle is within one f32 rounding plus K double roundings
-    of the exact rational result."""
+def round_f32_nearest(X: Fraction) -> int:
+    """f32 bits of the exact rational X, nearest even on the f32 grid with
+    subnormals kept (IEEE), infinite past the top: the neighbour search of
+    round_f32_grid_then_flush without its flush, written out again here."""
+    if X == 0:
+        return 0
+    neg = X < 0
+    A = -X if neg else X
+    top = (Fraction(2 ** 24) - Fraction(1, 2)) * Fraction(2) ** 104
+    if A >= top:
+        return 0xFF800000 if neg else 0x7F800000
+    c = np.float32(float(A)) if float(A) < 3.4e38 else np.float32(3.4028234663852886e38)
+    best = None
+    for k in range(-3, 4):
+        cand = c
+        step = np.float32(np.inf) if k > 0 else np.float32(0)
+        for _ in range(abs(k)):
+            cand = np.nextafter(cand, step, dtype=np.float32)
+        if np.isinf(cand):
+            continue
+        key = (abs(Fraction(float(cand)) - A), int(cand.view(np.uint32)) & 1)   # ties -> even significand
+        if best is None or key < best[0]:
+            best = (key, cand)
+    return int(best[1].view(np.uint32)) | (0x80000000 if neg else 0)
+
+
+def test_random_exact(orc):
+    """Random data: the oracle's result is the exact rational dot of the f32
+    activation with the f32-rounded dequantized weights, rounded once to the
+    nearest f32 (ties even) -- bit for bit; its absdot is the sum of |x_i w_i|
+    within K double roundings."""
     rng = np.random.default_rng(72)
     rows, K = 8, 384
     W, scales = _draw(rng, rows, K)
@@ -92,9 +120,27 @@ def test_random_within_double_rounding(orc):
               for i in range(K)]
         X = sum(Fraction(float(x[0, i])) * ws[i] for i in range(K))
         S = sum(abs(Fraction(float(x[0, i])) * ws[i]) for i in range(K))
-        err = abs(Fraction(float(out[0, r])) - X)
-        assert err <= Fraction(2) ** -24 * abs(X) + K * Fraction(2) ** -52 * S + Fraction(2) ** -149
+        assert bits(out[0, r]) == round_f32_nearest(X), r
         assert abs(Fraction(ab[0, r]) - S) <= K * Fraction(2) ** -52 * S
+
+
+def test_cancellation_and_range(orc):
+    """Sums that a double accumulation gets wrong, and the ends of the range:
+    2^60 + 1 - 2^60 is exactly 1; a result below 2^-126 stays subnormal (no
+    flush on this path); a sum past the top is infinite; opposite infinities
+    give NaN."""
+    def dot(xs, ws):
+        return orc.exact_dot_f32(np.array(xs, np.float32), np.array(ws, np.float32))
+    assert dot([2.0 ** 30, 1.0, -2.0 ** 30], [2.0 ** 30, 1.0, 2.0 ** 30]) == 1.0
+    assert bits(dot([2.0 ** -100], [2.0 ** -40])) == 0x00000200                # 2^-140: subnormal kept
+    # 2^-149 + 2^-150: 1.5 quanta of the subnormal grid, a tie, to even (2 quanta);
+    # 2^-149 + 2^-151: 1.25 quanta, down to 1
+    assert bits(dot([2.0 ** -100, 2.0 ** -100], [2.0 ** -49, 2.0 ** -50])) == 0x00000002
+    assert bits(dot([2.0 ** -100, 2.0 ** -100], [2.0 ** -49, 2.0 ** -51])) == 0x00000001
+    assert np.isinf(dot([3e38, 3e38], [1.0, 1.0])) and dot([3e38, 3e38], [1.0, 1.0]) > 0
+    assert np.isnan(dot([np.inf, 1.0], [1.0, -np.inf]))
+    assert np.isnan(dot([np.inf], [0.0]))
+    assert bits(dot([1.0, -1.0], [5.0, 5.0])) == 0                             # an exact zero is +0
 
 
 def test_nan_weight(orc):
