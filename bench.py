@@ -958,6 +958,26 @@ def oracle_pass(fmt, rows, K, Wh, x, nthreads, row_limit=None, sub32=False):
     return r_end
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else platform)."""
+    import platform
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return platform.processor() or platform.machine()
+
+
 def cpu_baseline(fmt, rows, K, ncols, Wh, x, wbytes, budget_s=10.0, sub32=False):
     n = _oracle_threads()
     oracle_pass(fmt, rows, K, Wh, x, n, sub32=sub32)          # warm (also builds the oracle if needed)
@@ -968,9 +988,23 @@ def cpu_baseline(fmt, rows, K, ncols, Wh, x, wbytes, budget_s=10.0, sub32=False)
         el = time.perf_counter() - t0
         if el >= budget_s:
             break
+    # single thread: passes over a sample of the rows, about a quarter of the budget
+    r1 = max(1, rows // 16)
+    reps1, t1 = 0, time.perf_counter()
+    while True:
+        oracle_pass(fmt, rows, K, Wh, x, 1, row_limit=r1, sub32=sub32)
+        reps1 += 1
+        el1 = time.perf_counter() - t1
+        if el1 >= budget_s / 4:
+            break
+    rec = wbytes / rows
     return {"value": round(wbytes * reps / el / 1e9, 4), "unit": "GB/s", "cores": n, "kind": "oracle",
             "sample": f"{reps} full passes (quantize + all {rows} rows) in {el:.1f} s, rows split over {n} "
-                      f"threads of the scalar C oracle"}
+                      f"threads of the scalar C oracle",
+            "single_thread": {"value": round(rec * r1 * reps1 / el1 / 1e9, 4), "unit": "GB/s",
+                              "sample": f"{reps1} passes of quantize + the first {r1} rows on one thread "
+                                        f"in {el1:.1f} s"},
+            "cpu_model": cpu_model()}
 
 
 def sampled_oracle_pass(mats, n, frac):
