@@ -248,6 +248,17 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
+def tensor_peak():
+    """Dense f16 tensor-core TFLOP/s: the measured bf16 burst figure (f16 and
+    bf16 share the nominal rate), else the stated fallback."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        if "bf16_tflops" in d:
+            return float(d["bf16_tflops"]), "measured (cuBLAS bf16 GEMM, burst; f16 has the same nominal rate)"
+    return 1900.0, "fallback"
+
+
 class ClockSampler:
     """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
@@ -350,6 +361,29 @@ def one_col_gemv7(fmt, rows, K):
     return (fmt == synth.FMT_Q4K and per <= 32) or smem <= (228 * 1024) // 2 - 1024 - 256
 
 
+TC_MIN_COLS = 9
+
+
+def tc_applies(fmt, K, ncols):
+    """The library's rule for the tensor-core (tcgen05) kernel: Q4_K-like or
+    Q6_K-like, K % 256 == 0, from TC_MIN_COLS columns, and some cluster split of
+    the blocks (1..8 CTAs) whose shared memory fits 227 KB."""
+    if fmt not in (synth.FMT_Q4K, synth.FMT_Q6K) or K % 256 or ncols < TC_MIN_COLS:
+        return False
+    nb = K // 256
+    bb = 144 if fmt == synth.FMT_Q4K else 208
+    for ks in range(1, min(8, nb) + 1):
+        nbq, cpc = -(-nb // ks), -(-ncols // ks)
+        if fmt == synth.FMT_Q6K and 2 * nbq + 14 > 64:
+            continue
+        bact = (8 * (8 + nbq) + 4 + 127) // 128 * 128
+        total = (bact + nbq * 8192 + (nbq * 512 if fmt == synth.FMT_Q4K else 0) + (16 * nbq * 4 + 127) // 128 * 128 +
+                 (cpc * nb * 512 + 127) // 128 * 128 + nbq * 128 * bb + (128 * 64 if fmt == synth.FMT_Q6K else 0))
+        if total <= 227 * 1024:
+            return True
+    return False
+
+
 def roofline(fmt, ncols, single, achieved, peak, peak_kind, traffic, roof_bytes, per_launch_s, prod_s, abytes,
              ops_per_step, roof_launches, sub32=False, rows=0, K=0):
     g7 = ncols == 1 and not sub32 and fmt != synth.FMT_F16 and one_col_gemv7(fmt, rows, K)
@@ -367,13 +401,22 @@ def roofline(fmt, ncols, single, achieved, peak, peak_kind, traffic, roof_bytes,
             f"gemv3_kernel<{synth.FORMAT_NAMES[fmt]}, one column, single launch> (quantize + product)"
             if single and g3 else
             f"gemv2_kernel<{synth.FORMAT_NAMES[fmt]}, single launch> (quantize + product)" if single else
-            f"gemv5_kernel<q4k, {ncols} columns> (f16 tensor-core sub-block sums)"
-            if fmt == synth.FMT_Q4K and 11 <= ncols <= 16 and K % 256 == 0 and K <= 4096 else
+            f"tc_kernel<{synth.FORMAT_NAMES[fmt]}, {ncols} columns> (tcgen05 f16 MMAs, accumulators in tensor memory)"
+            if tc_applies(fmt, K, ncols) else
             f"gemv3_kernel<{synth.FORMAT_NAMES[fmt]}, {ncols} columns>")
     prod = {"avg_launch_us": round(prod_s * 1e6, 4),
             "achieved_gbs": round(abytes / prod_s / 1e9, 1),
             "frac_of_hbm": round(abytes / prod_s / 1e9 / peak, 4),
             "note": "activation quantized beforehand (q_gemv)"}
+    if fmt != synth.FMT_F16 and ncols > 1 and not sub32 and tc_applies(fmt, K, ncols):
+        tflops = ops_per_step / prod_s / 1e12
+        tpk, tkind = tensor_peak()
+        return {"bound": "tensor", "kernel": name, "achieved": round(tflops, 2), "peak": round(tpk, 1),
+                "peak_kind": tkind, "unit": "TFLOP/s", "frac": round(tflops / tpk, 4), "traffic": traffic,
+                "algorithmic_ops_per_launch": ops_per_step, "avg_launch_us": round(prod_s * 1e6, 4),
+                "launches_timed": 3 * roof_launches, "hbm_side": prod,
+                "dp4a_side": {"achieved_tops": round(tflops, 2), "peak_tops": round(DP4A_PEAK_TOPS, 1),
+                              "frac": round(tflops / DP4A_PEAK_TOPS, 4)}}
     if fmt != synth.FMT_F16 and ncols > 1:
         tops = ops_per_step / prod_s / 1e12
         return {"bound": "alu", "kernel": name, "achieved": round(tops, 2), "peak": round(DP4A_PEAK_TOPS, 1),
@@ -1385,7 +1428,8 @@ def run_stack(args, rank, world):
         "frac_of_8tbs": round(value / 8000.0, 4), "frac_of_measured_copy": round(value / peak, 4),
         "gpu_launches": nrep * G * launches_step, "clocks": clocks,
         "roofline": {"bound": "hbm" if ncols == 1 else "alu", "kernel": "the step's 129 products (one-column "
-                     "streaming kernels at 1 column; dp4a / f16 tensor-core kernels at 4 and 16)",
+                     "streaming kernels at 1 column; the warp-per-block and dp4a kernels at 4; the tcgen05 "
+                     "tensor-core kernel at 16, the dp4a kernel for the K = 14336 down projection)",
                      "achieved": round(value, 1) if ncols == 1 else round(ops / step_s / 1e12, 2),
                      "peak": peak if ncols == 1 else round(DP4A_PEAK_TOPS, 1),
                      "peak_kind": f"{peak_kind} (HBM copy, burst)" if ncols == 1 else

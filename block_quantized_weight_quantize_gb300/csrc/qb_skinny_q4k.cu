@@ -1,20 +1,25 @@
 // qb_skinny_q4k.cu -- the 2..16-column kernels for the Q4_K-like format (a
 // translation unit of its own so the formats compile in parallel): the
-// tensor-core kernel from 11 columns, the dp4a streaming kernel otherwise;
-// and the one-column forms (qb_gemv6.cuh, qb_gemv3.cuh) where they apply.
+// tensor-core (tcgen05) kernel from kTcMinCols columns, the warp-per-block
+// kernel at 2..4 columns and K = 4096, the dp4a streaming kernel otherwise;
+// and the one-column forms (qb_gemv7.cuh, qb_gemv6.cuh, qb_gemv3.cuh) where
+// they apply.
 #include "qb_gemv.cuh"
 #include "qb_gemv3.cuh"
 #include "qb_gemv6.cuh"
 #include "qb_gemv7.cuh"
-#include "qb_gemv5.cuh"
+#include "qb_tc.cuh"
 
 namespace qb {
 template <>
 int launch_skinny<kQ4K>(const GemvArgs &a, cudaStream_t stream) {
+    if (a.ncols >= kTcMinCols) {
+        const int rt = launch_tc<kQ4K>(a, stream);
+        if (rt != QB_E_ARG) return rt;
+    }
     const int r7 = launch_gemv7_cols<kQ4K>(a, stream, nullptr);  // 2..4 columns at K = 4096
     if (r7 != QB_E_ARG) return r7;
-    const int rc = launch_gemv5<kQ4K>(a, stream);
-    return rc == QB_E_ARG ? launch_gemv3<kQ4K>(a, stream) : rc;
+    return launch_gemv3<kQ4K>(a, stream);
 }
 template <>
 int launch_one_col3<kQ4K>(const GemvArgs &a, cudaStream_t stream, const float *x) {

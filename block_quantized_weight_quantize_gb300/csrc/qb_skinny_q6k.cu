@@ -1,13 +1,20 @@
-// qb_skinny_q6k.cu -- the 2..16-column streaming kernel for one weight format
-// (a translation unit of its own so the formats compile in parallel).
+// qb_skinny_q6k.cu -- the 2..16-column kernels for the Q6_K-like format (a
+// translation unit of its own so the formats compile in parallel): the
+// tensor-core (tcgen05) kernel from kTcMinCols columns, the warp-per-block
+// kernel at 2..4 columns and K = 4096, the dp4a streaming kernel otherwise.
 #include "qb_gemv.cuh"
 #include "qb_gemv3.cuh"
 #include "qb_gemv6.cuh"
 #include "qb_gemv7.cuh"
+#include "qb_tc.cuh"
 
 namespace qb {
 template <>
 int launch_skinny<kQ6K>(const GemvArgs &a, cudaStream_t stream) {
+    if (a.ncols >= kTcMinCols) {
+        const int rt = launch_tc<kQ6K>(a, stream);
+        if (rt != QB_E_ARG) return rt;
+    }
     const int r7 = launch_gemv7_cols<kQ6K>(a, stream, nullptr);  // 2..4 columns at K = 4096
     if (r7 != QB_E_ARG) return r7;
     return launch_gemv3<kQ6K>(a, stream);
