@@ -20,9 +20,11 @@
  * rounded to f16; element i's exact product goes to lane i mod 8 in index
  * order from +0; the 8 lanes fold as ((l0+l1)+(l2+l3))+((l4+l5)+(l6+l7)).
  *
- * Devices: the launchers raise each kernel's dynamic shared-memory limit once
- * per process, on the device current at its first call, so one process drives
- * one GPU (several GPUs: one process each, as torchrun launches them).
+ * Devices and threads: every call works on the device current in the calling
+ * thread.  The launchers raise each kernel's dynamic shared-memory limit once
+ * per (kernel, device), under a lock, and cache per-device facts (SM count,
+ * the fault word's address) atomically, so one process may drive several
+ * GPUs and call the library from several host threads at once.
  *
  * Memory: every data pointer is DEVICE memory owned by the caller; the
  * library allocates nothing and keeps no per-call state.  Weight pointers
