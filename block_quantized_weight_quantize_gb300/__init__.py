@@ -34,7 +34,7 @@ EXPORTS = ("quantize_act", "q_gemv", "quantize_act_f16", "q_gemv_f16", "q_check_
            "q_block_values", "q_device_status", "q_strerror", "q_matvec", "q_matvec_workspace_bytes",
            "q_matvec_static", "q_gemv_many", "q_gemv_f16_many", "q_matvec_many", "quantize_act_sub32",
            "q_gemv_sub32", "q_matvec_sub32_workspace_bytes", "q_matvec_sub32", "kv_head_codes", "kv_cache_rows",
-           "kv_quantize_heads", "kv_scores", "q_gemv_fp8", "q_matvec_host_workspace_bytes", "q_matvec_host")
+           "kv_quantize_heads", "kv_scores", "q_gemv_fp8", "q_matvec_host_workspace_bytes", "q_matvec_host", "q_gemv_w2")
 PERBLOCK, SUB32 = 0, 1  # QB_PERBLOCK, QB_SUB32: how an activation (or a query head) is scaled
 
 
@@ -47,6 +47,10 @@ class QbError(RuntimeError):
 class _Act(ctypes.Structure):
     _fields_ = [("block", ctypes.c_int), ("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p),
                 ("sums16", ctypes.c_void_p)]
+
+
+class _Act16(ctypes.Structure):
+    _fields_ = [("block", ctypes.c_int), ("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p)]
 
 
 _lib = None
@@ -67,6 +71,7 @@ def lib() -> ctypes.CDLL:
         L.q_gemv_f16.argtypes, L.q_gemv_f16.restype = [P, i64, i64, P, i32, P, P], i32
         L.q_check_weights.argtypes, L.q_check_weights.restype = [i32, P, i64, i64, P], i32
         L.q_weight_bytes.argtypes, L.q_weight_bytes.restype = [i32, i64, i64], i64
+        L.q_gemv_w2.argtypes, L.q_gemv_w2.restype = [i32, P, i64, i64, ctypes.POINTER(_Act16), i32, P, P], i32
         L.q_block_values.argtypes = [i32, P, i64, i64, ctypes.POINTER(_Act), i32, P, P, P, P]
         L.q_block_values.restype = i32
         L.q_device_status.argtypes, L.q_device_status.restype = [P], i32
@@ -253,6 +258,13 @@ def q_gemv(fmt: int, W, rows: int, K: int, act, ncols: int, out, stream=None) ->
     codes, scales, sums16 = act
     a = _act(BLOCK[fmt], codes, scales, sums16)
     _check(lib().q_gemv(fmt, _ptr(W), rows, K, ctypes.byref(a), ncols, _ptr(out), _stream(stream)), "q_gemv")
+
+
+def q_gemv_w2(fmt: int, W, rows: int, K: int, codes16, scales, ncols: int, out, stream=None) -> None:
+    """q_gemv with two-word activation codes: codes16 int16 [ncols, K], scales
+    int32 [ncols, K/block] (qb_scale), out f32 [ncols, rows]."""
+    a = _Act16(BLOCK[fmt], _ptr(codes16).value, _ptr(scales).value)
+    _check(lib().q_gemv_w2(fmt, _ptr(W), rows, K, ctypes.byref(a), ncols, _ptr(out), _stream(stream)), "q_gemv_w2")
 
 
 def q_block_values(fmt: int, W, rows: int, K: int, act, ncols: int, C=None, O=None, v=None, stream=None) -> None:

@@ -190,6 +190,24 @@ int q_gemv(qb_fmt fmt, const void *W, int64_t rows, int64_t K, const qb_act *act
     return gemv_common(fmt, W, rows, K, act, ncols, out, nullptr, nullptr, nullptr, 0, stream);
 }
 
+int q_gemv_w2(qb_fmt fmt, const void *W, int64_t rows, int64_t K, const qb_act16 *act, int ncols, float *out,
+              void *stream) {
+    const int f = fmt_index(fmt);
+    if (f < 0) return QB_E_FORMAT;
+    if (!W || !act || !out || !act->codes || !act->scales) return QB_E_ARG;
+    if (act->block != fmt_block(f)) return QB_E_BLOCK;
+    if (rows < 0 || K < 0 || K % fmt_block(f) != 0 || K > kMaxK || ncols < 1 || ncols > 16) return QB_E_ARG;
+    if (rows > (int64_t(1) << 31)) return QB_E_ARG;
+    if (misaligned(W) || misaligned(act->codes) || (reinterpret_cast<uintptr_t>(act->scales) & 3u) ||
+        (reinterpret_cast<uintptr_t>(out) & 3u))
+        return QB_E_ARG;
+    if (rows == 0) return QB_OK;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (K == 0)  // rows of no blocks: the fold of no terms is +0
+        return cudaMemsetAsync(out, 0, (size_t)ncols * rows * sizeof(float), s) == cudaSuccess ? QB_OK : QB_E_CUDA;
+    return launch_gemv_w2(f, W, rows, K, act->codes, act->scales, ncols, out, s);
+}
+
 int q_block_values(qb_fmt fmt, const void *W, int64_t rows, int64_t K, const qb_act *act, int ncols, int32_t *C,
                    int32_t *O, float *v, void *stream) {
     const void *any = C ? (const void *)C : O ? (const void *)O : (const void *)v;

@@ -98,6 +98,9 @@ int launch_gemv_f16_many(const MatTable &t, int64_t K, const uint16_t *x16, int 
 // F16 from the f32 activation in one launch (rounded to f16 in the prologue); QB_E_ARG when it does not apply.
 int launch_matvec_f16(const MatTable &t, int64_t K, const float *x, int ncols, cudaStream_t stream);
 int launch_check_weights(int fmt, const void *W, int64_t rows, int64_t K, int *flag, cudaStream_t stream);
+// Two-word (16-bit) activation codes (qb_w2.cu); QB_E_ARG when a row's block values do not fit shared memory.
+int launch_gemv_w2(int fmt, const void *W, int64_t rows, int64_t K, const int16_t *codes, const qb_scale *scales,
+                   int ncols, float *out, cudaStream_t stream);
 // FP8 E4M3 weights with 128x128 block scales (qb_fp8.cu).
 int launch_gemv_fp8(const uint8_t *W, const float *scales, int64_t rows, int64_t K, const float *x, int ncols,
                     float *out, cudaStream_t stream);

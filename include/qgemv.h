@@ -135,6 +135,30 @@ QB_API int quantize_act(int block, const float *x, int64_t K, int ncols, int8_t 
 QB_API int q_gemv(qb_fmt fmt, const void *W, int64_t rows, int64_t K, const qb_act *act, int ncols, float *out,
            void *stream);
 
+/* An activation whose codes cross the array in two words (lane page, opening
+ * description and WordSums; numerics page, Words): each code a 16-bit integer
+ * a = 256*hi + lo, hi its signed high byte and lo its unsigned low byte, with
+ * one scale m*2^e per `block` elements (m in 1..255; m == 0: no scale).
+ * codes int16 [ncols][K] (16-byte aligned), scales as qb_act's. */
+typedef struct {
+    int block;
+    const int16_t *codes;
+    const qb_scale *scales;
+} qb_act16;
+
+/* dot under PerBlock (numerics page) with two-word activation codes: for
+ * every row of W and column of act, each block's sums sum(coef*a) and
+ * sum(offs*a) formed exactly over the 16-bit codes (the lane page's per-word
+ * sums joined as 256*high + low), times the block's scales and m*2^e, summed
+ * exactly, rounded once, the rounded values added in block order from +0;
+ * out[c*rows + r].  fmt in {QB_Q8_0, QB_Q4K, QB_Q6K}; act->block the format's
+ * block; K % block == 0 and K small enough that a row's block values fit
+ * shared memory (K <= 2^18 for Q4K/Q6K, <= 2^15 for Q8_0, else QB_E_ARG);
+ * ncols in 1..16.  Unreadable weight scales and activation blocks without a
+ * scale give the engine's NaN rows, as in q_gemv.  Asynchronous on stream. */
+QB_API int q_gemv_w2(qb_fmt fmt, const void *W, int64_t rows, int64_t K, const qb_act16 *act, int ncols,
+                     float *out, void *stream);
+
 /* Bytes of the workspace q_matvec needs for a K x ncols activation: its
  * quantized form (codes, scales, unit sums; or the f16 rounding for QB_F16),
  * each part 16-byte aligned.  Negative QB_E_* for bad arguments. */

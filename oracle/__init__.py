@@ -68,6 +68,12 @@ def lib():
         L.or_gemv.argtypes, L.or_gemv.restype = [i32, P, i64, i64, P, P, P, i32, P], i32
         L.or_block_sums_excess.argtypes, L.or_block_sums_excess.restype = [i32, P, i64, i64, P, i32, P, P], i32
         L.or_count_unreadable.argtypes, L.or_count_unreadable.restype = [i32, P, i64, i64], i64
+        L.or_block_values_w2.argtypes = [i32, P, i64, i64, P, P, P, i32, P, P, P]
+        L.or_block_values_w2.restype = i32
+        L.or_gemv_w2_rows.argtypes = [i32, P, i64, i64, i64, i64, P, P, P, i32, P]
+        L.or_gemv_w2_rows.restype = i32
+        L.or_block_sums_excess_w2.argtypes = [i32, P, i64, i64, P, i32, P, P]
+        L.or_block_sums_excess_w2.restype = i32
         L.or_f32_to_f16.argtypes, L.or_f32_to_f16.restype = [ctypes.c_float], ctypes.c_uint16
         L.or_f16_to_f32.argtypes, L.or_f16_to_f32.restype = [ctypes.c_uint16], ctypes.c_float
         L.or_gemv_f16.argtypes, L.or_gemv_f16.restype = [P, i64, i64, P, i32, P], i32
@@ -222,6 +228,47 @@ def block_sums_excess(fmt: int, W: np.ndarray, rows: int, K: int, codes):
     C = np.zeros((ncols, rows, nb), np.int64); O = np.zeros_like(C)
     assert lib().or_block_sums_excess(fmt, _p(W), rows, K, _p(codes), ncols, _p(C), _p(O)) == 0
     return C, O
+
+
+def block_values_w2(fmt: int, W: np.ndarray, rows: int, K: int, codes16, m, e):
+    """Two-word (16-bit) activation codes: per (column, row, block) the exact
+    sums C, O (int64) and the rounded f32 value."""
+    codes16 = np.ascontiguousarray(np.atleast_2d(codes16), np.int16)
+    m = np.ascontiguousarray(np.atleast_2d(m), np.uint8)
+    e = np.ascontiguousarray(np.atleast_2d(e), np.int16)
+    W = np.ascontiguousarray(W, np.uint8)
+    ncols = codes16.shape[0]
+    nb = K // _BLOCK[fmt]
+    C = np.zeros((ncols, rows, nb), np.int64); O = np.zeros_like(C)
+    v = np.zeros((ncols, rows, nb), np.float32)
+    assert lib().or_block_values_w2(fmt, _p(W), rows, K, _p(codes16), _p(m), _p(e), ncols, _p(C), _p(O), _p(v)) == 0
+    return C, O, v
+
+
+def block_sums_excess_w2(fmt: int, W: np.ndarray, rows: int, K: int, codes16):
+    """The lane's two-word delivery: block sums rebuilt from the per-word unit sums."""
+    codes16 = np.ascontiguousarray(np.atleast_2d(codes16), np.int16)
+    W = np.ascontiguousarray(W, np.uint8)
+    ncols = codes16.shape[0]
+    nb = K // _BLOCK[fmt]
+    C = np.zeros((ncols, rows, nb), np.int64); O = np.zeros_like(C)
+    assert lib().or_block_sums_excess_w2(fmt, _p(W), rows, K, _p(codes16), ncols, _p(C), _p(O)) == 0
+    return C, O
+
+
+def gemv_w2(fmt: int, W: np.ndarray, rows: int, K: int, codes16, m, e, r0: int = 0, r1: int | None = None,
+            out: np.ndarray | None = None) -> np.ndarray:
+    """out f32 [ncols][rows] for two-word codes: the in-order fold of the rounded block values."""
+    codes16 = np.ascontiguousarray(np.atleast_2d(codes16), np.int16)
+    m = np.ascontiguousarray(np.atleast_2d(m), np.uint8)
+    e = np.ascontiguousarray(np.atleast_2d(e), np.int16)
+    W = np.ascontiguousarray(W, np.uint8)
+    ncols = codes16.shape[0]
+    if out is None:
+        out = np.zeros((ncols, rows), np.float32)
+    r1 = rows if r1 is None else r1
+    assert lib().or_gemv_w2_rows(fmt, _p(W), rows, r0, r1, K, _p(codes16), _p(m), _p(e), ncols, _p(out)) == 0
+    return out
 
 
 def gemv(fmt: int, W: np.ndarray, rows: int, K: int, codes, m, e, r0: int = 0, r1: int | None = None,

@@ -53,6 +53,9 @@
  *       640-bit integer), rounded once to nearest even, subnormals kept; a
  *       GPU result is held to the f32 summation bound
  *       (K + 4) * 2^-24 * sum |x_i * w_i| around it.
+ *   R20 (two-word codes) a code crossing in two words is the 16-bit integer
+ *       256*hi + lo (hi the signed high byte, lo the unsigned low byte);
+ *       its block sums, combine, rounding and fold are PerBlock's.
  *   R18 (int8 cache) a score against a key row whose f16 scale is infinite
  *       or NaN (a row whose amax*INV_127 overflows binary16) is NAN, as an
  *       unreadable weight scale is (R7); a query block without a scale too.
@@ -510,6 +513,133 @@ int or_block_sums_excess(int fmt, const uint8_t *W, int64_t rows, int64_t K, con
                     else { z = 32; cu = w.sc6[b * 16 + u]; nu = 0; }
                     Cs += cu * (P1 - 128 * Q - z * S1 + 128 * 16 * z);
                     Os += nu * (S1 - 128 * 16);
+                }
+                int64_t idx = ((int64_t)c * rows + r) * nb + b;
+                C[idx] = Cs;
+                O[idx] = Os;
+            }
+        }
+    }
+    row_free(&w);
+    return 0;
+}
+
+/* ---------------------------------------------------------------------
+ * Two-word activation codes (lane page, opening description and WordSums;
+ * numerics page, Words): a code that crosses in two words is a 16-bit integer
+ * a = 256*hi + lo, hi its signed high byte and lo its unsigned low byte.  The
+ * block's sums against such codes are the same definitions as block_sums --
+ * sum coef*a and sum offs*a, element by element -- now over 16-bit codes; the
+ * lane combines them with the block's scales and the activation scale
+ * exactly and rounds once (or_lane_value: the terms stay below 2^56, shifted
+ * by at most 29 places, inside its 128-bit sum), and dot adds the rounded
+ * values in block order.
+ * ------------------------------------------------------------------- */
+static void block_sums_w2(const or_row *w, int64_t b, const int16_t *a, or_block *ob) {
+    ob->C = 0; ob->O = 0; ob->kind = 0; ob->s2 = 0;
+    if (w->fmt == OR_Q8_0) {
+        for (int i = 0; i < 32; i++) ob->C += (int64_t)w->q8[b * 32 + i] * a[b * 32 + i];
+        ob->s1 = w->d[b];
+    } else if (w->fmt == OR_Q4K) {
+        for (int i = 0; i < 256; i++) {
+            int64_t e = b * 256 + i;
+            int s = i / 32;
+            ob->C += (int64_t)w->sc[b * 8 + s] * w->q[e] * a[e];
+            ob->O += (int64_t)w->mn[b * 8 + s] * a[e];
+        }
+        ob->s1 = w->d[b]; ob->s2 = w->dm[b]; ob->kind = 1;
+    } else {
+        for (int i = 0; i < 256; i++) {
+            int64_t e = b * 256 + i;
+            ob->C += (int64_t)w->sc6[b * 16 + i / 16] * ((int64_t)w->q[e] - 32) * a[e];
+        }
+        ob->s1 = w->d[b];
+    }
+}
+
+/* Per (column, row, block) sums and rounded values for two-word codes; layouts as or_block_values. */
+int or_block_values_w2(int fmt, const uint8_t *W, int64_t rows, int64_t K, const int16_t *codes,
+                       const uint8_t *am, const int16_t *ae, int ncols, int64_t *C, int64_t *O, float *v) {
+    or_row w;
+    int64_t nb = K / fmt_block(fmt), rec = or_record_bytes(fmt, K);
+    if (row_alloc(&w, fmt, K)) { row_free(&w); return -1; }
+    for (int64_t r = 0; r < rows; r++) {
+        row_unpack(&w, W + r * rec);
+        for (int c = 0; c < ncols; c++)
+            for (int64_t b = 0; b < nb; b++) {
+                or_block ob;
+                block_sums_w2(&w, b, codes + (int64_t)c * K, &ob);
+                int64_t idx = ((int64_t)c * rows + r) * nb + b;
+                if (C) C[idx] = ob.C;
+                if (O) O[idx] = ob.O;
+                if (v) v[idx] = or_lane_value(ob.C, ob.O, ob.s1, ob.s2, ob.kind,
+                                              am[(int64_t)c * nb + b], ae[(int64_t)c * nb + b]);
+            }
+    }
+    row_free(&w);
+    return 0;
+}
+
+/* dot for two-word codes: rows [r0, r1), out[c*rows + r], the rounded block values added in order from +0. */
+int or_gemv_w2_rows(int fmt, const uint8_t *W, int64_t rows, int64_t r0, int64_t r1, int64_t K,
+                    const int16_t *codes, const uint8_t *am, const int16_t *ae, int ncols, float *out) {
+    or_row w;
+    int64_t nb = K / fmt_block(fmt), rec = or_record_bytes(fmt, K);
+    if (row_alloc(&w, fmt, K)) { row_free(&w); return -1; }
+    for (int64_t r = r0; r < r1; r++) {
+        row_unpack(&w, W + r * rec);
+        for (int c = 0; c < ncols; c++) {
+            float acc = 0.0f;
+            for (int64_t b = 0; b < nb; b++) {
+                or_block ob;
+                block_sums_w2(&w, b, codes + (int64_t)c * K, &ob);
+                acc = or_ftz(acc + or_lane_value(ob.C, ob.O, ob.s1, ob.s2, ob.kind,
+                                                 am[(int64_t)c * nb + b], ae[(int64_t)c * nb + b]));
+            }
+            if (isnan(acc)) acc = engine_nan();
+            out[(int64_t)c * rows + r] = acc;
+        }
+    }
+    row_free(&w);
+    return 0;
+}
+
+/* The lane's two-word delivery (lane page, opening description): per
+ * 16-element unit and per word, P' = sum q*a', Q = sum q, S' = sum a', where
+ * the high word crosses in excess form (a' = hi + 128) and the low byte as
+ * itself (a' = lo); the unit's signed sums are the excess word's
+ *   P' - 128*Q - z*S' + 128*16*z  and  S' - 128*16
+ * weighted by 256, plus the low byte's  P' - z*S'  and  S'.  Block sums as in
+ * or_block_sums_excess. */
+int or_block_sums_excess_w2(int fmt, const uint8_t *W, int64_t rows, int64_t K, const int16_t *codes,
+                            int ncols, int64_t *C, int64_t *O) {
+    or_row w;
+    int blk = fmt_block(fmt);
+    int64_t nb = K / blk, rec = or_record_bytes(fmt, K);
+    if (row_alloc(&w, fmt, K)) { row_free(&w); return -1; }
+    for (int64_t r = 0; r < rows; r++) {
+        row_unpack(&w, W + r * rec);
+        for (int c = 0; c < ncols; c++) {
+            const int16_t *a = codes + (int64_t)c * K;
+            for (int64_t b = 0; b < nb; b++) {
+                int64_t Cs = 0, Os = 0;
+                for (int u = 0; u < blk / 16; u++) {
+                    int64_t Ph = 0, Pl = 0, Q = 0, Sh = 0, Sl = 0, z, cu, nu;
+                    for (int i = 0; i < 16; i++) {
+                        int64_t e = b * blk + 16 * u + i;
+                        int64_t code = a[e];
+                        int64_t lo = code & 255, hi = (code - lo) / 256;   /* code = 256*hi + lo, lo in 0..255 */
+                        int64_t ah = hi + 128;                             /* the high word in excess form */
+                        int64_t qu = (fmt == OR_Q8_0) ? (int64_t)w.q8[e] + 128 : (int64_t)w.q[e];
+                        Ph += qu * ah; Pl += qu * lo; Q += qu; Sh += ah; Sl += lo;
+                    }
+                    if (fmt == OR_Q8_0) { z = 128; cu = 1; nu = 0; }
+                    else if (fmt == OR_Q4K) { z = 0; cu = w.sc[b * 8 + u / 2]; nu = w.mn[b * 8 + u / 2]; }
+                    else { z = 32; cu = w.sc6[b * 16 + u]; nu = 0; }
+                    const int64_t dot = 256 * (Ph - 128 * Q - z * Sh + 128 * 16 * z) + (Pl - z * Sl);
+                    const int64_t sum = 256 * (Sh - 128 * 16) + Sl;
+                    Cs += cu * dot;
+                    Os += nu * sum;
                 }
                 int64_t idx = ((int64_t)c * rows + r) * nb + b;
                 C[idx] = Cs;

@@ -48,6 +48,12 @@ def test_host_argument_checks():
     assert L.q_gemv(qb.Q4K, None, 4, 256, ctypes.byref(act), 1, out, None) == qb.QB_E_ARG
     assert L.q_gemv(qb.Q4K, W, 4, 256, None, 1, out, None) == qb.QB_E_ARG
     assert L.q_gemv(qb.Q4K, W, 4, 256, ctypes.byref(act), 0, out, None) == qb.QB_E_ARG
+    a16 = qb._Act16(256, 16, 16)
+    assert L.q_gemv_w2(qb.Q4K, W, 4, 256, ctypes.byref(a16), 17, out, None) == qb.QB_E_ARG
+    assert L.q_gemv_w2(qb.Q4K, W, 4, 100, ctypes.byref(a16), 1, out, None) == qb.QB_E_ARG
+    assert L.q_gemv_w2(qb.Q8_0, W, 4, 256, ctypes.byref(a16), 1, out, None) == qb.QB_E_BLOCK
+    assert L.q_gemv_w2(3, W, 4, 256, ctypes.byref(a16), 1, out, None) == qb.QB_E_FORMAT
+    assert L.q_gemv_w2(qb.Q4K, W, 0, 256, ctypes.byref(a16), 1, out, None) == qb.QB_OK   # no rows: nothing to do
     assert L.q_gemv(qb.Q4K, W, 4, 256, ctypes.byref(act), 17, out, None) == qb.QB_E_ARG
     assert L.q_gemv(qb.Q4K, W, 4, 100, ctypes.byref(act), 1, out, None) == qb.QB_E_ARG
     assert L.q_gemv(qb.Q4K, ctypes.c_void_p(4097), 4, 256, ctypes.byref(act), 1, out, None) == qb.QB_E_ARG
