@@ -104,6 +104,14 @@ FP8 = {
 # (Q4_K-like) and the 128256x4096 Q6_K-like output -- each from its f32
 # activation in one q_matvec call (name: columns)
 STACK = {"stack_8b_b1": 1, "stack_8b_b4": 4, "stack_8b_b16": 16}
+
+# Activation codes that cross in two words (16-bit codes: a signed high byte
+# weighted by 256 and an unsigned low byte), q_gemv_w2 a step:
+# name: (fmt, rows, K, ncols, seed, description)
+W2 = {
+    "q4k_4096x4096_w2": (synth.FMT_Q4K, 4096, 4096, 1, 8,
+                         "Q4_K-like GEMV 4096x4096, batch 1, two-word (16-bit) activation codes"),
+}
 STACK_LAYERS = 32
 STACK_MATS = [("qkv", synth.FMT_Q4K, 6144, 4096), ("o", synth.FMT_Q4K, 4096, 4096),
               ("gate_up", synth.FMT_Q4K, 28672, 4096), ("down", synth.FMT_Q4K, 4096, 14336)]
@@ -120,7 +128,7 @@ def metric_for(workload):
     if workload in KV:
         return f"key-cache GB/s ({KV[workload][-1]})"
     desc = (WORKLOADS[workload][-1] if workload in WORKLOADS else GROUPED[workload][-1] if workload in GROUPED
-            else FFN[workload][-1] if workload in FFN else FP8[workload][-1])
+            else FFN[workload][-1] if workload in FFN else W2[workload][-1] if workload in W2 else FP8[workload][-1])
     return f"weight GB/s ({desc})"
 
 
@@ -1765,6 +1773,175 @@ def run_reference(args):
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
+# ---------------------------------------------------------------- two-word activation codes
+
+def _w2_inputs(fmt, rows, K, ncols, seed):
+    rng = np.random.default_rng(seed)
+    Wh = synth.pack(fmt, synth.draw(fmt, rng, rows, K))
+    nb = K // synth.BLOCK[fmt]
+    a16 = rng.integers(-32768, 32768, (ncols, K)).astype(np.int16)
+    m = rng.integers(128, 256, (ncols, nb)).astype(np.uint8)
+    e = rng.integers(-40, -10, (ncols, nb)).astype(np.int16)
+    return Wh, a16, m, e
+
+
+def _w2_packed(m, e):
+    return (m.astype(np.uint32) | (e.astype(np.int32).astype(np.uint32) << 16)).view(np.int32)
+
+
+def w2_oracle_pass(fmt, rows, K, Wh, a16, m, e, nthreads, row_limit=None):
+    import oracle
+    r_end = rows if row_limit is None else min(rows, row_limit)
+    out = np.zeros((a16.shape[0], rows), np.float32)
+    bounds = np.linspace(0, r_end, nthreads + 1).astype(int)
+    list(_pool(nthreads).map(lambda i: oracle.gemv_w2(fmt, Wh, rows, K, a16, m, e, int(bounds[i]),
+                                                       int(bounds[i + 1]), out), range(nthreads)))
+    return r_end
+
+
+def run_w2(args, rank, world):
+    """A step is one q_gemv_w2 call: the matrix times a two-word activation."""
+    import torch
+    import block_quantized_weight_quantize_gb300 as qb
+
+    fmt, rows, K, ncols, seed, desc = W2[args.workload]
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    Wh, a16, m, e = _w2_inputs(fmt, rows, K, ncols, seed + 1000 * rank)
+    wbytes = synth.weight_bytes(fmt, rows, K)
+    ncopy = max(2, -(-4 * L2_BYTES // wbytes))
+    W = torch.empty((ncopy, Wh.size), dtype=torch.uint8, device=dev)
+    W[0].copy_(torch.from_numpy(Wh))
+    for i in range(1, ncopy):
+        W[i].copy_(W[0])
+    ad = torch.from_numpy(a16).to(dev)
+    sd = torch.from_numpy(_w2_packed(m, e)).to(dev)
+    out = torch.empty((ncols, rows), dtype=torch.float32, device=dev)
+    stream = torch.cuda.Stream(dev)
+
+    def step(i, s):
+        qb.q_gemv_w2(fmt, W[i % ncopy], rows, K, ad, sd, ncols, out, s)
+
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            step(i, stream)
+    stream.synchronize()
+    g_one = one_graph_timing(capture_steps=lambda n0, n: [step(n0 + i, stream) for i in range(n)],
+                             stream=stream, warmup=args.warmup, steps=min(args.steps, 1000))
+    steps = min(args.steps, 1000)
+    if g_one is None:  # no event nodes in this torch: one graph of the steps between two stream events
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            g.capture_begin()
+            for i in range(steps):
+                step(i, stream)
+            g.capture_end()
+            g.replay()
+        stream.synchronize()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev.index) as clk:
+        barrier()
+        torch.cuda.synchronize()
+        if g_one is not None:
+            g, t0, t1 = g_one
+            with torch.cuda.stream(stream):
+                g.replay()
+        else:
+            with torch.cuda.stream(stream):
+                t0.record(stream)
+                g.replay()
+                t1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        ms = max_over_ranks(t0.elapsed_time(t1), dev)
+    clocks = clk.summary()
+    step_s = ms / 1e3 / steps
+    # e2e: host codes in, the call, host result out, one step at a time on the stream
+    ah = torch.from_numpy(a16).pin_memory()
+    oh = torch.empty((ncols, rows), dtype=torch.float32).pin_memory()
+    n_e2e = min(steps, 2000)
+    barrier()
+    t0h = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for i in range(n_e2e):
+            ad.copy_(ah, non_blocking=True)
+            step(i, stream)
+            oh.copy_(out, non_blocking=True)
+    stream.synchronize()
+    e2e_s = max_over_ranks(time.perf_counter() - t0h, dev)
+    assert qb.q_device_status() == qb.QB_OK
+    peak, peak_kind = measured_peaks()
+    roof_bytes = wbytes + 2 * K * ncols + 4 * (K // synth.BLOCK[fmt]) * ncols + 4 * rows * ncols
+    value = world * wbytes / step_s / 1e9
+    res = {
+        "metric": metric_for(args.workload), "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": steps, "warmup": args.warmup, "ms_per_step": round(ms / steps, 6), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "int8 codes x 16-bit codes (two words), exact int64/int128, "
+                                                          "f32 rounding",
+        "data": "synthetic (seeded PCG64; 16-bit codes uniform over their range, m in 128..255, e in -40..-11)",
+        "config": {"workload": desc, "rows": rows, "K": K, "ncols": ncols, "format": synth.FORMAT_NAMES[fmt],
+                   "weight_bytes_per_step": wbytes,
+                   "l2": f"each step reads a different one of {ncopy} weight copies; no flush",
+                   "timing": f"CUDA graph of {steps} q_gemv_w2 steps (one launch each); CUDA events",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "rows_per_s": round(world * rows / step_s, 1),
+        "frac_of_8tbs": round(value / 8000.0, 4), "frac_of_measured_copy": round(value / peak, 4),
+        "gpu_launches": steps, "clocks": clocks,
+        "roofline": {"bound": "hbm", "kernel": f"w2_kernel<{synth.FORMAT_NAMES[fmt]}> (a warp a row, lanes over "
+                                               "blocks, per-word dp4a sums)",
+                     "achieved": round(roof_bytes / step_s / 1e9, 1), "peak": peak,
+                     "peak_kind": f"{peak_kind} (HBM copy, burst)", "unit": "GB/s",
+                     "frac": round(roof_bytes / step_s / 1e9 / peak, 4), "traffic": traffic_for(args.workload),
+                     "algorithmic_bytes_per_launch": roof_bytes, "avg_launch_us": round(step_s * 1e6, 4)},
+        "e2e": {"value": round(world * wbytes * n_e2e / e2e_s / 1e9, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": int(a16.nbytes), "d2h_bytes_per_step": int(4 * rows * ncols),
+                "steps": n_e2e, "how": "per step: the codes copied from pinned host memory, q_gemv_w2, the result "
+                                       "copied back to pinned host memory, all on the stream; host wall clock"},
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        n = _oracle_threads()
+        w2_oracle_pass(fmt, rows, K, Wh, a16, m, e, n)
+        reps, t0c = 0, time.perf_counter()
+        while True:
+            w2_oracle_pass(fmt, rows, K, Wh, a16, m, e, n)
+            reps += 1
+            el = time.perf_counter() - t0c
+            if el >= args.cpu_seconds:
+                break
+        res["cpu_baseline"] = {"value": round(wbytes * reps / el / 1e9, 4), "unit": "GB/s", "cores": n,
+                               "kind": "oracle", "sample": f"{reps} full passes over all {rows} rows in {el:.1f} s, "
+                                                           f"rows split over {n} threads of the scalar C oracle",
+                               "cpu_model": cpu_model()}
+    return res
+
+
+def run_w2_reference(args):
+    fmt, rows, K, ncols, seed, desc = W2[args.workload]
+    Wh, a16, m, e = _w2_inputs(fmt, rows, K, ncols, seed)
+    n = _oracle_threads()
+    t0 = time.perf_counter()
+    w2_oracle_pass(fmt, rows, K, Wh, a16, m, e, n)
+    full = time.perf_counter() - t0
+    budget = 100.0 / max(1, args.steps + args.warmup)
+    rows_s = int(max(1, min(rows, rows * budget / max(full, 1e-6))))
+    for _ in range(args.warmup):
+        w2_oracle_pass(fmt, rows, K, Wh, a16, m, e, n, rows_s)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        w2_oracle_pass(fmt, rows, K, Wh, a16, m, e, n, rows_s)
+    el = time.perf_counter() - t0
+    value = synth.record_bytes(fmt, K) * rows_s * args.steps / el / 1e9
+    sample = f"each step: {rows_s} of {rows} rows, split over {n} threads of the scalar C oracle"
+    return {
+        "impl": "reference", "metric": metric_for(args.workload), "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": 0, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el * 1e3 / args.steps, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "int64/int128 exact, f32 rounding (scalar C)", "data": "synthetic (seeded PCG64)",
+        "config": {"workload": desc, "rows": rows, "K": K, "ncols": ncols},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": n, "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
 
 def main():
     ap = argparse.ArgumentParser()
@@ -1773,7 +1950,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=1000)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="q4k_4096x4096", choices=sorted(WORKLOADS) + sorted(GROUPED) + sorted(FFN) + sorted(KV) + sorted(FP8) +
-                    sorted(STACK))
+                    sorted(STACK) + sorted(W2))
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--roof-launches", type=int, default=2000,
@@ -1794,6 +1971,8 @@ def main():
                 print(json.dumps(run_fp8_reference(args)), flush=True)
             elif args.workload in STACK:
                 print(json.dumps(run_stack_reference(args)), flush=True)
+            elif args.workload in W2:
+                print(json.dumps(run_w2_reference(args)), flush=True)
             else:
                 print(json.dumps(run_reference(args)), flush=True)
         return
@@ -1806,7 +1985,8 @@ def main():
            run_stack(args, rank, world) if args.workload in STACK else
            run_ffn(args, rank, world) if args.workload in FFN else
            run_kv(args, rank, world) if args.workload in KV else
-           run_fp8(args, rank, world) if args.workload in FP8 else run_ours(args, rank, world))
+           run_fp8(args, rank, world) if args.workload in FP8 else
+           run_w2(args, rank, world) if args.workload in W2 else run_ours(args, rank, world))
     if rank == 0:
         print(json.dumps(res), flush=True)
     if world > 1:

@@ -46,13 +46,11 @@
 #include <cstring>
 #include <mutex>
 
-#include <cuda.h>
-#include <cudaTypedefs.h>
-
 #include "qb_common.cuh"
 #include "qb_gemv2.cuh"
 #include "qb_launch.h"
 #include "qb_mats.cuh"
+#include "qb_tmap.cuh"
 
 namespace qb {
 
@@ -376,13 +374,6 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
 //   mdone[s]   the MMAs reading stage buffer s are done (commit -> decoders)
 //   dfull[t]   accumulator t holds a finished block    (commit -> combiners)
 //   dempty[t]  accumulator t has been read             (8 combiner warps -> MMA)
-__device__ __forceinline__ void tma_box_2d(void *dst, const CUtensorMap *map, int x, int y, uint64_t *bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
-            "r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
-        : "memory");
-}
 __device__ __forceinline__ void st_cluster_f32_nc(uint32_t addr, float v) {
     asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v));
 }
@@ -762,34 +753,6 @@ inline int tc_active_ctas(int ks, int smem) {
     return v;
 }
 
-// cuTensorMapEncodeTiled from the driver, looked up once.
-inline PFN_cuTensorMapEncodeTiled_v12000 tc_encoder() {
-    static std::once_flag once;
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    std::call_once(once, [] {
-        void *f = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-    });
-    return fn;
-}
-
-// A matrix of `rows` records of `rec` bytes as a 2-D byte tensor, read in boxes of `bx` bytes x 128 rows.
-inline bool tc_map(CUtensorMap *m, const void *W, int64_t rows, int64_t rec, int bx) {
-    auto enc = tc_encoder();
-    if (!enc) return false;
-    const cuuint64_t dims[2] = {(cuuint64_t)rec, (cuuint64_t)rows};
-    const cuuint64_t strides[1] = {(cuuint64_t)rec};
-    const cuuint32_t box[2] = {(cuuint32_t)bx, (cuuint32_t)kTcRows};
-    const cuuint32_t es[2] = {1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(W), dims, strides, box, es,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 // The Q4_K-like / Q6_K-like product of 1..16 columns on the tensor cores;
 // QB_E_ARG where it does not take the shape (the caller then uses another kernel).
 template <int F>
@@ -810,8 +773,8 @@ int launch_tc(const GemvArgs &a, cudaStream_t stream) {
         const int64_t ri = k.mt.start[i + 1] - k.mt.start[i];
         k.tstart[i] = tiles;
         if (ri > 0 && (reinterpret_cast<uintptr_t>(k.mt.W[i]) % 16 != 0 || ri > (int64_t(1) << 31))) return QB_E_ARG;
-        if (ri > 0 && !tc_map(&k.tmap[i], k.mt.W[i], ri, k.rec, F == kQ4K ? 144 : 208)) return QB_E_ARG;
-        if (ri > 0 && F == kQ6K && !tc_map(&k.dmap[i], k.mt.W[i], ri, k.rec, 64)) return QB_E_ARG;
+        if (ri > 0 && !tmap_rows(&k.tmap[i], k.mt.W[i], ri, k.rec, F == kQ4K ? 144 : 208, kTcRows)) return QB_E_ARG;
+        if (ri > 0 && F == kQ6K && !tmap_rows(&k.dmap[i], k.mt.W[i], ri, k.rec, 64, kTcRows)) return QB_E_ARG;
         tiles += (ri + kTcRows - 1) / kTcRows;
     }
     for (int i = k.mt.n; i <= kMaxMats; ++i) k.tstart[i] = tiles;

@@ -503,6 +503,32 @@ def test_one_column_long_rows(fmt, rows, K):
 
 
 @pytest.mark.parametrize("fmt", [synth.FMT_Q4K, synth.FMT_Q6K])
+@pytest.mark.parametrize("K", [4352, 6400, 14336, 16384])
+@pytest.mark.parametrize("rows", [1, 152 * 27 - 8, 4096, 152 * 32, 152 * 32 + 1])
+def test_long_k_row_ranges(fmt, K, rows):
+    """One column of rows longer than K = 4096 from a quantized activation (17,
+    25, 56 and 64 blocks a row) over row counts around 27 and 32 rows a CTA;
+    an unreadable block scale in the last block and a zero activation block."""
+    import torch
+    rng = np.random.default_rng(rows + 3 * K + fmt)
+    lg = synth.draw(fmt, rng, rows, K)
+    lg["d"][rows // 2, K // 256 - 1] = 0x7E00                   # unreadable, in the last chunk
+    W = synth.pack(fmt, lg)
+    x = synth.draw_act(rng, 1, K, outlier_frac=0.001)
+    x[0, 256:512] = 0.0
+    codes, m, e, s16, packed = oracle_act(x, 256)
+    want = oracle.gemv(fmt, W, rows, K, codes, m, e)
+    act = qb.alloc_act(1, K, 256)
+    qb.quantize_act(256, dev(x), *act)
+    out = torch.full((1, rows), float("nan"), dtype=torch.float32, device="cuda")
+    qb.q_gemv(fmt, dev(W), rows, K, act, 1, out)
+    torch.cuda.synchronize()
+    got = host(out)
+    assert np.array_equal(bits(got), bits(want))
+    assert bits(got)[0, rows // 2] == 0x7FC00000
+
+
+@pytest.mark.parametrize("fmt", [synth.FMT_Q4K, synth.FMT_Q6K])
 @pytest.mark.parametrize("ncols", [1, 2, 3, 4])
 @pytest.mark.parametrize("rows", [1, 31, 152, 152 * 31 + 7, 152 * 32, 152 * 32 + 1, 152 * 64, 152 * 64 + 1])
 def test_k4096_row_ranges(fmt, ncols, rows):

@@ -95,7 +95,7 @@ def _all_workloads():
     sys.path.insert(0, ROOT)
     import bench
     return (sorted(bench.WORKLOADS) + sorted(bench.GROUPED) + sorted(bench.FFN) + sorted(bench.KV) +
-            sorted(bench.FP8) + sorted(bench.STACK))
+            sorted(bench.FP8) + sorted(bench.STACK) + sorted(bench.W2))
 
 
 @pytest.mark.parametrize("workload", _all_workloads())
