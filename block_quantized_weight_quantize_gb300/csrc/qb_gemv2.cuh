@@ -98,6 +98,13 @@ __device__ __forceinline__ float round_fast(long long n, int E) {
     return round_to_f32_cold(n, E);  // out of line: rare
 }
 
+// The two terms of a block whose scale exponents lie more than 17 (or 21)
+// places apart: combined in 128 bits.  Out of line: rare.
+static __device__ __noinline__ float lane_value_spread(long long t1, long long t2, int d, int ex1, int ex2, int e) {
+    const __int128 w = d >= 0 ? ((__int128)t1 << d) + t2 : (__int128)t1 + ((__int128)t2 << (-d));
+    return round_to_f32_wide(w, (d >= 0 ? ex2 : ex1) + e);
+}
+
 template <int KIND>
 __device__ __forceinline__ float lane_value_fast(int C, int O, uint32_t s1, uint32_t s2, int m, int e) {
     int sig1, ex1;
@@ -112,10 +119,11 @@ __device__ __forceinline__ float lane_value_fast(int C, int O, uint32_t s1, uint
         const long long t1 = (long long)(sig1 * m) * (long long)C;   // |t1| < 2^44
         const long long t2 = -(long long)(sig2 * m) * (long long)O;  // |t2| < 2^40
         const int d = ex1 - ex2;
-        if (d >= 0 && d <= 17) return round_fast((t1 << d) + t2, ex2 + e);
-        if (d < 0 && d >= -21) return round_fast(t1 + (t2 << (-d)), ex1 + e);
-        const __int128 w = d >= 0 ? ((__int128)t1 << d) + t2 : (__int128)t1 + ((__int128)t2 << (-d));
-        return round_to_f32_wide(w, (d >= 0 ? ex2 : ex1) + e);
+        if (d > 17 || d < -21) return lane_value_spread(t1, t2, d, ex1, ex2, e);
+        // the term of the larger exponent shifted up to the other's: no branch
+        // on the sign of d, whose lanes (rows) would otherwise take both forms
+        const int sh1 = d > 0 ? d : 0, sh2 = d < 0 ? -d : 0;
+        return round_fast((t1 << sh1) + (t2 << sh2), (d >= 0 ? ex2 : ex1) + e);
     }
 }
 

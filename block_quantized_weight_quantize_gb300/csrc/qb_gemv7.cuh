@@ -91,56 +91,44 @@ __device__ __forceinline__ void block_q4k(const uint8_t *blk, const uint8_t *a, 
     O = dp2a_hi_su(sw.w, mb1, dp2a_lo_su(sw.z, mb1, dp2a_hi_su(sw.y, mb0, dp2a_lo_su(sw.x, mb0, 0))));
 }
 
-// block_q4k for two activation columns at once (codes a0/a1, sums S0/S1): the
-// weights are read and unpacked once for both.
-template <int UNR>
-__device__ __forceinline__ void block_q4k_pair(const uint8_t *blk, const uint8_t *a0, const uint8_t *a1,
-                                               const int16_t *S0, const int16_t *S1, int &C0, int &O0, int &C1,
-                                               int &O1, uint32_t &dd) {
+// block_q4k for NC activation columns (codes at a + c*stride, sums at
+// S + c*sstride): the weights read and unpacked once for all of them.
+template <int NC>
+__device__ __forceinline__ void block_q4k_cols(const uint8_t *blk, const uint8_t *a, int stride, const int16_t *S,
+                                               int sstride, int (&C)[NC], int (&O)[NC], uint32_t &dd) {
     const uint4 meta = *reinterpret_cast<const uint4 *>(blk);
     dd = meta.x;
     const unsigned long long sc48 = (unsigned long long)meta.y | ((unsigned long long)(meta.z & 0xFFFFu) << 32);
     const unsigned long long mn48 = (unsigned long long)(meta.z >> 16) | ((unsigned long long)meta.w << 16);
-    int c0 = 0, c1 = 0;
-#pragma unroll UNR
+#pragma unroll
+    for (int c = 0; c < NC; ++c) C[c] = 0;
+#pragma unroll 2
     for (int s = 0; s < 8; ++s) {
         const uint4 w = *reinterpret_cast<const uint4 *>(blk + 16 + 16 * s);
-        const uint32_t l[4] = {w.x & 0x0F0F0F0Fu, w.y & 0x0F0F0F0Fu, w.z & 0x0F0F0F0Fu, w.w & 0x0F0F0F0Fu};
-        const uint32_t g[4] = {w.x & 0xF0F0F0F0u, w.y & 0xF0F0F0F0u, w.z & 0xF0F0F0F0u, w.w & 0xF0F0F0F0u};
+        const uint32_t l0 = w.x & 0x0F0F0F0Fu, l1 = w.y & 0x0F0F0F0Fu, l2 = w.z & 0x0F0F0F0Fu, l3 = w.w & 0x0F0F0F0Fu;
+        const uint32_t g0 = w.x & 0xF0F0F0F0u, g1 = w.y & 0xF0F0F0F0u, g2 = w.z & 0xF0F0F0F0u, g3 = w.w & 0xF0F0F0F0u;
         const int sc = (int)((sc48 >> (6 * s)) & 63u);
-        {
-            const uint4 al = *reinterpret_cast<const uint4 *>(a0 + 32 * s);
-            const uint4 ah = *reinterpret_cast<const uint4 *>(a0 + 32 * s + 16);
-            int pl = dp4a_ss(l[0], al.x, 0);
-            pl = dp4a_ss(l[1], al.y, pl);
-            pl = dp4a_ss(l[2], al.z, pl);
-            pl = dp4a_ss(l[3], al.w, pl);
-            int ph = dp4a_us(g[0], ah.x, 0);
-            ph = dp4a_us(g[1], ah.y, ph);
-            ph = dp4a_us(g[2], ah.z, ph);
-            ph = dp4a_us(g[3], ah.w, ph);
-            c0 += sc * (16 * pl + ph);
-        }
-        {
-            const uint4 al = *reinterpret_cast<const uint4 *>(a1 + 32 * s);
-            const uint4 ah = *reinterpret_cast<const uint4 *>(a1 + 32 * s + 16);
-            int pl = dp4a_ss(l[0], al.x, 0);
-            pl = dp4a_ss(l[1], al.y, pl);
-            pl = dp4a_ss(l[2], al.z, pl);
-            pl = dp4a_ss(l[3], al.w, pl);
-            int ph = dp4a_us(g[0], ah.x, 0);
-            ph = dp4a_us(g[1], ah.y, ph);
-            ph = dp4a_us(g[2], ah.z, ph);
-            ph = dp4a_us(g[3], ah.w, ph);
-            c1 += sc * (16 * pl + ph);
+#pragma unroll
+        for (int c = 0; c < NC; ++c) {
+            const uint4 al = *reinterpret_cast<const uint4 *>(a + c * stride + 32 * s);
+            const uint4 ah = *reinterpret_cast<const uint4 *>(a + c * stride + 32 * s + 16);
+            int pl = dp4a_ss(l0, al.x, 0);
+            pl = dp4a_ss(l1, al.y, pl);
+            pl = dp4a_ss(l2, al.z, pl);
+            pl = dp4a_ss(l3, al.w, pl);
+            int ph = dp4a_us(g0, ah.x, 0);
+            ph = dp4a_us(g1, ah.y, ph);
+            ph = dp4a_us(g2, ah.z, ph);
+            ph = dp4a_us(g3, ah.w, ph);
+            C[c] += sc * (16 * pl + ph);
         }
     }
-    C0 = c0;
-    C1 = c1;
     const uint32_t mb0 = spread6((uint32_t)mn48 & 0xFFFFFFu), mb1 = spread6((uint32_t)(mn48 >> 24));
-    const uint4 s0 = *reinterpret_cast<const uint4 *>(S0), s1 = *reinterpret_cast<const uint4 *>(S1);
-    O0 = dp2a_hi_su(s0.w, mb1, dp2a_lo_su(s0.z, mb1, dp2a_hi_su(s0.y, mb0, dp2a_lo_su(s0.x, mb0, 0))));
-    O1 = dp2a_hi_su(s1.w, mb1, dp2a_lo_su(s1.z, mb1, dp2a_hi_su(s1.y, mb0, dp2a_lo_su(s1.x, mb0, 0))));
+#pragma unroll
+    for (int c = 0; c < NC; ++c) {
+        const uint4 sw = *reinterpret_cast<const uint4 *>(S + c * sstride);
+        O[c] = dp2a_hi_su(sw.w, mb1, dp2a_lo_su(sw.z, mb1, dp2a_hi_su(sw.y, mb0, dp2a_lo_su(sw.x, mb0, 0))));
+    }
 }
 
 // Q6_K-like block at blk (ql, qh, 16 int8 sub-scales) against the warp's codes a
@@ -394,7 +382,8 @@ __host__ __device__ inline int gemv7m_smem(int nc, int rows, int pitch) { return
 // NC activation columns (2..4) in one launch: each warp prepares block w of
 // every column (quantizing it in the single-launch form), each lane forms its
 // rows' block w for every column from the one copy of the weights in shared
-// memory, column by column.
+// memory (Q4_K-like: the weights unpacked once for all the columns;
+// Q6_K-like: column by column).
 template <int F, bool FUSED, int MINB, int UNR, int NC>
 __global__ void __launch_bounds__(kG7Warps * 32, MINB) gemv7m_kernel(const Gemv7K p) {
     extern __shared__ __align__(128) uint8_t smem[];
@@ -430,14 +419,24 @@ __global__ void __launch_bounds__(kG7Warps * 32, MINB) gemv7m_kernel(const Gemv7
     // ---- block w of the activation, each column: codes (natural order), the
     // sums the format needs (Q4_K-like: per 32-element sub-block; Q6_K-like:
     // per 16-element unit) and the block's scale
+    // every column's elements requested before the first is quantized (the
+    // quantizer's shuffles would otherwise hold each load behind the last)
+    float4 xv[FUSED ? 2 * NC : 1];
+    if constexpr (FUSED) {
+#pragma unroll
+        for (int col = 0; col < NC; ++col) {
+            const float4 *xp = reinterpret_cast<const float4 *>(p.x + (int64_t)col * kG7K + 256 * w + 8 * lane);
+            xv[2 * col] = ldg_f4_ordered(xp);
+            xv[2 * col + 1] = ldg_f4_ordered(xp + 1);
+        }
+    }
 #pragma unroll
     for (int col = 0; col < NC; ++col) {
         uint32_t scale;
         uint8_t *ac = aw + col * kG7K;
         int16_t *Sc = Sw + col * (kG7Warps * 16);
         if constexpr (FUSED) {
-            const float4 *xp = reinterpret_cast<const float4 *>(p.x + (int64_t)col * kG7K + 256 * w + 8 * lane);
-            const float4 v0 = ldg_f4_ordered(xp), v1 = ldg_f4_ordered(xp + 1);
+            const float4 v0 = xv[2 * col], v1 = xv[2 * col + 1];
             const uint32_t xb[8] = {__float_as_uint(v0.x), __float_as_uint(v0.y), __float_as_uint(v0.z),
                                     __float_as_uint(v0.w), __float_as_uint(v1.x), __float_as_uint(v1.y),
                                     __float_as_uint(v1.z), __float_as_uint(v1.w)};
@@ -474,20 +473,17 @@ __global__ void __launch_bounds__(kG7Warps * 32, MINB) gemv7m_kernel(const Gemv7
         for (int r = lane; r < count; r += 32) {
             const uint8_t *row = slab + r * p.pitch;
             int col = 0;
-            if (F == kQ4K) {  // columns in pairs: the weights unpacked once for two
-#pragma unroll 1
-                for (; col + 1 < NC; col += 2) {
-                    int C0, O0, C1, O1;
-                    uint32_t dd;
-                    block_q4k_pair<UNR>(row + 144 * w, aw + col * kG7K, aw + (col + 1) * kG7K,
-                                        Sw + col * (kG7Warps * 16), Sw + (col + 1) * (kG7Warps * 16), C0, O0, C1, O1,
-                                        dd);
-                    const uint32_t sv0 = sclw[col * kG7Warps], sv1 = sclw[(col + 1) * kG7Warps];
-                    vals[r * VS + col * 17 + w] = lane_value_fast<1>(C0 >> 4, O0, dd & 0xFFFFu, dd >> 16,
-                                                                     (int)(sv0 & 0xFFu), (int)(int16_t)(sv0 >> 16));
-                    vals[r * VS + (col + 1) * 17 + w] = lane_value_fast<1>(
-                        C1 >> 4, O1, dd & 0xFFFFu, dd >> 16, (int)(sv1 & 0xFFu), (int)(int16_t)(sv1 >> 16));
+            if (F == kQ4K) {  // every column at once: the weights unpacked once
+                int C[NC], O[NC];
+                uint32_t dd;
+                block_q4k_cols<NC>(row + 144 * w, aw, kG7K, Sw, kG7Warps * 16, C, O, dd);
+#pragma unroll
+                for (int cc = 0; cc < NC; ++cc) {
+                    const uint32_t sv = sclw[cc * kG7Warps];
+                    vals[r * VS + cc * 17 + w] = lane_value_fast<1>(C[cc] >> 4, O[cc], dd & 0xFFFFu, dd >> 16,
+                                                                    (int)(sv & 0xFFu), (int)(int16_t)(sv >> 16));
                 }
+                col = NC;
             }
 #pragma unroll 1
             for (; col < NC; ++col) {

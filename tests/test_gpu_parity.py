@@ -559,6 +559,41 @@ def test_k4096_row_ranges(fmt, ncols, rows):
     assert np.array_equal(bits(host(out)), bits(want))
 
 
+@pytest.mark.parametrize("ncols", [1, 2, 3, 4])
+@pytest.mark.parametrize("rows,K", [(300, 4096), (152 * 64 + 1, 4096), (200, 14336)])
+def test_scale_exponent_gaps(ncols, rows, K):
+    """Q4_K-like blocks whose d and dmin exponents differ by every gap on
+    either side of the combine's thresholds (d's term shifted up by at most
+    17 places, dmin's by at most 21, a 128-bit combine past those), one gap a
+    block and the gaps of neighbouring rows different, so that the lanes of a
+    warp take different shifts: through the product and the single-launch form."""
+    import torch
+    fmt = synth.FMT_Q4K
+    rng = np.random.default_rng(rows + K + ncols)
+    lg = synth.draw(fmt, rng, rows, K)
+    gaps = np.array([-29, -22, -21, -20, -7, -1, 0, 1, 9, 16, 17, 18, 29])
+    nb = K // 256
+    g = gaps[(np.arange(rows)[:, None] * 5 + np.arange(nb)[None, :] * 3) % len(gaps)]
+    E2 = rng.integers(1, 31, size=g.shape)
+    E2 = np.clip(E2, np.maximum(1, 1 - g), np.minimum(30, 30 - g))   # both exponents normal
+    E1 = E2 + g
+    lg["d"] = ((E1 << 10) | rng.integers(0, 1024, size=g.shape)).astype(np.uint16)
+    lg["dmin"] = ((E2 << 10) | rng.integers(0, 1024, size=g.shape)).astype(np.uint16)
+    W = synth.pack(fmt, lg)
+    x = synth.draw_act(rng, ncols, K, outlier_frac=0.001)
+    codes, m, e, s16, packed = oracle_act(x, 256)
+    want = oracle.gemv(fmt, W, rows, K, codes, m, e)
+    out = torch.full((ncols, rows), float("nan"), dtype=torch.float32, device="cuda")
+    qb.q_gemv(fmt, dev(W), rows, K, gpu_quantize(x, 256), ncols, out)
+    torch.cuda.synchronize()
+    assert np.array_equal(bits(host(out)), bits(want))
+    out.fill_(float("nan"))
+    ws = torch.empty(qb.q_matvec_workspace_bytes(fmt, K, ncols), dtype=torch.uint8, device="cuda")
+    qb.q_matvec(fmt, dev(W), rows, K, dev(x), out, workspace=ws)
+    torch.cuda.synchronize()
+    assert np.array_equal(bits(host(out)), bits(want))
+
+
 def test_matvec_repeated_launches_graph():
     """Many single-launch products back to back (programmatic dependent launch
     overlapping each launch's weight stream with the previous one) on distinct
