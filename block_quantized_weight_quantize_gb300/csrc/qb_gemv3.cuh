@@ -474,7 +474,11 @@ bool gemv3_shape(int64_t rows, int64_t K, int ncols, Gemv3K &k, int &grid, int &
     if (fused && K / 8 > 4 * threads) return false;
     k.H = std::max(1, std::min({k.n_iter, 8, threads / (k.nt * 2 * ncp)}));  // about one fold line a thread
     const int hist = L(0, k.H);
-    k.D = std::max(1, std::min({k.n_iter, 4, (budget - hist) / (2 * k.nt * k.rec)}));
+    // one column: two slots in flight.  With more, every slot of every CTA is
+    // requested at once and they land together near the end of the stream,
+    // leaving all the arithmetic for after it (Q4_K-like 4096 x 14336: 8.43 ->
+    // 7.83 us with two)
+    k.D = std::max(1, std::min({k.n_iter, CG == 1 ? 2 : 4, (budget - hist) / (2 * k.nt * k.rec)}));
     while (L(k.D, k.H) > budget && k.H > 1) --k.H;
     smem = L(k.D, k.H);
     return smem <= 227 * 1024;

@@ -550,16 +550,195 @@ int launch_gemv7m(const GemvArgs &a, cudaStream_t stream, const float *x) {
     return launch_pdl(kern, dim3(grid), dim3(kG7Warps * 32), (size_t)smem, stream, k);
 }
 
+// ---------------------------------------------------------------- many rows, 2..4 columns
+// The multi-column form over more rows than one slab holds (Q4_K-like): the
+// CTA's rows stream through a ring of two 32-row tiles.  As above, warp w
+// forms block w of every row of a tile (a lane a row) for every column with
+// the weights unpacked once; after each tile four warps fold its rows while
+// the tile two ahead is being fetched into the slot it leaves.
+constexpr int kG7RTile = 32;   // rows a tile (a lane a row)
+constexpr int kG7RSlots = 2;   // tiles in flight
+
+struct Gemv7RSmem {
+    int scl, act, sums, vals, slab, total;
+};
+__host__ __device__ inline Gemv7RSmem gemv7r_layout(int nc, int pitch) {
+    Gemv7RSmem s;
+    s.scl = 128;  // the slots' mbarriers at 0
+    s.act = s.scl + ((nc * kG7Warps * 4 + 127) & ~127);
+    s.sums = s.act + nc * kG7K;
+    s.vals = s.sums + nc * kG7Warps * 32;
+    s.slab = s.vals + ((kG7RTile * gemv7m_vs(nc) * 4 + 127) & ~127);
+    s.total = s.slab + kG7RSlots * kG7RTile * pitch;
+    return s;
+}
+
+template <bool FUSED, int NC>
+__global__ void __launch_bounds__(kG7Warps * 32, 1) gemv7r_kernel(const Gemv7K p) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    const Gemv7RSmem Lo = gemv7r_layout(NC, p.pitch);
+    constexpr int VS = gemv7m_vs(NC);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem);
+    uint32_t *sclw = reinterpret_cast<uint32_t *>(smem + Lo.scl) + w;  // column c at + c * 16
+    uint8_t *aw = smem + Lo.act + 256 * w;                             // column c at + c * K
+    int16_t *Sw = reinterpret_cast<int16_t *>(smem + Lo.sums + 32 * w);  // column c at + c * 256
+    float *vals = reinterpret_cast<float *>(smem + Lo.vals);
+    uint8_t *slab = smem + Lo.slab;
+
+    const int64_t c = blockIdx.x;
+    const int64_t row0 = c * p.base + (c < p.rem ? c : p.rem);
+    const int count = (int)(p.base + (c < p.rem ? 1 : 0));
+    const int ntiles = (count + kG7RTile - 1) / kG7RTile;
+    // tile t into slot t % kG7RSlots, a copy a row by the lanes of warp 0
+    auto fill = [&](int t) {
+        const int n = min(kG7RTile, count - t * kG7RTile);
+        uint64_t *bar = bars + t % kG7RSlots;
+        if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)(n * p.rec));
+        __syncwarp();
+        uint8_t *dst = slab + (t % kG7RSlots) * (kG7RTile * p.pitch);
+        if (lane < n)
+            bulk_g2s(dst + lane * p.pitch, row_ptr(p.mt, row0 + (int64_t)t * kG7RTile + lane, p.rec),
+                     (uint32_t)p.rec, bar);
+    };
+
+    if (tid == 0) {
+        for (int s = 0; s < kG7RSlots; ++s) mbar_init(bars + s, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    // the first tiles (weights depend on no earlier kernel)
+    if (w == 0)
+        for (int t = 0; t < kG7RSlots && t < ntiles; ++t) fill(t);
+    // the next launch may be scheduled now: it reads nothing this one writes
+    // before its own pdl_wait, which returns once this grid has finished
+    pdl_launch_dependents();
+    pdl_wait();
+
+    // ---- block w of the activation, each column (as in gemv7m_kernel)
+    float4 xv[FUSED ? 2 * NC : 1];
+    if constexpr (FUSED) {
+#pragma unroll
+        for (int col = 0; col < NC; ++col) {
+            const float4 *xp = reinterpret_cast<const float4 *>(p.x + (int64_t)col * kG7K + 256 * w + 8 * lane);
+            xv[2 * col] = ldg_f4_ordered(xp);
+            xv[2 * col + 1] = ldg_f4_ordered(xp + 1);
+        }
+    }
+#pragma unroll
+    for (int col = 0; col < NC; ++col) {
+        uint32_t scale;
+        uint8_t *ac = aw + col * kG7K;
+        int16_t *Sc = Sw + col * (kG7Warps * 16);
+        if constexpr (FUSED) {
+            const float4 v0 = xv[2 * col], v1 = xv[2 * col + 1];
+            const uint32_t xb[8] = {__float_as_uint(v0.x), __float_as_uint(v0.y), __float_as_uint(v0.z),
+                                    __float_as_uint(v0.w), __float_as_uint(v1.x), __float_as_uint(v1.y),
+                                    __float_as_uint(v1.z), __float_as_uint(v1.w)};
+            uint2 cd;
+            int usum;  // the sum of the 16-element unit of this lane pair
+            quantize8<32>(xb, cd, usum, scale);
+            *reinterpret_cast<uint2 *>(ac + 8 * lane) = cd;
+            const int s2 = usum + __shfl_down_sync(0xFFFFFFFFu, usum, 2);
+            if ((lane & 3) == 0) Sc[lane >> 2] = (int16_t)s2;
+        } else {
+            const uint2 cd = *reinterpret_cast<const uint2 *>(p.codes + (int64_t)col * kG7K + 256 * w + 8 * lane);
+            *reinterpret_cast<uint2 *>(ac + 8 * lane) = cd;
+            const int us = lane < 16 ? (int)p.sums16[(int64_t)col * (kG7K / 16) + 16 * w + lane] : 0;
+            const int s2 = us + __shfl_down_sync(0xFFFFFFFFu, us, 1);
+            if (lane < 16 && (lane & 1) == 0) Sc[lane >> 1] = (int16_t)s2;
+            scale = reinterpret_cast<const uint32_t *>(p.scales)[col * kG7Warps + w];
+        }
+        if (lane == 0) sclw[col * kG7Warps] = scale;
+    }
+    __syncwarp();
+    uint32_t sv[NC];
+#pragma unroll
+    for (int cc = 0; cc < NC; ++cc) sv[cc] = sclw[cc * kG7Warps];
+
+    // ---- the tiles
+    for (int t = 0; t < ntiles; ++t) {
+        const int slot = t % kG7RSlots;
+        const int n = min(kG7RTile, count - t * kG7RTile);
+        const bool ok = mbar_wait_bounded(bars + slot, (uint32_t)((t / kG7RSlots) & 1), p.fault);
+        // also: the previous tile's fold has read every value
+        if (!__syncthreads_and(ok)) return;  // a tile never completed: fault word raised
+        if (lane < n) {
+            const uint8_t *row = slab + slot * (kG7RTile * p.pitch) + lane * p.pitch;
+            int C[NC], O[NC];
+            uint32_t dd;
+            block_q4k_cols<NC>(row + 144 * w, aw, kG7K, Sw, kG7Warps * 16, C, O, dd);
+#pragma unroll
+            for (int cc = 0; cc < NC; ++cc)
+                vals[lane * VS + cc * 17 + w] = lane_value_fast<1>(C[cc] >> 4, O[cc], dd & 0xFFFFu, dd >> 16,
+                                                                   (int)(sv[cc] & 0xFFu), (int)(int16_t)(sv[cc] >> 16));
+        }
+        __syncthreads();  // every warp is done with the slot; the tile's values are complete
+        if (w == 0 && t + kG7RSlots < ntiles) {
+            fence_proxy_async_smem();  // the reads above before the copies into the slot
+            fill(t + kG7RSlots);
+        }
+        // ---- fold: thread (r, col) of the last warps adds row r's 16 block
+        // values of that column in block order from +0
+        const int f = tid - (kG7Warps * 32 - kG7RTile * NC);
+        if (f >= 0 && f < n * NC) {
+            const int r = f / NC, col = f - r * NC;
+            const float *vr = vals + r * VS + col * 17;
+            float acc = 0.0f;
+#pragma unroll
+            for (int b = 0; b < kG7Warps; ++b) acc = fadd_ftz(acc, vr[b]);
+            if (acc != acc) acc = __uint_as_float(kEngineNaN);
+            *out_ptr(p.mt, col, row0 + (int64_t)t * kG7RTile + r) = acc;
+        }
+    }
+}
+
+// NC columns (2..4) of a Q4_K-like matrix (or a table of them) at K = 4096,
+// more than kG7MaxRows rows a CTA.  QB_E_ARG when the shape does not fit.
+template <int NC>
+int launch_gemv7r(const GemvArgs &a, cudaStream_t stream, const float *x) {
+    if (a.ncols != NC || a.mode != 0 || a.K != kG7K) return QB_E_ARG;
+    Gemv7K k;
+    k.mt = a.mats ? *a.mats : single_table(a.W, a.rows, a.out);
+    k.rows = k.mt.start[k.mt.n];
+    if (k.rows < 1) return QB_E_ARG;
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(num_sms(), k.rows));
+    const int64_t per_cta = (k.rows + grid - 1) / grid;
+    if (per_cta <= kG7MaxRows) return QB_E_ARG;
+    k.rec = (int)record_bytes(kQ4K, kG7K);
+    k.pitch = k.rec + 16;
+    const int smem = gemv7r_layout(NC, k.pitch).total;
+    if (smem > 227 * 1024) return QB_E_ARG;
+    k.base = k.rows / grid;
+    k.rem = k.rows % grid;
+    k.codes = a.codes;
+    k.scales = a.scales;
+    k.sums16 = a.sums16;
+    k.x = x;
+    k.fault = fault_word();
+    if (!k.fault) return QB_E_CUDA;
+    auto kern = x ? gemv7r_kernel<true, NC> : gemv7r_kernel<false, NC>;
+    if (ensure_smem_limit(reinterpret_cast<const void *>(kern), smem) != QB_OK) return QB_E_CUDA;
+    return launch_pdl(kern, dim3(grid), dim3(kG7Warps * 32), (size_t)smem, stream, k);
+}
+
 // 2..4 columns at K = 4096 (the multi-column form above); QB_E_ARG where it
 // does not apply.
 template <int F>
 int launch_gemv7_cols(const GemvArgs &a, cudaStream_t stream, const float *x) {
     constexpr int U = F == kQ4K ? 2 : 4;
+    int r = QB_E_ARG;
     switch (a.ncols) {
-    case 2: return launch_gemv7m<F, 2, U, 2>(a, stream, x);
-    case 3: return launch_gemv7m<F, 2, U, 3>(a, stream, x);
-    case 4: return launch_gemv7m<F, 2, U, 4>(a, stream, x);
+    case 2: r = launch_gemv7m<F, 2, U, 2>(a, stream, x); break;
+    case 3: r = launch_gemv7m<F, 2, U, 3>(a, stream, x); break;
+    case 4: r = launch_gemv7m<F, 2, U, 4>(a, stream, x); break;
     default: return QB_E_ARG;
+    }
+    if (r != QB_E_ARG || F != kQ4K) return r;
+    switch (a.ncols) {  // more rows a CTA: the ring form
+    case 2: return launch_gemv7r<2>(a, stream, x);
+    case 3: return launch_gemv7r<3>(a, stream, x);
+    default: return launch_gemv7r<4>(a, stream, x);
     }
 }
 

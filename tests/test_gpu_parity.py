@@ -559,6 +559,43 @@ def test_k4096_row_ranges(fmt, ncols, rows):
     assert np.array_equal(bits(host(out)), bits(want))
 
 
+@pytest.mark.parametrize("ncols", [2, 3, 4])
+@pytest.mark.parametrize("rows", [152 * 65, 152 * 189 + 17, 152 * 96 - 5])
+def test_k4096_many_rows_ring(ncols, rows):
+    """2..4 columns at K = 4096 past 64 rows a CTA: rows streaming through
+    the two-slot ring of 32-row tiles (full tiles, a ragged last one, CTAs
+    with one row more than others), from codes and from x; and the same
+    rows as a table of three matrices sharing the activation."""
+    import torch
+    fmt, K = synth.FMT_Q4K, 4096
+    rng = np.random.default_rng(rows + ncols)
+    lg = synth.draw(fmt, rng, rows, K)
+    W = synth.pack(fmt, lg)
+    x = synth.draw_act(rng, ncols, K, outlier_frac=0.001)
+    codes, m, e, s16, packed = oracle_act(x, 256)
+    want = oracle.gemv(fmt, W, rows, K, codes, m, e)
+    act = gpu_quantize(x, 256)
+    out = torch.full((ncols, rows), float("nan"), dtype=torch.float32, device="cuda")
+    qb.q_gemv(fmt, dev(W), rows, K, act, ncols, out)
+    torch.cuda.synchronize()
+    assert np.array_equal(bits(host(out)), bits(want))
+    out.fill_(float("nan"))
+    ws = torch.empty(qb.q_matvec_workspace_bytes(fmt, K, ncols), dtype=torch.uint8, device="cuda")
+    qb.q_matvec(fmt, dev(W), rows, K, dev(x), out, workspace=ws)
+    torch.cuda.synchronize()
+    assert np.array_equal(bits(host(out)), bits(want))
+    # three matrices: the first rows, a middle part, the last 7 rows
+    cut = [0, rows // 2 + 3, rows - 7, rows]
+    Wr = W.reshape(rows, -1)
+    parts = [np.ascontiguousarray(Wr[cut[i]:cut[i + 1]]) for i in range(3)]
+    outs = [torch.full((ncols, cut[i + 1] - cut[i]), float("nan"), dtype=torch.float32, device="cuda")
+            for i in range(3)]
+    qb.q_gemv_many(fmt, [dev(P) for P in parts], [cut[i + 1] - cut[i] for i in range(3)], K, act, ncols, outs)
+    torch.cuda.synchronize()
+    for i in range(3):
+        assert np.array_equal(bits(host(outs[i])), bits(want[:, cut[i]:cut[i + 1]])), i
+
+
 @pytest.mark.parametrize("ncols", [1, 2, 3, 4])
 @pytest.mark.parametrize("rows,K", [(300, 4096), (152 * 64 + 1, 4096), (200, 14336)])
 def test_scale_exponent_gaps(ncols, rows, K):
