@@ -93,7 +93,7 @@ __device__ __forceinline__ void block_q4k(const uint8_t *blk, const uint8_t *a, 
 
 // block_q4k for NC activation columns (codes at a + c*stride, sums at
 // S + c*sstride): the weights read and unpacked once for all of them.
-template <int NC>
+template <int NC, int UNR = 2>
 __device__ __forceinline__ void block_q4k_cols(const uint8_t *blk, const uint8_t *a, int stride, const int16_t *S,
                                                int sstride, int (&C)[NC], int (&O)[NC], uint32_t &dd) {
     const uint4 meta = *reinterpret_cast<const uint4 *>(blk);
@@ -102,7 +102,7 @@ __device__ __forceinline__ void block_q4k_cols(const uint8_t *blk, const uint8_t
     const unsigned long long mn48 = (unsigned long long)(meta.z >> 16) | ((unsigned long long)meta.w << 16);
 #pragma unroll
     for (int c = 0; c < NC; ++c) C[c] = 0;
-#pragma unroll 2
+#pragma unroll UNR
     for (int s = 0; s < 8; ++s) {
         const uint4 w = *reinterpret_cast<const uint4 *>(blk + 16 + 16 * s);
         const uint32_t l0 = w.x & 0x0F0F0F0Fu, l1 = w.y & 0x0F0F0F0Fu, l2 = w.z & 0x0F0F0F0Fu, l3 = w.w & 0x0F0F0F0Fu;
@@ -552,70 +552,117 @@ int launch_gemv7m(const GemvArgs &a, cudaStream_t stream, const float *x) {
 
 // ---------------------------------------------------------------- many rows, 2..4 columns
 // The multi-column form over more rows than one slab holds (Q4_K-like): the
-// CTA's rows stream through a ring of two 32-row tiles.  As above, warp w
-// forms block w of every row of a tile (a lane a row) for every column with
-// the weights unpacked once; after each tile four warps fold its rows while
-// the tile two ahead is being fetched into the slot it leaves.
+// CTA's rows stream through a ring of two 32-row tiles.  As above, warps
+// 0..15 (compute) form block w of every row of a tile (a lane a row) for every
+// column with the weights unpacked once.  A 17th warp (producer) issues each
+// tile's row copies and folds each computed tile, so that neither the copy
+// issue (which stalls while the copy engine is busy) nor the fold delays the
+// arithmetic; the roles hand over through mbarriers only:
+//   full[s]   the copies of the tile in slot s have landed (transaction count)
+//   done[b]   the 16 compute warps have read the tile in slot b and written its
+//             block values into value buffer b
+//   vfree[b]  the producer has folded value buffer b (it may be rewritten)
+// Tile t uses slot and buffer t & 1; each barrier completes once per tile that
+// uses it, so tile t waits for phase (t >> 1) & 1.
 constexpr int kG7RTile = 32;   // rows a tile (a lane a row)
-constexpr int kG7RSlots = 2;   // tiles in flight
+constexpr int kG7RSlots = 2;   // tiles in flight (and value buffers)
+constexpr int kG7RThreads = (kG7Warps + 1) * 32;
+constexpr int kG7RUnr = 2;     // sub-blocks unrolled (the register budget of one CTA a SM)
 
 struct Gemv7RSmem {
     int scl, act, sums, vals, slab, total;
 };
 __host__ __device__ inline Gemv7RSmem gemv7r_layout(int nc, int pitch) {
     Gemv7RSmem s;
-    s.scl = 128;  // the slots' mbarriers at 0
+    s.scl = 128;  // 3 * kG7RSlots mbarriers at 0
     s.act = s.scl + ((nc * kG7Warps * 4 + 127) & ~127);
     s.sums = s.act + nc * kG7K;
     s.vals = s.sums + nc * kG7Warps * 32;
-    s.slab = s.vals + ((kG7RTile * gemv7m_vs(nc) * 4 + 127) & ~127);
+    s.slab = s.vals + kG7RSlots * ((kG7RTile * gemv7m_vs(nc) * 4 + 127) & ~127);
     s.total = s.slab + kG7RSlots * kG7RTile * pitch;
     return s;
 }
 
 template <bool FUSED, int NC>
-__global__ void __launch_bounds__(kG7Warps * 32, 1) gemv7r_kernel(const Gemv7K p) {
+__global__ void __launch_bounds__(kG7RThreads, 1) gemv7r_kernel(const Gemv7K p) {
     extern __shared__ __align__(128) uint8_t smem[];
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
     const Gemv7RSmem Lo = gemv7r_layout(NC, p.pitch);
     constexpr int VS = gemv7m_vs(NC);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem);
-    uint32_t *sclw = reinterpret_cast<uint32_t *>(smem + Lo.scl) + w;  // column c at + c * 16
-    uint8_t *aw = smem + Lo.act + 256 * w;                             // column c at + c * K
-    int16_t *Sw = reinterpret_cast<int16_t *>(smem + Lo.sums + 32 * w);  // column c at + c * 256
-    float *vals = reinterpret_cast<float *>(smem + Lo.vals);
+    constexpr int kVBuf = (kG7RTile * VS * 4 + 127) & ~127;  // bytes a value buffer
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem);
+    uint64_t *done = full + kG7RSlots;
+    uint64_t *vfree = done + kG7RSlots;
     uint8_t *slab = smem + Lo.slab;
 
     const int64_t c = blockIdx.x;
     const int64_t row0 = c * p.base + (c < p.rem ? c : p.rem);
     const int count = (int)(p.base + (c < p.rem ? 1 : 0));
     const int ntiles = (count + kG7RTile - 1) / kG7RTile;
-    // tile t into slot t % kG7RSlots, a copy a row by the lanes of warp 0
-    auto fill = [&](int t) {
-        const int n = min(kG7RTile, count - t * kG7RTile);
-        uint64_t *bar = bars + t % kG7RSlots;
-        if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)(n * p.rec));
-        __syncwarp();
-        uint8_t *dst = slab + (t % kG7RSlots) * (kG7RTile * p.pitch);
-        if (lane < n)
-            bulk_g2s(dst + lane * p.pitch, row_ptr(p.mt, row0 + (int64_t)t * kG7RTile + lane, p.rec),
-                     (uint32_t)p.rec, bar);
-    };
 
     if (tid == 0) {
-        for (int s = 0; s < kG7RSlots; ++s) mbar_init(bars + s, 1);
+        for (int s = 0; s < kG7RSlots; ++s) {
+            mbar_init(full + s, 1);
+            mbar_init(done + s, kG7Warps);
+            mbar_init(vfree + s, 1);
+        }
         fence_mbar_init();
     }
-    __syncthreads();
-    // the first tiles (weights depend on no earlier kernel)
-    if (w == 0)
+    __syncthreads();  // the last CTA-wide barrier: the roles part here
+
+    if (w == kG7Warps) {
+        // ---- producer: tile t into slot t & 1, a copy a row by the lanes
+        auto fill = [&](int t) {
+            const int n = min(kG7RTile, count - t * kG7RTile);
+            uint64_t *bar = full + (t & 1);
+            if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)(n * p.rec));
+            __syncwarp();
+            uint8_t *dst = slab + (t & 1) * (kG7RTile * p.pitch);
+            if (lane < n)
+                bulk_g2s(dst + lane * p.pitch, row_ptr(p.mt, row0 + (int64_t)t * kG7RTile + lane, p.rec),
+                         (uint32_t)p.rec, bar);
+        };
+        // the first tiles (weights depend on no earlier kernel)
         for (int t = 0; t < kG7RSlots && t < ntiles; ++t) fill(t);
-    // the next launch may be scheduled now: it reads nothing this one writes
-    // before its own pdl_wait, which returns once this grid has finished
+        pdl_launch_dependents();
+        pdl_wait();  // the outputs this warp writes: after the previous kernel
+        for (int t = 0; t < ntiles; ++t) {
+            const int b = t & 1;
+            if (!mbar_wait_bounded(done + b, (uint32_t)((t >> 1) & 1), p.fault)) return;
+            if (t + kG7RSlots < ntiles) {
+                fence_proxy_async_smem();  // the compute warps' reads of the slot before the copies into it
+                fill(t + kG7RSlots);
+            }
+            // fold tile t: line (r, col) adds row r's 16 block values of that
+            // column in block order from +0, four lines a lane at once
+            const float *vb = reinterpret_cast<const float *>(smem + Lo.vals + b * kVBuf);
+            const int n = min(kG7RTile, count - t * kG7RTile);
+#pragma unroll
+            for (int q = 0; q < (kG7RTile * NC) / 32; ++q) {
+                const int f = lane + 32 * q;
+                const int r = f / NC, col = f - r * NC;
+                if (r < n) {
+                    const float *vr = vb + r * VS + col * 17;
+                    float acc = 0.0f;
+#pragma unroll
+                    for (int k = 0; k < kG7Warps; ++k) acc = fadd_ftz(acc, vr[k]);
+                    if (acc != acc) acc = __uint_as_float(kEngineNaN);
+                    *out_ptr(p.mt, col, row0 + (int64_t)t * kG7RTile + r) = acc;
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(vfree + b);
+        }
+        return;
+    }
+
+    // ---- compute warps
+    uint32_t *sclw = reinterpret_cast<uint32_t *>(smem + Lo.scl) + w;  // column c at + c * 16
+    uint8_t *aw = smem + Lo.act + 256 * w;                             // column c at + c * K
+    int16_t *Sw = reinterpret_cast<int16_t *>(smem + Lo.sums + 32 * w);  // column c at + c * 256
     pdl_launch_dependents();
     pdl_wait();
-
-    // ---- block w of the activation, each column (as in gemv7m_kernel)
+    // block w of the activation, each column (as in gemv7m_kernel)
     float4 xv[FUSED ? 2 * NC : 1];
     if constexpr (FUSED) {
 #pragma unroll
@@ -656,40 +703,25 @@ __global__ void __launch_bounds__(kG7Warps * 32, 1) gemv7r_kernel(const Gemv7K p
 #pragma unroll
     for (int cc = 0; cc < NC; ++cc) sv[cc] = sclw[cc * kG7Warps];
 
-    // ---- the tiles
     for (int t = 0; t < ntiles; ++t) {
-        const int slot = t % kG7RSlots;
+        const int b = t & 1;
+        const uint32_t ph = (uint32_t)((t >> 1) & 1);
+        if (!mbar_wait_bounded(full + b, ph, p.fault)) return;                          // the tile landed
+        if (t >= kG7RSlots && !mbar_wait_bounded(vfree + b, ph ^ 1u, p.fault)) return;  // tile t-2 folded
         const int n = min(kG7RTile, count - t * kG7RTile);
-        const bool ok = mbar_wait_bounded(bars + slot, (uint32_t)((t / kG7RSlots) & 1), p.fault);
-        // also: the previous tile's fold has read every value
-        if (!__syncthreads_and(ok)) return;  // a tile never completed: fault word raised
+        float *vb = reinterpret_cast<float *>(smem + Lo.vals + b * kVBuf);
         if (lane < n) {
-            const uint8_t *row = slab + slot * (kG7RTile * p.pitch) + lane * p.pitch;
+            const uint8_t *row = slab + b * (kG7RTile * p.pitch) + lane * p.pitch;
             int C[NC], O[NC];
             uint32_t dd;
-            block_q4k_cols<NC>(row + 144 * w, aw, kG7K, Sw, kG7Warps * 16, C, O, dd);
+            block_q4k_cols<NC, kG7RUnr>(row + 144 * w, aw, kG7K, Sw, kG7Warps * 16, C, O, dd);
 #pragma unroll
             for (int cc = 0; cc < NC; ++cc)
-                vals[lane * VS + cc * 17 + w] = lane_value_fast<1>(C[cc] >> 4, O[cc], dd & 0xFFFFu, dd >> 16,
-                                                                   (int)(sv[cc] & 0xFFu), (int)(int16_t)(sv[cc] >> 16));
+                vb[lane * VS + cc * 17 + w] = lane_value_fast<1>(C[cc] >> 4, O[cc], dd & 0xFFFFu, dd >> 16,
+                                                                 (int)(sv[cc] & 0xFFu), (int)(int16_t)(sv[cc] >> 16));
         }
-        __syncthreads();  // every warp is done with the slot; the tile's values are complete
-        if (w == 0 && t + kG7RSlots < ntiles) {
-            fence_proxy_async_smem();  // the reads above before the copies into the slot
-            fill(t + kG7RSlots);
-        }
-        // ---- fold: thread (r, col) of the last warps adds row r's 16 block
-        // values of that column in block order from +0
-        const int f = tid - (kG7Warps * 32 - kG7RTile * NC);
-        if (f >= 0 && f < n * NC) {
-            const int r = f / NC, col = f - r * NC;
-            const float *vr = vals + r * VS + col * 17;
-            float acc = 0.0f;
-#pragma unroll
-            for (int b = 0; b < kG7Warps; ++b) acc = fadd_ftz(acc, vr[b]);
-            if (acc != acc) acc = __uint_as_float(kEngineNaN);
-            *out_ptr(p.mt, col, row0 + (int64_t)t * kG7RTile + r) = acc;
-        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(done + b);
     }
 }
 
@@ -719,7 +751,7 @@ int launch_gemv7r(const GemvArgs &a, cudaStream_t stream, const float *x) {
     if (!k.fault) return QB_E_CUDA;
     auto kern = x ? gemv7r_kernel<true, NC> : gemv7r_kernel<false, NC>;
     if (ensure_smem_limit(reinterpret_cast<const void *>(kern), smem) != QB_OK) return QB_E_CUDA;
-    return launch_pdl(kern, dim3(grid), dim3(kG7Warps * 32), (size_t)smem, stream, k);
+    return launch_pdl(kern, dim3(grid), dim3(kG7RThreads), (size_t)smem, stream, k);
 }
 
 // 2..4 columns at K = 4096 (the multi-column form above); QB_E_ARG where it

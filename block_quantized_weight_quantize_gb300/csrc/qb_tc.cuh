@@ -361,9 +361,6 @@ __device__ __forceinline__ bool elect_one() {
         : "=r"(e));
     return e != 0;
 }
-__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
-    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
 
 // Roles: warps 0-7 decode weights into tensor memory (two threads a row),
 // warps 8-15 combine and send block values (two threads a row, eight columns
