@@ -550,196 +550,217 @@ int launch_gemv7m(const GemvArgs &a, cudaStream_t stream, const float *x) {
     return launch_pdl(kern, dim3(grid), dim3(kG7Warps * 32), (size_t)smem, stream, k);
 }
 
-// ---------------------------------------------------------------- many rows, 2..4 columns
-// The multi-column form over more rows than one slab holds (Q4_K-like): the
-// CTA's rows stream through a ring of two 32-row tiles.  As above, warps
-// 0..15 (compute) form block w of every row of a tile (a lane a row) for every
-// column with the weights unpacked once.  A 17th warp (producer) issues each
-// tile's row copies and folds each computed tile, so that neither the copy
-// issue (which stalls while the copy engine is busy) nor the fold delays the
-// arithmetic; the roles hand over through mbarriers only:
+// ---------------------------------------------------------------- ring form
+// Q4_K-like, 2..4 columns, more rows than one slab holds or a longer K: the
+// CTA's rows stream through a ring of two tiles, a tile being 32 rows by one
+// chunk of NW blocks (K = 256 * NW * chunks; chunks of a row tile in order).
+// Compute warps 0..NW-1 form block k*NW + w of every row of the tile in chunk
+// k (a lane a row) for every column, the weights unpacked once.  A producer
+// warp issues each tile's row copies and folds each computed tile into its
+// rows' running sums (block order: the chunks in order, blocks in order within
+// each), so that neither the copy issue (which stalls while the copy engine is
+// busy) nor the fold delays the arithmetic.  The roles hand over through
+// mbarriers only:
 //   full[s]   the copies of the tile in slot s have landed (transaction count)
-//   done[b]   the 16 compute warps have read the tile in slot b and written its
+//   done[b]   the compute warps have read the tile in slot b and written its
 //             block values into value buffer b
 //   vfree[b]  the producer has folded value buffer b (it may be rewritten)
-// Tile t uses slot and buffer t & 1; each barrier completes once per tile that
-// uses it, so tile t waits for phase (t >> 1) & 1.
+// Tile t (row tile t / chunks, chunk t % chunks) uses slot and buffer t & 1;
+// each barrier completes once per tile that uses it, so tile t waits for phase
+// (t >> 1) & 1.
 constexpr int kG7RTile = 32;   // rows a tile (a lane a row)
-constexpr int kG7RSlots = 2;   // tiles in flight (and value buffers)
-constexpr int kG7RThreads = (kG7Warps + 1) * 32;
 constexpr int kG7RUnr = 2;     // sub-blocks unrolled (the register budget of one CTA a SM)
 
 struct Gemv7RSmem {
-    int scl, act, sums, vals, slab, total;
+    int scl, act, sums, vals, slab, vbuf, total;
 };
-__host__ __device__ inline Gemv7RSmem gemv7r_layout(int nc, int pitch) {
+// nc columns, K, nw blocks a chunk, pitch: bytes a row of a tile in shared memory
+__host__ __device__ inline Gemv7RSmem gemv7r_layout(int nc, int K, int nw, int pitch) {
+    const int nb = K / 256;
     Gemv7RSmem s;
-    s.scl = 128;  // 3 * kG7RSlots mbarriers at 0
-    s.act = s.scl + ((nc * kG7Warps * 4 + 127) & ~127);
-    s.sums = s.act + nc * kG7K;
-    s.vals = s.sums + nc * kG7Warps * 32;
-    s.slab = s.vals + kG7RSlots * ((kG7RTile * gemv7m_vs(nc) * 4 + 127) & ~127);
-    s.total = s.slab + kG7RSlots * kG7RTile * pitch;
+    s.scl = 128;  // 6 mbarriers at 0
+    s.act = s.scl + ((nc * nb * 4 + 127) & ~127);
+    s.sums = s.act + nc * K;
+    s.vals = s.sums + ((nc * nb * 32 + 127) & ~127);
+    s.vbuf = (kG7RTile * ((nc * (nw + 1)) | 1) * 4 + 127) & ~127;
+    s.slab = s.vals + 2 * s.vbuf;
+    s.total = s.slab + 2 * kG7RTile * pitch;
     return s;
 }
 
-template <bool FUSED, int NC>
-__global__ void __launch_bounds__(kG7RThreads, 1) gemv7r_kernel(const Gemv7K p) {
+template <bool FUSED, int NC, int NW, int NCH>
+__global__ void __launch_bounds__((NW + 1) * 32, 1) gemv7r_kernel(const Gemv7K p, int pitch) {
     extern __shared__ __align__(128) uint8_t smem[];
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-    const Gemv7RSmem Lo = gemv7r_layout(NC, p.pitch);
-    constexpr int VS = gemv7m_vs(NC);
-    constexpr int kVBuf = (kG7RTile * VS * 4 + 127) & ~127;  // bytes a value buffer
+    constexpr int nch = NCH, nb = NW * NCH, K = 256 * nb;  // chunks, blocks and elements a row
+    const int cbytes = NW * 144;               // bytes of a row's chunk
+    const Gemv7RSmem Lo = gemv7r_layout(NC, K, NW, pitch);
+    constexpr int VS = (NC * (NW + 1)) | 1;    // floats a row of a value buffer (odd: rows in distinct banks)
     uint64_t *full = reinterpret_cast<uint64_t *>(smem);
-    uint64_t *done = full + kG7RSlots;
-    uint64_t *vfree = done + kG7RSlots;
+    uint64_t *done = full + 2;
+    uint64_t *vfree = done + 2;
+    uint32_t *scl = reinterpret_cast<uint32_t *>(smem + Lo.scl);  // [col][block]
+    uint8_t *act = smem + Lo.act;                                              // [col][K]
+    int16_t *sums = reinterpret_cast<int16_t *>(smem + Lo.sums);               // [col][block][16]
     uint8_t *slab = smem + Lo.slab;
 
     const int64_t c = blockIdx.x;
     const int64_t row0 = c * p.base + (c < p.rem ? c : p.rem);
     const int count = (int)(p.base + (c < p.rem ? 1 : 0));
-    const int ntiles = (count + kG7RTile - 1) / kG7RTile;
+    const int ntiles = ((count + kG7RTile - 1) / kG7RTile) * nch;
 
     if (tid == 0) {
-        for (int s = 0; s < kG7RSlots; ++s) {
+        for (int s = 0; s < 2; ++s) {
             mbar_init(full + s, 1);
-            mbar_init(done + s, kG7Warps);
+            mbar_init(done + s, NW);
             mbar_init(vfree + s, 1);
         }
         fence_mbar_init();
     }
     __syncthreads();  // the last CTA-wide barrier: the roles part here
 
-    if (w == kG7Warps) {
+    if (w == NW) {
         // ---- producer: tile t into slot t & 1, a copy a row by the lanes
         auto fill = [&](int t) {
-            const int n = min(kG7RTile, count - t * kG7RTile);
+            const int rt = t / nch, k = t - rt * nch;
+            const int n = min(kG7RTile, count - rt * kG7RTile);
             uint64_t *bar = full + (t & 1);
-            if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)(n * p.rec));
+            if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)(n * cbytes));
             __syncwarp();
-            uint8_t *dst = slab + (t & 1) * (kG7RTile * p.pitch);
+            uint8_t *dst = slab + (t & 1) * (kG7RTile * pitch);
             if (lane < n)
-                bulk_g2s(dst + lane * p.pitch, row_ptr(p.mt, row0 + (int64_t)t * kG7RTile + lane, p.rec),
-                         (uint32_t)p.rec, bar);
+                bulk_g2s(dst + lane * pitch,
+                         row_ptr(p.mt, row0 + (int64_t)rt * kG7RTile + lane, p.rec) + (int64_t)k * cbytes,
+                         (uint32_t)cbytes, bar);
         };
         // the first tiles (weights depend on no earlier kernel)
-        for (int t = 0; t < kG7RSlots && t < ntiles; ++t) fill(t);
+        for (int t = 0; t < 2 && t < ntiles; ++t) fill(t);
         pdl_launch_dependents();
         pdl_wait();  // the outputs this warp writes: after the previous kernel
+        float acc[NC];  // lane = row of the row tile: its running sums
+#pragma unroll
+        for (int cc = 0; cc < NC; ++cc) acc[cc] = 0.0f;
         for (int t = 0; t < ntiles; ++t) {
             const int b = t & 1;
             if (!mbar_wait_bounded(done + b, (uint32_t)((t >> 1) & 1), p.fault)) return;
-            if (t + kG7RSlots < ntiles) {
+            if (t + 2 < ntiles) {
                 fence_proxy_async_smem();  // the compute warps' reads of the slot before the copies into it
-                fill(t + kG7RSlots);
+                fill(t + 2);
             }
-            // fold tile t: line (r, col) adds row r's 16 block values of that
-            // column in block order from +0, four lines a lane at once
-            const float *vb = reinterpret_cast<const float *>(smem + Lo.vals + b * kVBuf);
-            const int n = min(kG7RTile, count - t * kG7RTile);
+            // fold chunk k of row tile rt: block values in block order
+            const int rt = t / nch, k = t - rt * nch;
+            const int n = min(kG7RTile, count - rt * kG7RTile);
+            const float *vr = reinterpret_cast<const float *>(smem + Lo.vals + b * Lo.vbuf) + lane * VS;
 #pragma unroll
-            for (int q = 0; q < (kG7RTile * NC) / 32; ++q) {
-                const int f = lane + 32 * q;
-                const int r = f / NC, col = f - r * NC;
-                if (r < n) {
-                    const float *vr = vb + r * VS + col * 17;
-                    float acc = 0.0f;
+            for (int cc = 0; cc < NC; ++cc)
 #pragma unroll
-                    for (int k = 0; k < kG7Warps; ++k) acc = fadd_ftz(acc, vr[k]);
-                    if (acc != acc) acc = __uint_as_float(kEngineNaN);
-                    *out_ptr(p.mt, col, row0 + (int64_t)t * kG7RTile + r) = acc;
-                }
-            }
+                for (int q = 0; q < NW; ++q) acc[cc] = fadd_ftz(acc[cc], vr[cc * (NW + 1) + q]);
             __syncwarp();
             if (lane == 0) mbar_arrive(vfree + b);
+            if (k == nch - 1) {
+                if (lane < n)
+#pragma unroll
+                    for (int cc = 0; cc < NC; ++cc) {
+                        const float v = acc[cc] != acc[cc] ? __uint_as_float(kEngineNaN) : acc[cc];
+                        *out_ptr(p.mt, cc, row0 + (int64_t)rt * kG7RTile + lane) = v;
+                    }
+#pragma unroll
+                for (int cc = 0; cc < NC; ++cc) acc[cc] = 0.0f;
+            }
         }
         return;
     }
 
     // ---- compute warps
-    uint32_t *sclw = reinterpret_cast<uint32_t *>(smem + Lo.scl) + w;  // column c at + c * 16
-    uint8_t *aw = smem + Lo.act + 256 * w;                             // column c at + c * K
-    int16_t *Sw = reinterpret_cast<int16_t *>(smem + Lo.sums + 32 * w);  // column c at + c * 256
     pdl_launch_dependents();
     pdl_wait();
-    // block w of the activation, each column (as in gemv7m_kernel)
-    float4 xv[FUSED ? 2 * NC : 1];
-    if constexpr (FUSED) {
+    // blocks w, NW + w, 2*NW + w, ... of the activation, each column: codes
+    // (natural order), the per-32 sums and the block's scale
+    for (int k = 0; k < nch; ++k) {
+        const int blk = k * NW + w;
+        float4 xv[FUSED ? 2 * NC : 1];
+        if constexpr (FUSED) {  // every column's elements requested first
+#pragma unroll
+            for (int col = 0; col < NC; ++col) {
+                const float4 *xp = reinterpret_cast<const float4 *>(p.x + (int64_t)col * K + 256 * blk + 8 * lane);
+                xv[2 * col] = ldg_f4_ordered(xp);
+                xv[2 * col + 1] = ldg_f4_ordered(xp + 1);
+            }
+        }
 #pragma unroll
         for (int col = 0; col < NC; ++col) {
-            const float4 *xp = reinterpret_cast<const float4 *>(p.x + (int64_t)col * kG7K + 256 * w + 8 * lane);
-            xv[2 * col] = ldg_f4_ordered(xp);
-            xv[2 * col + 1] = ldg_f4_ordered(xp + 1);
+            uint32_t scale;
+            uint8_t *ac = act + col * K + 256 * blk;
+            int16_t *Sc = sums + (col * nb + blk) * 16;
+            if constexpr (FUSED) {
+                const float4 v0 = xv[2 * col], v1 = xv[2 * col + 1];
+                const uint32_t xb[8] = {__float_as_uint(v0.x), __float_as_uint(v0.y), __float_as_uint(v0.z),
+                                        __float_as_uint(v0.w), __float_as_uint(v1.x), __float_as_uint(v1.y),
+                                        __float_as_uint(v1.z), __float_as_uint(v1.w)};
+                uint2 cd;
+                int usum;  // the sum of the 16-element unit of this lane pair
+                quantize8<32>(xb, cd, usum, scale);
+                *reinterpret_cast<uint2 *>(ac + 8 * lane) = cd;
+                const int s2 = usum + __shfl_down_sync(0xFFFFFFFFu, usum, 2);
+                if ((lane & 3) == 0) Sc[lane >> 2] = (int16_t)s2;
+            } else {
+                const uint2 cd = *reinterpret_cast<const uint2 *>(p.codes + (int64_t)col * K + 256 * blk + 8 * lane);
+                *reinterpret_cast<uint2 *>(ac + 8 * lane) = cd;
+                const int us = lane < 16 ? (int)p.sums16[(int64_t)col * (K / 16) + 16 * blk + lane] : 0;
+                const int s2 = us + __shfl_down_sync(0xFFFFFFFFu, us, 1);
+                if (lane < 16 && (lane & 1) == 0) Sc[lane >> 1] = (int16_t)s2;
+                scale = reinterpret_cast<const uint32_t *>(p.scales)[(int64_t)col * nb + blk];
+            }
+            if (lane == 0) scl[col * nb + blk] = scale;
         }
-    }
-#pragma unroll
-    for (int col = 0; col < NC; ++col) {
-        uint32_t scale;
-        uint8_t *ac = aw + col * kG7K;
-        int16_t *Sc = Sw + col * (kG7Warps * 16);
-        if constexpr (FUSED) {
-            const float4 v0 = xv[2 * col], v1 = xv[2 * col + 1];
-            const uint32_t xb[8] = {__float_as_uint(v0.x), __float_as_uint(v0.y), __float_as_uint(v0.z),
-                                    __float_as_uint(v0.w), __float_as_uint(v1.x), __float_as_uint(v1.y),
-                                    __float_as_uint(v1.z), __float_as_uint(v1.w)};
-            uint2 cd;
-            int usum;  // the sum of the 16-element unit of this lane pair
-            quantize8<32>(xb, cd, usum, scale);
-            *reinterpret_cast<uint2 *>(ac + 8 * lane) = cd;
-            const int s2 = usum + __shfl_down_sync(0xFFFFFFFFu, usum, 2);
-            if ((lane & 3) == 0) Sc[lane >> 2] = (int16_t)s2;
-        } else {
-            const uint2 cd = *reinterpret_cast<const uint2 *>(p.codes + (int64_t)col * kG7K + 256 * w + 8 * lane);
-            *reinterpret_cast<uint2 *>(ac + 8 * lane) = cd;
-            const int us = lane < 16 ? (int)p.sums16[(int64_t)col * (kG7K / 16) + 16 * w + lane] : 0;
-            const int s2 = us + __shfl_down_sync(0xFFFFFFFFu, us, 1);
-            if (lane < 16 && (lane & 1) == 0) Sc[lane >> 1] = (int16_t)s2;
-            scale = reinterpret_cast<const uint32_t *>(p.scales)[col * kG7Warps + w];
-        }
-        if (lane == 0) sclw[col * kG7Warps] = scale;
     }
     __syncwarp();
-    uint32_t sv[NC];
+    uint32_t sv1[NC];  // one chunk: the scales of my block held in registers
 #pragma unroll
-    for (int cc = 0; cc < NC; ++cc) sv[cc] = sclw[cc * kG7Warps];
+    for (int cc = 0; cc < NC; ++cc) sv1[cc] = scl[cc * nb + w];
 
     for (int t = 0; t < ntiles; ++t) {
         const int b = t & 1;
         const uint32_t ph = (uint32_t)((t >> 1) & 1);
-        if (!mbar_wait_bounded(full + b, ph, p.fault)) return;                          // the tile landed
-        if (t >= kG7RSlots && !mbar_wait_bounded(vfree + b, ph ^ 1u, p.fault)) return;  // tile t-2 folded
-        const int n = min(kG7RTile, count - t * kG7RTile);
-        float *vb = reinterpret_cast<float *>(smem + Lo.vals + b * kVBuf);
+        const int rt = t / nch, k = t - rt * nch;
+        const int blk = k * NW + w;
+        if (!mbar_wait_bounded(full + b, ph, p.fault)) return;              // the tile landed
+        if (t >= 2 && !mbar_wait_bounded(vfree + b, ph ^ 1u, p.fault)) return;  // tile t-2 folded
+        const int n = min(kG7RTile, count - rt * kG7RTile);
+        float *vb = reinterpret_cast<float *>(smem + Lo.vals + b * Lo.vbuf);
         if (lane < n) {
-            const uint8_t *row = slab + b * (kG7RTile * p.pitch) + lane * p.pitch;
+            const uint8_t *row = slab + b * (kG7RTile * pitch) + lane * pitch + 144 * w;
             int C[NC], O[NC];
             uint32_t dd;
-            block_q4k_cols<NC, kG7RUnr>(row + 144 * w, aw, kG7K, Sw, kG7Warps * 16, C, O, dd);
+            block_q4k_cols<NC, kG7RUnr>(row, act + 256 * blk, K, sums + blk * 16, nb * 16, C, O, dd);
 #pragma unroll
-            for (int cc = 0; cc < NC; ++cc)
-                vb[lane * VS + cc * 17 + w] = lane_value_fast<1>(C[cc] >> 4, O[cc], dd & 0xFFFFu, dd >> 16,
-                                                                 (int)(sv[cc] & 0xFFu), (int)(int16_t)(sv[cc] >> 16));
+            for (int cc = 0; cc < NC; ++cc) {
+                const uint32_t sv = NCH == 1 ? sv1[cc] : scl[cc * nb + blk];
+                vb[lane * VS + cc * (NW + 1) + w] = lane_value_fast<1>(C[cc] >> 4, O[cc], dd & 0xFFFFu, dd >> 16,
+                                                                       (int)(sv & 0xFFu), (int)(int16_t)(sv >> 16));
+            }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(done + b);
     }
 }
 
-// NC columns (2..4) of a Q4_K-like matrix (or a table of them) at K = 4096,
-// more than kG7MaxRows rows a CTA.  QB_E_ARG when the shape does not fit.
-template <int NC>
-int launch_gemv7r(const GemvArgs &a, cudaStream_t stream, const float *x) {
-    if (a.ncols != NC || a.mode != 0 || a.K != kG7K) return QB_E_ARG;
+// The ring form for NC columns (2..4) of a Q4_K-like matrix (or a table of
+// them) at K = 256 * NW * NCH; QB_E_ARG when the shape does not fit.
+// min_rows: take it only past this many rows a CTA.
+template <int NC, int NW, int NCH>
+int launch_gemv7r(const GemvArgs &a, cudaStream_t stream, const float *x, int64_t min_rows) {
+    if (a.ncols != NC || a.mode != 0 || a.K != 256 * NW * NCH) return QB_E_ARG;
     Gemv7K k;
     k.mt = a.mats ? *a.mats : single_table(a.W, a.rows, a.out);
     k.rows = k.mt.start[k.mt.n];
     if (k.rows < 1) return QB_E_ARG;
     const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(num_sms(), k.rows));
     const int64_t per_cta = (k.rows + grid - 1) / grid;
-    if (per_cta <= kG7MaxRows) return QB_E_ARG;
-    k.rec = (int)record_bytes(kQ4K, kG7K);
-    k.pitch = k.rec + 16;
-    const int smem = gemv7r_layout(NC, k.pitch).total;
+    if (per_cta <= min_rows) return QB_E_ARG;
+    k.rec = (int)record_bytes(kQ4K, a.K);
+    k.pitch = NW * 144 + 16;  // a row's chunk, offset by 16 B a row: the lanes of a phase in distinct banks
+    const int smem = gemv7r_layout(NC, (int)a.K, NW, k.pitch).total;
     if (smem > 227 * 1024) return QB_E_ARG;
     k.base = k.rows / grid;
     k.rem = k.rows % grid;
@@ -749,9 +770,29 @@ int launch_gemv7r(const GemvArgs &a, cudaStream_t stream, const float *x) {
     k.x = x;
     k.fault = fault_word();
     if (!k.fault) return QB_E_CUDA;
-    auto kern = x ? gemv7r_kernel<true, NC> : gemv7r_kernel<false, NC>;
+    auto kern = x ? gemv7r_kernel<true, NC, NW, NCH> : gemv7r_kernel<false, NC, NW, NCH>;
     if (ensure_smem_limit(reinterpret_cast<const void *>(kern), smem) != QB_OK) return QB_E_CUDA;
-    return launch_pdl(kern, dim3(grid), dim3(kG7RThreads), (size_t)smem, stream, k);
+    return launch_pdl(kern, dim3(grid), dim3((NW + 1) * 32), (size_t)smem, stream, k, k.pitch);
+}
+
+// The ring form for a.ncols (2..4) columns at K = 4096 (one chunk of 16
+// blocks), 8192 (two) or 14336 (four chunks of 14).
+template <int NC>
+int launch_gemv7r_k(const GemvArgs &a, cudaStream_t stream, const float *x, int64_t min_rows) {
+    switch (a.K) {
+    case 4096: return launch_gemv7r<NC, 16, 1>(a, stream, x, min_rows);
+    case 8192: return launch_gemv7r<NC, 16, 2>(a, stream, x, min_rows);
+    case 14336: return launch_gemv7r<NC, 14, 4>(a, stream, x, min_rows);
+    default: return QB_E_ARG;
+    }
+}
+inline int launch_gemv7r_cols(const GemvArgs &a, cudaStream_t stream, const float *x, int64_t min_rows) {
+    switch (a.ncols) {
+    case 2: return launch_gemv7r_k<2>(a, stream, x, min_rows);
+    case 3: return launch_gemv7r_k<3>(a, stream, x, min_rows);
+    case 4: return launch_gemv7r_k<4>(a, stream, x, min_rows);
+    default: return QB_E_ARG;
+    }
 }
 
 // 2..4 columns at K = 4096 (the multi-column form above); QB_E_ARG where it
@@ -767,11 +808,8 @@ int launch_gemv7_cols(const GemvArgs &a, cudaStream_t stream, const float *x) {
     default: return QB_E_ARG;
     }
     if (r != QB_E_ARG || F != kQ4K) return r;
-    switch (a.ncols) {  // more rows a CTA: the ring form
-    case 2: return launch_gemv7r<2>(a, stream, x);
-    case 3: return launch_gemv7r<3>(a, stream, x);
-    default: return launch_gemv7r<4>(a, stream, x);
-    }
+    // more rows a CTA (K = 4096), or a longer K: the ring form
+    return launch_gemv7r_cols(a, stream, x, a.K == kG7K ? kG7MaxRows : 0);
 }
 
 }  // namespace qb

@@ -559,16 +559,20 @@ def test_k4096_row_ranges(fmt, ncols, rows):
     assert np.array_equal(bits(host(out)), bits(want))
 
 
-@pytest.mark.parametrize("ncols", [2, 3, 4])
-@pytest.mark.parametrize("rows", [152 * 65, 152 * 189 + 17, 152 * 96 - 5])
-def test_k4096_many_rows_ring(ncols, rows):
-    """2..4 columns at K = 4096 past 64 rows a CTA: rows streaming through
-    the two-slot ring of 32-row tiles (full tiles, a ragged last one, CTAs
-    with one row more than others), from codes and from x; and the same
+_RING_CASES = [(n, r, 4096) for n in (2, 3, 4) for r in (152 * 65, 152 * 189 + 17, 152 * 96 - 5)] + \
+              [(n, r, K) for n in (2, 3, 4) for r, K in ((4096, 14336), (152 * 33 + 7, 14336), (300, 8192))]
+
+
+@pytest.mark.parametrize("ncols,rows,K", _RING_CASES)
+def test_ring_rows_and_chunks(ncols, rows, K):
+    """Q4_K-like through the ring form: 2..4 columns at K = 4096 past 64 rows
+    a CTA, and at longer K (chunks of 14 or 16 blocks a tile,
+    the fold carried across a row's chunks): full tiles, a ragged last one,
+    CTAs with one row more than others; from codes and from x; and the same
     rows as a table of three matrices sharing the activation."""
     import torch
-    fmt, K = synth.FMT_Q4K, 4096
-    rng = np.random.default_rng(rows + ncols)
+    fmt = synth.FMT_Q4K
+    rng = np.random.default_rng(rows + ncols + K)
     lg = synth.draw(fmt, rng, rows, K)
     W = synth.pack(fmt, lg)
     x = synth.draw_act(rng, ncols, K, outlier_frac=0.001)
