@@ -48,6 +48,8 @@ WORKLOADS = {
     "q6k_14336x4096": (synth.FMT_Q6K, 14336, 4096, 1, 2, 0.0, "Q6_K-like FFN gate 14336x4096, batch 1"),
     "f16_49152x576": (synth.FMT_F16, 49152, 576, 1, 3, 0.0, "F16 tied-embedding logits 49152x576, batch 1"),
     "q4k_4096x4096_b16": (synth.FMT_Q4K, 4096, 4096, 16, 1, 0.001, "Q4_K-like GEMV 4096x4096, 16 columns"),
+    "q4k_28672x4096_b4": (synth.FMT_Q4K, 28672, 4096, 4, 1, 0.001,
+                          "Q4_K-like FFN gate+up 28672x4096, 4 columns"),
     # ActScaling::Sub32: activation scales per 32 elements, one rounding per 256-element group
     "q4k_4096x4096_sub32": (synth.FMT_Q4K, 4096, 4096, 1, 1, 0.001,
                             "Q4_K-like GEMV 4096x4096, batch 1, activation scaled per 32 (Sub32)"),
@@ -392,6 +394,31 @@ def tc_applies(fmt, K, ncols):
     return False
 
 
+def multi_col_kernel(fmt, rows, K, ncols):
+    """The library's choice of product kernel for 2..16 columns (Q4_K-like /
+    Q6_K-like): the tensor-core kernel from TC_MIN_COLS columns; at 2..4
+    columns and K = 4096 the warp-per-block kernel while a CTA's rows (at
+    most 64) fit its shared memory, else (Q4_K-like) its ring form, which also
+    takes K = 8192 and 14336; the dp4a CTA-ring kernel otherwise."""
+    if tc_applies(fmt, K, ncols):
+        return f"tc_kernel<{synth.FORMAT_NAMES[fmt]}, {ncols} columns> (tcgen05 f16 MMAs, accumulators in tensor memory)"
+    g = max(1, min(152, rows))
+    per = (rows + g - 1) // g
+    if 2 <= ncols <= 4 and K == 4096 and per <= 64:
+        pitch = synth.weight_bytes(fmt, 1, K) + 16
+        vs = (ncols * 17) | 1
+        smem = (128 + (ncols * 64 + 127) // 128 * 128 + ncols * 4096 + ncols * 512 + (64 * vs * 4 + 127) // 128 * 128 +
+                per * pitch)
+        minb = 1 if ncols >= 3 and per > 32 else 2
+        if smem <= (228 * 1024) // minb - 1280:
+            return (f"gemv7m_kernel<{synth.FORMAT_NAMES[fmt]}, {ncols} columns, a warp per block, a lane per row, "
+                    f"{minb} CTA(s) a SM>")
+    if fmt == synth.FMT_Q4K and 2 <= ncols <= 4 and K in (4096, 8192, 14336) and (K != 4096 or per > 64):
+        return (f"gemv7r_kernel<q4k, {ncols} columns, ring of 32-row tiles, a warp per block, a lane per row, "
+                f"producer warp>")
+    return f"gemv3_kernel<{synth.FORMAT_NAMES[fmt]}, {ncols} columns>"
+
+
 def roofline(fmt, ncols, single, achieved, peak, peak_kind, traffic, roof_bytes, per_launch_s, prod_s, abytes,
              ops_per_step, roof_launches, sub32=False, rows=0, K=0):
     g7 = ncols == 1 and not sub32 and fmt != synth.FMT_F16 and one_col_gemv7(fmt, rows, K)
@@ -408,10 +435,8 @@ def roofline(fmt, ncols, single, achieved, peak, peak_kind, traffic, roof_bytes,
              else f"s32_kernel<{synth.FORMAT_NAMES[fmt]}, {min(ncols, 2)} column(s) a thread group>") if sub32 else
             f"gemv3_kernel<{synth.FORMAT_NAMES[fmt]}, one column, single launch> (quantize + product)"
             if single and g3 else
-            f"gemv2_kernel<{synth.FORMAT_NAMES[fmt]}, single launch> (quantize + product)" if single else
-            f"tc_kernel<{synth.FORMAT_NAMES[fmt]}, {ncols} columns> (tcgen05 f16 MMAs, accumulators in tensor memory)"
-            if tc_applies(fmt, K, ncols) else
-            f"gemv3_kernel<{synth.FORMAT_NAMES[fmt]}, {ncols} columns>")
+            f"gemv2_kernel<{synth.FORMAT_NAMES[fmt]}, single launch> (quantize + product)" if single and ncols == 1
+            else multi_col_kernel(fmt, rows, K, ncols))
     prod = {"avg_launch_us": round(prod_s * 1e6, 4),
             "achieved_gbs": round(abytes / prod_s / 1e9, 1),
             "frac_of_hbm": round(abytes / prod_s / 1e9 / peak, 4),
@@ -788,7 +813,10 @@ def run_ours(args, rank, world):
     # Q4_K-like rows of K >= 12288 given a workspace take quantize + product)
     single = ((fmt != synth.FMT_F16 and ncols == 1 and K % 256 == 0 and
                (sub32 or not (fmt == synth.FMT_Q4K and K >= 12288))) or
-              (fmt == synth.FMT_F16 and ncols * K * 4 <= 227 * 1024))
+              (fmt == synth.FMT_F16 and ncols * K * 4 <= 227 * 1024) or
+              # 2..4 columns at K = 4096: the warp-per-block kernel or its ring form from x
+              (not sub32 and 2 <= ncols <= 4 and K == 4096 and
+               multi_col_kernel(fmt, rows, K, ncols).startswith(("gemv7m", "gemv7r"))))
     launches_per_step = 1 if single else 2
     stream = torch.cuda.Stream(dev)
 

@@ -800,11 +800,15 @@ inline int launch_gemv7r_cols(const GemvArgs &a, cudaStream_t stream, const floa
 template <int F>
 int launch_gemv7_cols(const GemvArgs &a, cudaStream_t stream, const float *x) {
     constexpr int U = F == kQ4K ? 2 : 4;
+    // 3..4 columns past 32 rows a CTA: one CTA a SM (twice the registers) beat
+    // two (Q4_K-like 6144 x 4096 at 4 columns: 8.24 -> 7.68 us)
+    const int64_t g = std::max<int64_t>(1, std::min<int64_t>(num_sms(), a.mats ? a.mats->start[a.mats->n] : a.rows));
+    const bool one = ((a.mats ? a.mats->start[a.mats->n] : a.rows) + g - 1) / g > 32;
     int r = QB_E_ARG;
     switch (a.ncols) {
     case 2: r = launch_gemv7m<F, 2, U, 2>(a, stream, x); break;
-    case 3: r = launch_gemv7m<F, 2, U, 3>(a, stream, x); break;
-    case 4: r = launch_gemv7m<F, 2, U, 4>(a, stream, x); break;
+    case 3: r = one ? launch_gemv7m<F, 1, U, 3>(a, stream, x) : launch_gemv7m<F, 2, U, 3>(a, stream, x); break;
+    case 4: r = one ? launch_gemv7m<F, 1, U, 4>(a, stream, x) : launch_gemv7m<F, 2, U, 4>(a, stream, x); break;
     default: return QB_E_ARG;
     }
     if (r != QB_E_ARG || F != kQ4K) return r;
