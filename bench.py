@@ -1464,8 +1464,9 @@ def run_stack(args, rank, world):
         "frac_of_8tbs": round(value / 8000.0, 4), "frac_of_measured_copy": round(value / peak, 4),
         "gpu_launches": nrep * G * launches_step, "clocks": clocks,
         "roofline": {"bound": "hbm" if ncols == 1 else "alu", "kernel": "the step's 129 products (one-column "
-                     "streaming kernels at 1 column; the warp-per-block and dp4a kernels at 4; the tcgen05 "
-                     "tensor-core kernel at 16, the dp4a kernel for the K = 14336 down projection)",
+                     "streaming kernels at 1 column; at 4 the warp-per-block kernel for QKV and O, its ring form "
+                     "for gate+up and the K = 14336 down projection, the dp4a kernel for the Q6_K-like output; "
+                     "the tcgen05 tensor-core kernel at 16, the dp4a kernel for the down projection)",
                      "achieved": round(value, 1) if ncols == 1 else round(ops / step_s / 1e12, 2),
                      "peak": peak if ncols == 1 else round(DP4A_PEAK_TOPS, 1),
                      "peak_kind": f"{peak_kind} (HBM copy, burst)" if ncols == 1 else
