@@ -931,8 +931,10 @@ def run_ours(args, rank, world):
     wsh = torch.empty(qb.q_matvec_host_workspace_bytes(scaling, fmt, rows, K, ncols), dtype=torch.uint8, device=dev)
     n_e2e = min(args.steps, 3000)
 
+    Wv = [W[j] for j in range(ncopy)]  # the rotating copies as tensors (indexing them is the bench's, not the call's)
+
     def host_step(i):
-        qb.q_matvec_host(fmt, W[i % ncopy], rows, K, xh, oh, wsh, scaling=scaling, stream=stream)
+        qb.q_matvec_host(fmt, Wv[i % ncopy], rows, K, xh, oh, wsh, scaling=scaling, stream=stream)
 
     for i in range(5):
         host_step(i)

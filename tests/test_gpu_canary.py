@@ -6,8 +6,9 @@ set to a canary pattern; after each call the canary bytes on both sides must
 be intact, and the outputs must equal those of the same call on plain
 buffers.  The calls and shapes are those of the parity tests: the one-column
 kernels (warp rings, the one-column gemv3 form for long rows, Q8_0's), two
-launches through a workspace, the grouped launch, 16 columns, Sub32, F16,
-FP8 and the score kernel.
+launches through a workspace, 2..4 columns (the warp-per-block kernel and its
+ring form), the grouped launch, 16 columns, Sub32, F16, FP8 and the score
+kernel.
 """
 import numpy as np
 import pytest
@@ -67,7 +68,8 @@ def _plain(shape):
 @pytest.mark.parametrize("fmt", [synth.FMT_Q8_0, synth.FMT_Q4K, synth.FMT_Q6K])
 @pytest.mark.parametrize("rows,K,ncols,use_ws", [(4096, 4096, 1, False), (1200, 14336, 1, False),
                                                  (1200, 14336, 1, True), (261, 4096, 3, True),
-                                                 (1000, 1024, 3, True)])
+                                                 (1000, 1024, 3, True), (152 * 65 + 3, 4096, 4, True),
+                                                 (1200, 14336, 3, True)])
 def test_matvec_writes_only_its_outputs(fmt, rows, K, ncols, use_ws):
     import torch
     rng = np.random.default_rng(rows + K + ncols + fmt)
