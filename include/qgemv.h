@@ -167,9 +167,11 @@ QB_API int64_t q_matvec_workspace_bytes(qb_fmt fmt, int64_t K, int ncols);
 /* The whole product from an f32 activation: quantize_act (or
  * quantize_act_f16) then q_gemv (or q_gemv_f16), out[c*rows + r], bit for bit
  * the same results.  For one column of a Q8_0/Q4_K/Q6_K matrix with
- * K % 256 == 0, for 2..4 columns of a Q4_K/Q6_K matrix at K = 4096 whose rows
- * fit the multi-column kernel's shared memory (up to about 45 Q4_K or 31 Q6_K
- * rows per SM), and for F16 with ncols * K * 4 <= 227 KB (rows short enough
+ * K % 256 == 0, for 2..4 columns of a Q4_K/Q6_K matrix at K = 4096 that the
+ * multi-column kernels take (Q4_K: every row count at 3..4 columns, and at
+ * 2 columns up to 40 or past 64 rows per SM; Q6_K: up to about 22..28 rows
+ * per SM, and 33..57 at 3..4 columns), and for F16 with
+ * ncols * K * 4 <= 227 KB (rows short enough
  * for the F16 kernel's rings), it is a single launch that quantizes (or
  * rounds) the activation inside the product kernel and needs no workspace
  * (`workspace` may be NULL; a Q4_K matrix with K >= 12288 given a workspace
