@@ -48,6 +48,7 @@ WORKLOADS = {
     "q6k_14336x4096": (synth.FMT_Q6K, 14336, 4096, 1, 2, 0.0, "Q6_K-like FFN gate 14336x4096, batch 1"),
     "f16_49152x576": (synth.FMT_F16, 49152, 576, 1, 3, 0.0, "F16 tied-embedding logits 49152x576, batch 1"),
     "q4k_4096x4096_b16": (synth.FMT_Q4K, 4096, 4096, 16, 1, 0.001, "Q4_K-like GEMV 4096x4096, 16 columns"),
+    "q4k_4096x4096_b4": (synth.FMT_Q4K, 4096, 4096, 4, 1, 0.001, "Q4_K-like GEMV 4096x4096, 4 columns"),
     "q4k_28672x4096_b4": (synth.FMT_Q4K, 28672, 4096, 4, 1, 0.001,
                           "Q4_K-like FFN gate+up 28672x4096, 4 columns"),
     # ActScaling::Sub32: activation scales per 32 elements, one rounding per 256-element group
