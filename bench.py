@@ -1368,10 +1368,18 @@ def run_stack(args, rank, world):
     wsb = max(qb.q_matvec_workspace_bytes(f, k, ncols) for _, f, _, k in STACK_MATS + [STACK_OUT])
     ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
     stream = torch.cuda.Stream(dev)
-    # q_matvec launches a call: one for a single column, except Q4_K-like at
-    # K >= 12288 given a workspace (quantize, then the product), two otherwise
-    calls = [(f, k) for _, f, _, k in STACK_MATS] * STACK_LAYERS + [(STACK_OUT[1], STACK_OUT[3])]
-    launches_step = sum(1 if ncols == 1 and not (f == synth.FMT_Q4K and k >= 12288) else 2 for f, k in calls)
+    # q_matvec launches a call: one for a single column (except Q4_K-like at
+    # K >= 12288 given a workspace: quantize, then the product) and for 2..4
+    # columns at K = 4096 where the warp-per-block kernels take the rows, two
+    # otherwise
+    calls = [(f, r, k) for _, f, r, k in STACK_MATS] * STACK_LAYERS + [(STACK_OUT[1], STACK_OUT[2], STACK_OUT[3])]
+
+    def one_launch(f, r, k):
+        if ncols == 1:
+            return not (f == synth.FMT_Q4K and k >= 12288)
+        return 2 <= ncols <= 4 and k == 4096 and multi_col_kernel(f, r, k, ncols).startswith(("gemv7m", "gemv7r"))
+
+    launches_step = sum(1 if one_launch(f, r, k) else 2 for f, r, k in calls)
 
     def step(i, s):
         for layer in range(STACK_LAYERS):
